@@ -1,0 +1,297 @@
+/*
+ * kd_oracle.c -- plain, slow CPU reference of one batched decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  The product
+ * path (the CUDA library) shares no code, header, table or helper with it.
+ *
+ * What it computes follows the batched decode step of memra-engine's
+ * `decode_batch.rs` (module header "EXACTNESS CONTRACT"; `decode_batch_layers`,
+ * the per-layer body; `decode_step_batch_lean_masked`, embedding and head;
+ * `decode_batch_epilogue`, the device argmax), restricted to a dense
+ * Llama-shaped model: no QK-norm, no output gate, no linear-attention or MoE
+ * layers.  Batching changes no arithmetic ("row-parallel ops batch trivially";
+ * every projection row is bit-identical to its m=1 result), so the oracle is
+ * the plain single-session step, run once per session.
+ *
+ * All arithmetic is fp64.  Only the method's storage roundings are mirrored:
+ *   - matmul inputs (normed activations, attention output, SwiGLU output) are
+ *     rounded to fp16, the KV cache is fp16, the residual stream and the
+ *     logits are fp32.
+ * Conventions the pages leave open (each is listed with its reason in the
+ * design notes): Q8_0 blocks run along the input dimension; RoPE is the NeoX
+ * rotate-half form over the whole head; q head h reads KV head
+ * h / (n_heads / n_kv_heads); the attention scale is 1/sqrt(head_dim); the new
+ * token is written at its position p and attends keys 0..p; argmax ties go
+ * to the lowest index and NaN never wins.
+ *
+ * No blocking, fusion or reordering: every dot product runs over its blocks in
+ * order; OpenMP only spreads independent output rows or heads over threads,
+ * so the results do not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KDO_EXPORT __attribute__((visibility("default")))
+
+/* ---------------------------------------------------------------------------
+ * IEEE 754 binary16 <-> binary64, written from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 holds
+ * the subnormals (fraction * 2^-24), exponent 31 holds Inf and NaN.
+ * ------------------------------------------------------------------------- */
+KDO_EXPORT double kdo_half_to_double(uint16_t h) {
+    int sign = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp((double)(f + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+/* Round to nearest, ties to even (nearbyint in the default rounding mode). */
+KDO_EXPORT uint16_t kdo_double_to_half(double x) {
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return 0x7e00;
+    if (isinf(x)) return sign | 0x7c00;
+    double a = fabs(x);
+    if (a < ldexp(1.0, -14)) {                 /* subnormal range: units of 2^-24 */
+        double r = nearbyint(a * 16777216.0);  /* exact scaling, one rounding */
+        return sign | (uint16_t)r;             /* r == 1024 is the smallest normal */
+    }
+    int e;
+    double f = frexp(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+    double r = nearbyint(ldexp(f, 11));        /* 11 significant bits: [1024, 2048] */
+    if (r == 2048.0) { r = 1024.0; e += 1; }
+    int be = e - 1 + 15;
+    if (be >= 31) return sign | 0x7c00;        /* overflow rounds to infinity */
+    return sign | (uint16_t)(be << 10) | (uint16_t)((int)r - 1024);
+}
+
+static double round_half(double x) { return kdo_half_to_double(kdo_double_to_half(x)); }
+static double round_float(double x) { return (double)(float)x; }
+
+/* ---------------------------------------------------------------------------
+ * Q8_0: one block = fp16 scale d then 32 int8 quants q_j; value_j = q_j * d.
+ * (Named as the weight format on memra's and hf2q's pages; the closed form is
+ * value = int8 x fp16 scale per 32-element block.)
+ * ------------------------------------------------------------------------- */
+#define QK 32
+#define QB 34
+
+static double q8_scale(const uint8_t* blk) {
+    uint16_t h = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
+    return kdo_half_to_double(h);
+}
+
+/* Dequantise one row of `cols` values (cols a multiple of 32). */
+KDO_EXPORT void kdo_q8_0_dequant_row(const uint8_t* row, int32_t cols, double* out) {
+    for (int b = 0; b < cols / QK; ++b) {
+        const uint8_t* blk = row + (size_t)b * QB;
+        double d = q8_scale(blk);
+        for (int j = 0; j < QK; ++j) out[b * QK + j] = (double)(int8_t)blk[2 + j] * d;
+    }
+}
+
+/* y[r] = sum over blocks b of d_rb * sum_j q_rbj * x[32b + j]  (W is [rows][cols/32] blocks).
+ * This is the projection `matmul(W, x)` of the layer body, one input vector. */
+KDO_EXPORT void kdo_matvec_q8_0(const uint8_t* W, int32_t rows, int32_t cols,
+                                const double* x, double* y) {
+    const size_t row_bytes = (size_t)(cols / QK) * QB;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        const uint8_t* row = W + (size_t)r * row_bytes;
+        double acc = 0.0;
+        for (int b = 0; b < cols / QK; ++b) {
+            const uint8_t* blk = row + (size_t)b * QB;
+            double s = 0.0;
+            for (int j = 0; j < QK; ++j) s += (double)(int8_t)blk[2 + j] * x[b * QK + j];
+            acc += q8_scale(blk) * s;
+        }
+        y[r] = acc;
+    }
+}
+
+/* RMSNorm then fp16 rounding: out_i = fp16(x_i / sqrt(mean(x^2) + eps) * w_i).
+ * (`rms_norm(x, w, out, n_embd, rows, eps)` of the layer body.) */
+KDO_EXPORT void kdo_rmsnorm_f16(const double* x, const float* w, int32_t n, double eps,
+                                double* out) {
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    double r = 1.0 / sqrt(ss / n + eps);
+    for (int i = 0; i < n; ++i) out[i] = round_half(x[i] * r * (double)w[i]);
+}
+
+/* NeoX rotate-half RoPE of one head vector u[hd] at position pos:
+ * for i < hd/2, with w_i = theta^(-2i/hd) and a = pos * w_i,
+ * (u_i, u_{i+hd/2}) <- (u_i cos a - u_{i+hd/2} sin a, u_i sin a + u_{i+hd/2} cos a).
+ * (`rope_neox(x, pos_d, head_dim, rope_dims, n_heads, B, base, 1.0)`, each row at its own position.) */
+KDO_EXPORT void kdo_rope_neox(double* u, int32_t hd, int32_t pos, double theta) {
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double a = (double)pos * pow(theta, -2.0 * i / hd);
+        double c = cos(a), s = sin(a);
+        double x0 = u[i], x1 = u[i + half];
+        u[i] = x0 * c - x1 * s;
+        u[i + half] = x0 * s + x1 * c;
+    }
+}
+
+/* Single-head attention over t_kv cached rows, two-pass softmax:
+ * s_t = scale * q . K_t ; m = max_t s_t ; a = sum_t exp(s_t - m) V_t / sum_t exp(s_t - m).
+ * K, V are fp16 bits with row stride `stride` elements. */
+KDO_EXPORT void kdo_attention_head(const double* q, const uint16_t* K, const uint16_t* V,
+                                   int32_t t_kv, int32_t hd, int64_t stride, double scale,
+                                   double* out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(t_kv > 0 ? t_kv : 1));
+    double m = -INFINITY;
+    for (int t = 0; t < t_kv; ++t) {
+        double dot = 0.0;
+        for (int i = 0; i < hd; ++i) dot += q[i] * kdo_half_to_double(K[(size_t)t * stride + i]);
+        s[t] = dot * scale;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int t = 0; t < t_kv; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+    for (int i = 0; i < hd; ++i) {
+        double acc = 0.0;
+        for (int t = 0; t < t_kv; ++t) acc += s[t] * kdo_half_to_double(V[(size_t)t * stride + i]);
+        out[i] = acc / l;
+    }
+    free(s);
+}
+
+/* silu(y) = y / (1 + e^-y). (`silu_mul(g, u, act, n)` computes silu(g) * u.) */
+KDO_EXPORT double kdo_silu(double y) { return y / (1.0 + exp(-y)); }
+
+/* Greedy pick: the largest value, ties to the lowest index, NaN never wins;
+ * a row with no non-NaN value gives -1.  (`argmax_token_device_col`.) */
+KDO_EXPORT int32_t kdo_argmax_f32(const float* v, int32_t n) {
+    int32_t best = -1;
+    for (int32_t i = 0; i < n; ++i) {
+        if (isnan(v[i])) continue;
+        if (best < 0 || v[i] > v[best]) best = i;
+    }
+    return best;
+}
+
+/* ---------------------------------------------------------------------------
+ * The model and one decode step.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+    double rope_theta, rms_eps;
+} kdo_config;
+
+typedef struct {
+    const uint8_t* tok_embd;          /* Q8_0 [vocab][hidden/32] */
+    const uint8_t* output;            /* Q8_0 [vocab][hidden/32] (lm_head) */
+    const float* output_norm;         /* [hidden] */
+    const uint8_t* const* wq;         /* per layer, Q8_0 [n_heads*hd][hidden/32] */
+    const uint8_t* const* wk;         /* [n_kv*hd][hidden/32] */
+    const uint8_t* const* wv;         /* [n_kv*hd][hidden/32] */
+    const uint8_t* const* wo;         /* [hidden][n_heads*hd/32] */
+    const uint8_t* const* w_gate;     /* [ffn][hidden/32] */
+    const uint8_t* const* w_up;       /* [ffn][hidden/32] */
+    const uint8_t* const* w_down;     /* [hidden][ffn/32] */
+    const float* const* attn_norm;    /* [hidden] */
+    const float* const* ffn_norm;     /* [hidden] */
+} kdo_weights;
+
+/* One session, one step.  k_cache / v_cache are the session's fp16 caches,
+ * [n_layers][n_kv][cap][hd]; rows 0..pos-1 hold its history, row `pos` is
+ * overwritten with this step's key/value, rows beyond pos are never read.
+ * logits: [vocab] fp32.  hidden: NULL or [n_layers+1][hidden] fp32, the residual
+ * after the embedding and after every layer. */
+KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
+                                    int32_t token, int32_t pos,
+                                    uint16_t* k_cache, uint16_t* v_cache, int32_t cap,
+                                    float* logits, float* hidden) {
+    const int H = c->hidden, nh = c->n_heads, nkv = c->n_kv_heads, hd = c->head_dim;
+    const int F = c->ffn, V = c->vocab, L = c->n_layers;
+    if (token < 0 || token >= V || pos < 0 || pos >= cap || nh % nkv || hd % 2) return -1;
+    const int group = nh / nkv;
+    const double scale = 1.0 / sqrt((double)hd);
+
+    double* x = malloc(sizeof(double) * H);
+    double* xn = malloc(sizeof(double) * H);
+    double* q = malloc(sizeof(double) * nh * hd);
+    double* k = malloc(sizeof(double) * nkv * hd);
+    double* v = malloc(sizeof(double) * nkv * hd);
+    double* att = malloc(sizeof(double) * nh * hd);
+    double* o = malloc(sizeof(double) * H);
+    double* g = malloc(sizeof(double) * F);
+    double* u = malloc(sizeof(double) * F);
+    double* act = malloc(sizeof(double) * F);
+    double* lg = malloc(sizeof(double) * V);
+
+    /* Embedding: the token's Q8_0 row, dequantised (exact in fp32). */
+    kdo_q8_0_dequant_row(w->tok_embd + (size_t)token * (H / QK) * QB, H, x);
+    for (int i = 0; i < H; ++i) x[i] = round_float(x[i]);
+    if (hidden) for (int i = 0; i < H; ++i) hidden[i] = (float)x[i];
+
+    for (int l = 0; l < L; ++l) {
+        uint16_t* Kl = k_cache + (size_t)l * nkv * cap * hd;
+        uint16_t* Vl = v_cache + (size_t)l * nkv * cap * hd;
+        /* attn_norm, then the q/k/v projections of the fp16 normed row. */
+        kdo_rmsnorm_f16(x, w->attn_norm[l], H, c->rms_eps, xn);
+        kdo_matvec_q8_0(w->wq[l], nh * hd, H, xn, q);
+        kdo_matvec_q8_0(w->wk[l], nkv * hd, H, xn, k);
+        kdo_matvec_q8_0(w->wv[l], nkv * hd, H, xn, v);
+        /* RoPE of q and k at this session's own position. */
+        for (int h = 0; h < nh; ++h) kdo_rope_neox(q + h * hd, hd, pos, c->rope_theta);
+        for (int h = 0; h < nkv; ++h) kdo_rope_neox(k + h * hd, hd, pos, c->rope_theta);
+        /* KV append: row `pos` of this session's cache, stored as fp16. */
+        for (int h = 0; h < nkv; ++h)
+            for (int i = 0; i < hd; ++i) {
+                Kl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(k[h * hd + i]);
+                Vl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(v[h * hd + i]);
+            }
+        /* Attention over keys 0..pos (t_kv = pos + 1), GQA head mapping h -> h / group. */
+#pragma omp parallel for schedule(static)
+        for (int h = 0; h < nh; ++h) {
+            int kh = h / group;
+            kdo_attention_head(q + h * hd, Kl + (size_t)kh * cap * hd, Vl + (size_t)kh * cap * hd,
+                               pos + 1, hd, hd, scale, att + h * hd);
+        }
+        for (int i = 0; i < nh * hd; ++i) att[i] = round_half(att[i]);
+        /* o-projection and residual add (fp32 residual). */
+        kdo_matvec_q8_0(w->wo[l], H, nh * hd, att, o);
+        for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
+        /* ffn_norm, SwiGLU, down-projection, residual add. */
+        kdo_rmsnorm_f16(x, w->ffn_norm[l], H, c->rms_eps, xn);
+        kdo_matvec_q8_0(w->w_gate[l], F, H, xn, g);
+        kdo_matvec_q8_0(w->w_up[l], F, H, xn, u);
+        for (int i = 0; i < F; ++i) act[i] = round_half(kdo_silu(g[i]) * u[i]);
+        kdo_matvec_q8_0(w->w_down[l], H, F, act, o);
+        for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
+        if (hidden) for (int i = 0; i < H; ++i) hidden[(size_t)(l + 1) * H + i] = (float)x[i];
+    }
+    /* Head: output_norm, lm_head, fp32 logits. */
+    kdo_rmsnorm_f16(x, w->output_norm, H, c->rms_eps, xn);
+    kdo_matvec_q8_0(w->output, V, H, xn, lg);
+    for (int i = 0; i < V; ++i) logits[i] = (float)lg[i];
+
+    free(x); free(xn); free(q); free(k); free(v); free(att); free(o);
+    free(g); free(u); free(act); free(lg);
+    return 0;
+}
+
+/* B sessions, one step each: the batched step is B independent single-session
+ * steps (the exactness contract).  Per-session arrays: k_caches[b], v_caches[b].
+ * logits [B][vocab]; hidden NULL or [B][n_layers+1][hidden]; argmax [B]. */
+KDO_EXPORT int32_t kdo_decode_step(const kdo_config* c, const kdo_weights* w, int32_t B,
+                                   const int32_t* tokens, const int32_t* positions,
+                                   uint16_t* const* k_caches, uint16_t* const* v_caches,
+                                   int32_t cap, float* logits, float* hidden, int32_t* argmax) {
+    for (int b = 0; b < B; ++b) {
+        float* lg = logits + (size_t)b * c->vocab;
+        float* hb = hidden ? hidden + (size_t)b * (c->n_layers + 1) * c->hidden : NULL;
+        int32_t rc = kdo_session_step(c, w, tokens[b], positions[b], k_caches[b], v_caches[b],
+                                      cap, lg, hb);
+        if (rc) return rc;
+        if (argmax) argmax[b] = kdo_argmax_f32(lg, c->vocab);
+    }
+    return 0;
+}
