@@ -1,0 +1,398 @@
+"""Throughput of the batched multi-session decode step on GB300.
+
+Workload (default): the Llama-3-8B-shaped dense model with random Q8_0 weights
+(32 layers, hidden 4096, 32/8 heads of 128, FFN 14336, vocab 128256), B = 8
+sessions, each slot pre-filled with 1238 random fp16 positions; every step
+decodes one token per session at positions 1238 .. 1365 (cycling), so the
+attended lengths stay within the 128-step decode window of the workload.
+
+Prints ONE JSON line (rank 0): aggregate decode tok/s (`value`, inputs resident
+on the device, steps issued back to back), achieved HBM GB/s, an end-to-end
+number through the public API with a host round trip every step (`e2e`), the
+dominant kernel's roofline, the B = 1..16 sweep, the CPU oracle's baseline and
+the SM clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--no-sweep]
+  python bench.py --impl reference ...   (the CPU oracle on the same workload)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PREFILL = synth.DENSE_8B_CASE["prefill"]
+CAPACITY = synth.DENSE_8B_CASE["capacity"]
+WINDOW = synth.DENSE_8B_CASE["steps"]  # positions PREFILL .. PREFILL+WINDOW-1
+METRIC = "aggregate decode tok/s (8B-shaped Q8_0, B sessions, 1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kv_bytes_per_pos(s):
+    return 2 * s.n_layers * s.n_kv_heads * s.head_dim * 2  # K and V, fp16
+
+
+def step_bytes(s, positions):
+    """Algorithmic HBM bytes of one step: every weight once, the embedding rows,
+    the KV rows attended (incl. the new one) and the new rows written."""
+    B = len(positions)
+    kvb = kv_bytes_per_pos(s)
+    return (s.weight_bytes() + B * (s.hidden // 32) * 34 + sum(int(p) + 1 for p in positions) * kvb
+            + B * kvb)
+
+
+def kernels_per_step(s, with_argmax=True):
+    return 1 + s.n_layers * 8 + 2 + (1 if with_argmax else 0)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in d:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[kernel]
+        src = os.path.join(ROOT, e["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return e["dram_bytes_per_launch"] if h == e["source_sha256_16"] else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# --------------------------------------------------------------------------- ours
+def run_kd(args, rank, world):
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kbuild.build()
+    shape = synth.LLAMA3_8B
+    B = args.batch
+    max_b = 16 if args.sweep else B
+    w = synth.model_weights(shape, seed=0)
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=max_b, max_ctx=CAPACITY), w)
+    ids = []
+    for i in range(max_b):
+        k, v = synth.kv_prefill(shape, 0, i, PREFILL)
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, k, v, PREFILL)
+        ids.append(sid)
+        del k, v
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    tok = synth.tokens(0, "bench", max_b, shape.vocab)
+    am = torch.empty(max_b, dtype=torch.int32, device=dev)
+
+    def pos_at(i, b):
+        return np.full(b, PREFILL + (i % WINDOW), np.int32)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def timed(b, steps, warmup):
+        for i in range(warmup):
+            kd.kd_decode_step(m, ids[:b], tok[:b], pos_at(i, b), None, am[:b], stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        byts = 0
+        e0.record(stream)
+        for i in range(warmup, warmup + steps):
+            p = pos_at(i, b)
+            kd.kd_decode_step(m, ids[:b], tok[:b], p, None, am[:b], stream)
+            byts += step_bytes(shape, p)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, byts
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    with ClockSampler(gpu_index) as clk:
+        ms, byts = timed(B, args.steps, args.warmup)
+    status = kd.kd_device_status(m)
+    tok_s = B * args.steps * world / (ms / 1e3)
+    gbs = byts / (ms / 1e3) / 1e9
+
+    # ---- end to end through the public API: host tokens in, host argmax out, every step
+    host_tok = torch.tensor(tok[:B], dtype=torch.int32).pin_memory()
+    host_out = torch.empty(B, dtype=torch.int32).pin_memory()
+    e2e_steps = min(args.steps, 128)
+    for i in range(args.warmup):
+        kd.kd_decode_step(m, ids[:B], host_tok.numpy(), pos_at(i, B), None, am[:B], stream)
+        host_out.copy_(am[:B], non_blocking=True)
+        torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        kd.kd_decode_step(m, ids[:B], host_tok.numpy(), pos_at(i, B), None, am[:B], stream)
+        host_out.copy_(am[:B], non_blocking=True)
+        stream.synchronize()
+        host_tok.copy_(host_out)  # greedy feedback through the host
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": round(B * e2e_steps * world / e2e_s, 2), "unit": "tok/s",
+           "h2d_bytes_per_step": 3 * 16 * 4, "d2h_bytes_per_step": B * 4, "steps": e2e_steps}
+
+    # ---- per-kernel device times (events around every launch) for the roofline
+    kd.kd_profile_enable(m, True)
+    kd.kd_profile_read(m)
+    n_prof = 8
+    for i in range(n_prof):
+        kd.kd_decode_step(m, ids[:B], tok[:B], pos_at(i, B), None, am[:B], stream)
+    prof = kd.kd_profile_read(m)
+    kd.kd_profile_enable(m, False)
+    peak, peak_kind = read_peaks()
+    wb = synth.Q8_BLOCK_BYTES / synth.Q8_BLOCK
+    H, F = shape.hidden, shape.ffn
+    per_launch_bytes = {
+        "gate_up": 2 * F * H * wb + B * H * 2 + B * F * 2,
+        "down": H * F * wb + B * F * 2 + 2 * B * H * 4,
+        "qkv": (shape.q_dim + 2 * shape.kv_dim) * H * wb + B * H * 2 + B * shape.q_dim * 4 + 2 * B * shape.kv_dim * 2,
+        "wo": H * shape.q_dim * wb + B * shape.q_dim * 2 + 2 * B * H * 4,
+        "lm_head": shape.vocab * H * wb + B * H * 2 + B * shape.vocab * 4,
+        "attn_split": (sum(PREFILL + (i % WINDOW) + 1 for i in range(n_prof)) / n_prof) * B
+        * shape.n_kv_heads * shape.head_dim * 2 * 2,
+    }
+    dominant = max(prof, key=lambda k: prof[k][1])
+    n_l, t_ms = prof[dominant]
+    avg_s = t_ms / max(n_l, 1) / 1e3
+    alg = per_launch_bytes.get(dominant)
+    roofline = None
+    if alg is not None and avg_s > 0:
+        ach = alg / avg_s / 1e9
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak,
+                    "peak_source": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "traffic": traffic_for(dominant), "alg_bytes_per_launch": int(alg),
+                    "avg_launch_us": round(avg_s * 1e6, 2)}
+    kernel_share = {k: {"launches": v[0], "ms": round(v[1], 3),
+                        "share": round(v[1] / max(1e-9, sum(x[1] for x in prof.values())), 4)}
+                    for k, v in prof.items()}
+
+    # ---- B = 1 .. 16 sweep
+    sweep = {}
+    if args.sweep:
+        for b in (1, 2, 4, 8, 16):
+            sm, sb = timed(b, max(16, min(args.steps, 128)), args.warmup)
+            n = max(16, min(args.steps, 128))
+            sweep[str(b)] = {"tok_s": round(b * n * world / (sm / 1e3), 1),
+                             "hbm_gbs": round(sb / (sm / 1e3) / 1e9, 1),
+                             "frac_of_peak": round(sb / (sm / 1e3) / 1e9 / peak, 4)}
+    kd.kd_model_free(m)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, w, B)
+    return dict(value=tok_s, ms=ms, gbs=gbs, e2e=e2e, roofline=roofline, sweep=sweep, cpu=cpu,
+                clocks=clk.summary(), peak=peak, peak_kind=peak_kind, status=status, shares=kernel_share)
+
+
+def cpu_baseline(shape, w, B):
+    """The CPU oracle as it stands, one decode step of the B sessions (bounded sample)."""
+    import oracle
+    om = oracle.OracleModel(shape, w)
+    cap = PREFILL + 1
+    caches = [om.new_cache(cap, *synth.kv_prefill(shape, 0, i, PREFILL)) for i in range(B)]
+    tok = synth.tokens(0, "bench", B, shape.vocab)
+    t0 = time.perf_counter()
+    om.step(tok, [PREFILL] * B, caches, cap)
+    dt = time.perf_counter() - t0
+    return {"value": round(B / dt, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"1 decode step of {B} sessions at position {PREFILL} (8B-shaped Q8_0, fp64 C oracle, "
+                      f"OpenMP over rows), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The oracle timed as it stands on the host cores, one layer of one session per step."""
+    import oracle
+    shape = synth.LLAMA3_8B
+    B = args.batch
+    w = synth.model_weights(shape, seed=0)
+    om = oracle.OracleModel(shape, w)
+    cap = PREFILL + WINDOW
+    caches = [om.new_cache(cap, *synth.kv_prefill(shape, 0, i, PREFILL)) for i in range(B)]
+    x = [np.zeros(shape.hidden) for _ in range(B)]
+    for b in range(B):  # embedding rows as the start of each session's residual stream
+        x[b][:] = oracle.q8_0_dequant_row(w["tok_embd"][int(synth.tokens(0, "bench", B, shape.vocab)[b])],
+                                          shape.hidden)
+
+    def one(i):
+        b, l = i % B, (i // B) % shape.n_layers
+        om.layer_step(l, PREFILL + (i // (B * shape.n_layers)) % WINDOW, caches[b], cap, x[b])
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    per_layer = dt / args.steps
+    tok_s = 1.0 / (per_layer * shape.n_layers)
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"each step = one decoder layer of one session (1/{shape.n_layers} of a token, lm_head "
+              f"excluded) through the fp64 C oracle; {args.steps} steps in {dt:.1f} s")
+    return {"metric": METRIC, "value": round(tok_s, 4), "unit": "tok/s", "impl": "reference",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_layer * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"llama3-8b-shaped Q8_0, B={B} sessions at ctx {PREFILL}..{PREFILL + WINDOW - 1}",
+                       "batch": B},
+            "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--batch", type=int, default=8)
+    ap.add_argument("--impl", default="kd", choices=["kd", "reference"])
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    r = run_kd(args, rank, world)
+    if rank == 0:
+        shape = synth.LLAMA3_8B
+        out = {
+            "metric": METRIC, "value": round(r["value"], 2), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16xq8_0->f32", "data": "synthetic",
+            "config": {"workload": f"llama3-8b-shaped Q8_0 decode, B={args.batch} sessions, KV fp16 pre-filled to "
+                                   f"{PREFILL}, positions {PREFILL}..{PREFILL + WINDOW - 1} cycling",
+                       "batch": args.batch, "prefill": PREFILL, "capacity": CAPACITY,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 7.97 GB of Q8_0 weights streamed per step"},
+            "hbm_gbs": round(r["gbs"], 1),
+            "hbm_frac_of_peak": round(r["gbs"] / r["peak"], 4),
+            "peak_hbm_gbs": r["peak"], "peak_source": r["peak_kind"],
+            "e2e": r["e2e"], "roofline": r["roofline"], "batch_sweep": r["sweep"],
+            "cpu_baseline": r["cpu"], "clocks": r["clocks"],
+            "gpu_launches": kernels_per_step(shape) * args.steps,
+            "kernel_time_share": r["shares"], "device_status": r["status"],
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

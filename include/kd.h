@@ -1,0 +1,213 @@
+/*
+ * kd.h -- C ABI of the batched multi-session decode step for GB300 (sm_103a).
+ *
+ * One decode step runs B independent sessions (1 <= B <= 16) through one
+ * fused forward pass of a dense, Llama-shaped decoder with Q8_0 weights.  Each
+ * session owns a slot of the fp16 KV arena and sits at its own position; every
+ * weight matrix is streamed from HBM once per step for all B rows.  This is
+ * the batched decode step of memra-engine's `decode_batch.rs` (module header:
+ * "B sequences share one fused pass", the bandwidth thesis and the EXACTNESS
+ * CONTRACT; `decode_step_batch`) restated for one GB300: one process, one
+ * GPU, no collectives.
+ *
+ * Conventions for every function:
+ *   - Returns KD_OK (0) or a negative kd_status.  Nothing aborts, nothing
+ *     throws across the ABI; the reason for the last failure on the calling
+ *     thread is available from kd_last_error().
+ *   - Arguments are validated on the host before any work is enqueued, so a
+ *     call that fails leaves every piece of state as it was.
+ *   - "device" pointers are CUDA device (or managed) addresses on the current
+ *     device; "host" pointers are ordinary CPU memory.
+ *   - A kd_stream is a cudaStream_t passed as void*; NULL is the legacy
+ *     default stream.  Work is enqueued on it and the call returns without
+ *     waiting, unless the function says otherwise.
+ *   - A model handle is not thread-safe: callers serialise calls on it.
+ */
+#ifndef KD_H_
+#define KD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kd_status;
+enum {
+    KD_OK = 0,
+    KD_ERR_INVALID_ARG = -1,   /* null pointer, bad size, bad shape */
+    KD_ERR_OOM = -2,           /* device or pinned-host allocation failed */
+    KD_ERR_CUDA = -3,          /* a CUDA runtime call failed (message has the CUDA error) */
+    KD_ERR_NO_FREE_SLOT = -4,  /* every session slot is bound */
+    KD_ERR_BAD_SESSION = -5,   /* id out of range, not bound, or repeated within one step */
+    KD_ERR_POSITION = -6,      /* position < 0, > the session's length, or >= max_ctx */
+    KD_ERR_BATCH = -7,         /* B outside [1, KD_MAX_BATCH] */
+    KD_ERR_UNSUPPORTED = -8,   /* a shape the kernels do not implement (see kd_config) */
+    KD_ERR_DEVICE = -9         /* a kernel reported a device-side fault (bounded wait ran out) */
+};
+
+/* The widest batch with an exact kernel class: memra refuses B > 16 because no
+ * per-row-exact kernel exists above it (decode_batch.rs, module header,
+ * "B > 16 crosses into GEMM/dp4a-tail numeric configs ... refused"). */
+#define KD_MAX_BATCH 16
+
+typedef void* kd_stream;          /* cudaStream_t */
+typedef struct kd_model kd_model; /* opaque, library-owned */
+
+/* Model shape.  Requirements (else KD_ERR_UNSUPPORTED): hidden, ffn and
+ * n_heads*head_dim are multiples of 128; head_dim is 64 or 128; n_heads is
+ * 1, 2, 4 or 8 times n_kv_heads; vocab is a multiple of 32.  All sizes and
+ * max_sessions, max_ctx are >= 1 (else KD_ERR_INVALID_ARG).
+ * rope_theta is the NeoX RoPE base; rms_eps the RMSNorm epsilon. */
+typedef struct {
+    int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rope_theta, rms_eps;
+    int32_t max_sessions;   /* KV slots in the arena */
+    int32_t max_ctx;        /* positions per slot (the slot capacity) */
+    int32_t flags;          /* KD_FLAG_* */
+} kd_config;
+
+#define KD_FLAG_NO_GRAPH 1  /* launch each kernel every step instead of replaying a CUDA graph */
+
+/* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
+ * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the
+ * blocks running along the input dimension.  Per-layer arrays hold n_layers
+ * pointers.  Shapes ([rows][cols]): tok_embd and output [vocab][hidden];
+ * wq [n_heads*head_dim][hidden]; wk, wv [n_kv_heads*head_dim][hidden];
+ * wo [hidden][n_heads*head_dim]; w_gate, w_up [ffn][hidden]; w_down [hidden][ffn];
+ * norms fp32 [hidden].  The library copies everything; the caller may free the
+ * host memory once kd_model_load returns. */
+typedef struct {
+    const void* tok_embd;
+    const void* output;
+    const float* output_norm;
+    const void* const* wq;
+    const void* const* wk;
+    const void* const* wv;
+    const void* const* wo;
+    const void* const* w_gate;
+    const void* const* w_up;
+    const void* const* w_down;
+    const float* const* attn_norm;
+    const float* const* ffn_norm;
+} kd_weights;
+
+/* Copy and repack the weights into device memory and allocate the KV arena
+ * (2 * n_layers * max_sessions * n_kv_heads * max_ctx * head_dim fp16) and the
+ * step workspaces.  Synchronous.  On success *out owns all of it. */
+kd_status kd_model_load(const kd_config* cfg, const kd_weights* w, kd_model** out);
+
+/* Wait for the model's outstanding work, then free everything it owns. */
+kd_status kd_model_free(kd_model* m);
+
+/* Claim a free slot (lowest free id) for a new session of length 0.
+ * Slot ownership per session follows memra's per-sequence `Cache` (its own
+ * position and KV) and hf2q ADR-040's slot-indexed KV ("per-slot KV offset"). */
+kd_status kd_session_bind(kd_model* m, int32_t* session_id_out);
+
+/* Release a session's slot.  Waits on the host for the last step that used the
+ * model, so a freed slot is never rebound while a step may still write it. */
+kd_status kd_session_free(kd_model* m, int32_t session_id);
+
+/* Fill a bound session's cache with `len` positions (its prompt history):
+ * k_fp16 and v_fp16 are [n_layers][n_kv_heads][len][head_dim] fp16, host or
+ * device memory (any address CUDA can copy from).  Sets the length to len.
+ * Enqueued on `stream`; the source must stay valid until the stream reaches it. */
+kd_status kd_session_load_kv(kd_model* m, int32_t session_id, const void* k_fp16,
+                             const void* v_fp16, int32_t len, kd_stream stream);
+
+/* The number of positions a bound session holds. */
+kd_status kd_session_length(const kd_model* m, int32_t session_id, int32_t* len_out);
+
+/* One batched decode step (memra decode_batch.rs `decode_step_batch`: row b is
+ * session b with its own cache and position; every projection runs at m = B).
+ *   session_ids, tokens, positions: host arrays of length B.  Ids must be bound
+ *     and distinct; tokens in [0, vocab); 0 <= positions[b] <= length(session)
+ *     and positions[b] < max_ctx.  The token is written to the cache at
+ *     positions[b] and attends keys 0..positions[b]; afterwards the session's
+ *     length is positions[b] + 1 (a position below the length rewinds).
+ *   logits_out: NULL or device fp32 [B][vocab]; row b belongs to session_ids[b].
+ *   argmax_out: NULL or device int32 [B]: the greedy next token (largest logit,
+ *     ties to the lowest index, NaN never wins; -1 if a row is all NaN).
+ * Enqueued on `stream` without a host wait; outputs are valid once the stream
+ * has reached them.  Steps of one model may be issued on different streams:
+ * each step waits for the previous one on the device. */
+kd_status kd_decode_step(kd_model* m, const int32_t* session_ids, const int32_t* tokens,
+                         const int32_t* positions, int32_t B, float* logits_out,
+                         int32_t* argmax_out, kd_stream stream);
+
+/* Debug: when dev_buf is not NULL, later steps also write the residual stream
+ * after the embedding and after every layer to dev_buf, device fp32
+ * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off. */
+kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf);
+
+/* Wait for the model's work, then read and clear its device fault word.
+ * *flags_out = 0 when no kernel gave up a bounded wait; KD_ERR_DEVICE is
+ * returned when one did. */
+kd_status kd_device_status(kd_model* m, int32_t* flags_out);
+
+/* Measurement (the event-based counterpart of memra's per-phase breakdown,
+ * decode_batch.rs BATCH_PHASE, without its host syncs).  While enabled, steps
+ * launch kernel by kernel and bracket every kernel with CUDA events on the
+ * step's stream.  kd_profile_read waits for the model's work, then returns per
+ * kernel class (KD_K_*) the number of launches and their summed device time in
+ * milliseconds since the previous read, and resets the sums. */
+enum {
+    KD_K_EMBED = 0, KD_K_RMSNORM, KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO,
+    KD_K_GATE_UP, KD_K_DOWN, KD_K_LM_HEAD, KD_K_ARGMAX, KD_K_COUNT
+};
+kd_status kd_profile_enable(kd_model* m, int32_t on);
+kd_status kd_profile_read(kd_model* m, int32_t* launches /* [KD_K_COUNT] */,
+                          double* ms /* [KD_K_COUNT] */);
+
+/* The message of the last failure on the calling thread ("" if none). */
+const char* kd_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Op-level entry points: the step's kernels on their own, for isolated tests
+ * and measurements.  Same conventions as above.
+ * ---------------------------------------------------------------------- */
+
+typedef struct kd_q8_matrix kd_q8_matrix; /* a repacked Q8_0 matrix on the device */
+
+/* Copy a canonical Q8_0 matrix [rows][cols/32] (host memory) to the device in
+ * the kernel's tiled layout, with a split-K workspace for m <= KD_MAX_BATCH.
+ * rows must be a multiple of 32 and cols a multiple of 128.  Synchronous. */
+kd_status kd_q8_matrix_create(const void* q8_0_host, int32_t rows, int32_t cols,
+                              kd_q8_matrix** out);
+kd_status kd_q8_matrix_free(kd_q8_matrix* w);
+
+/* Weight-only Q8_0 matrix-vector product for m = 1..16 rows (memra's batched
+ * verify-tier mmvq, "bit-identical per (token,row) to m=1"):
+ *   y[r][o] = sum over blocks b of d[o][b] * sum_j q[o][b][j] * x[r][32b+j]
+ * x: device fp16 [m][cols]; y: device fp32 [m][rows].  Row r of y is
+ * bit-identical for every m.  Calls on one matrix must be stream-ordered
+ * (they share its workspace). */
+kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
+                  kd_stream stream);
+
+/* Bytes of device workspace kd_attn_append_decode needs for these sizes. */
+size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap);
+
+/* KV append then ragged GQA split-K flash-decode (memra decode_batch_layers,
+ * "phase A appends all B rows ... phase B attends all B sequences"):
+ *   for each row b: K[slot_b][h][pos_b] = fp16(k_new[b][h]), same for V; then
+ *   out[b][qh] = fp16(sum_{t<=pos_b} softmax_t(q[b][qh] . K_t / sqrt(head_dim)) V_t)
+ *   over KV head qh / (n_heads / n_kv_heads).
+ * q: device fp32 [B][n_heads][head_dim] (already rotated); k_new, v_new: device
+ * fp32 [B][n_kv_heads][head_dim]; k_cache, v_cache: device fp16
+ * [n_slots][n_kv_heads][cap][head_dim]; slots, positions: host int32 [B] (slots
+ * distinct, 0 <= positions[b] < cap); out: device fp16 [B][n_heads*head_dim];
+ * workspace: device memory of kd_attn_workspace_bytes(B, n_heads, head_dim, cap). */
+kd_status kd_attn_append_decode(const float* q, const float* k_new, const float* v_new,
+                                uint16_t* k_cache, uint16_t* v_cache, const int32_t* slots,
+                                const int32_t* positions, int32_t B, int32_t n_heads,
+                                int32_t n_kv_heads, int32_t head_dim, int32_t n_slots,
+                                int32_t cap, uint16_t* out, void* workspace,
+                                size_t workspace_bytes, kd_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KD_H_ */

@@ -84,6 +84,9 @@ def _declare(L):
     L.kdo_session_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32,
                                    C.c_int32, _u16p, _u16p, C.c_int32, _f32p, _f32p]
     L.kdo_session_step.restype = C.c_int32
+    L.kdo_layer_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32, C.c_int32,
+                                 _u16p, _u16p, C.c_int32, _f64p]
+    L.kdo_layer_step.restype = C.c_int32
     L.kdo_decode_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32,
                                   _i32p, _i32p, C.POINTER(_u16p), C.POINTER(_u16p), C.c_int32,
                                   _f32p, _f32p, _i32p]
@@ -200,6 +203,19 @@ class OracleModel:
             k[:, :, :n] = k_prefill
             v[:, :, :n] = v_prefill
         return k, v
+
+    def layer_step(self, layer: int, pos: int, cache, cap: int, x: np.ndarray) -> np.ndarray:
+        """One layer of one session: x (fp64 [hidden]) updated in place; cache = (k, v)."""
+        k, v = cache
+        s = self.shape
+        off = layer * s.n_kv_heads * cap * s.head_dim
+        kp = C.cast(k.ctypes.data + 2 * off, _u16p)
+        vp = C.cast(v.ctypes.data + 2 * off, _u16p)
+        rc = lib().kdo_layer_step(C.byref(self.cfg), C.byref(self.cw), layer, pos, kp, vp, cap,
+                                  _p(x, _f64p))
+        if rc != 0:
+            raise ValueError(f"oracle layer step rejected its inputs (rc={rc})")
+        return x
 
     def step(self, tokens, positions, caches, cap: int, want_hidden: bool = False):
         """One batched step.  caches: list of (k, v) per session, updated in place.

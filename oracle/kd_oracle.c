@@ -199,22 +199,17 @@ typedef struct {
     const float* const* ffn_norm;     /* [hidden] */
 } kdo_weights;
 
-/* One session, one step.  k_cache / v_cache are the session's fp16 caches,
- * [n_layers][n_kv][cap][hd]; rows 0..pos-1 hold its history, row `pos` is
- * overwritten with this step's key/value, rows beyond pos are never read.
- * logits: [vocab] fp32.  hidden: NULL or [n_layers+1][hidden] fp32, the residual
- * after the embedding and after every layer. */
-KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
-                                    int32_t token, int32_t pos,
-                                    uint16_t* k_cache, uint16_t* v_cache, int32_t cap,
-                                    float* logits, float* hidden) {
+/* One layer of one session (the body of `decode_batch_layers` for one row):
+ * x is the fp32-valued residual stream [hidden], updated in place.  The layer's
+ * fp16 caches are [n_kv][cap][hd]; row `pos` is written, rows 0..pos are read. */
+KDO_EXPORT int32_t kdo_layer_step(const kdo_config* c, const kdo_weights* w, int32_t l,
+                                  int32_t pos, uint16_t* Kl, uint16_t* Vl, int32_t cap,
+                                  double* x) {
     const int H = c->hidden, nh = c->n_heads, nkv = c->n_kv_heads, hd = c->head_dim;
-    const int F = c->ffn, V = c->vocab, L = c->n_layers;
-    if (token < 0 || token >= V || pos < 0 || pos >= cap || nh % nkv || hd % 2) return -1;
+    const int F = c->ffn;
+    if (l < 0 || l >= c->n_layers || pos < 0 || pos >= cap || nh % nkv || hd % 2) return -1;
     const int group = nh / nkv;
     const double scale = 1.0 / sqrt((double)hd);
-
-    double* x = malloc(sizeof(double) * H);
     double* xn = malloc(sizeof(double) * H);
     double* q = malloc(sizeof(double) * nh * hd);
     double* k = malloc(sizeof(double) * nkv * hd);
@@ -224,6 +219,58 @@ KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
     double* g = malloc(sizeof(double) * F);
     double* u = malloc(sizeof(double) * F);
     double* act = malloc(sizeof(double) * F);
+
+    /* attn_norm, then the q/k/v projections of the fp16 normed row. */
+    kdo_rmsnorm_f16(x, w->attn_norm[l], H, c->rms_eps, xn);
+    kdo_matvec_q8_0(w->wq[l], nh * hd, H, xn, q);
+    kdo_matvec_q8_0(w->wk[l], nkv * hd, H, xn, k);
+    kdo_matvec_q8_0(w->wv[l], nkv * hd, H, xn, v);
+    /* RoPE of q and k at this session's own position. */
+    for (int h = 0; h < nh; ++h) kdo_rope_neox(q + h * hd, hd, pos, c->rope_theta);
+    for (int h = 0; h < nkv; ++h) kdo_rope_neox(k + h * hd, hd, pos, c->rope_theta);
+    /* KV append: row `pos` of this session's cache, stored as fp16. */
+    for (int h = 0; h < nkv; ++h)
+        for (int i = 0; i < hd; ++i) {
+            Kl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(k[h * hd + i]);
+            Vl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(v[h * hd + i]);
+        }
+    /* Attention over keys 0..pos (t_kv = pos + 1), GQA head mapping h -> h / group. */
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < nh; ++h) {
+        int kh = h / group;
+        kdo_attention_head(q + h * hd, Kl + (size_t)kh * cap * hd, Vl + (size_t)kh * cap * hd,
+                           pos + 1, hd, hd, scale, att + h * hd);
+    }
+    for (int i = 0; i < nh * hd; ++i) att[i] = round_half(att[i]);
+    /* o-projection and residual add (fp32 residual). */
+    kdo_matvec_q8_0(w->wo[l], H, nh * hd, att, o);
+    for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
+    /* ffn_norm, SwiGLU, down-projection, residual add. */
+    kdo_rmsnorm_f16(x, w->ffn_norm[l], H, c->rms_eps, xn);
+    kdo_matvec_q8_0(w->w_gate[l], F, H, xn, g);
+    kdo_matvec_q8_0(w->w_up[l], F, H, xn, u);
+    for (int i = 0; i < F; ++i) act[i] = round_half(kdo_silu(g[i]) * u[i]);
+    kdo_matvec_q8_0(w->w_down[l], H, F, act, o);
+    for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
+
+    free(xn); free(q); free(k); free(v); free(att); free(o); free(g); free(u); free(act);
+    return 0;
+}
+
+/* One session, one step.  k_cache / v_cache are the session's fp16 caches,
+ * [n_layers][n_kv][cap][hd]; rows 0..pos-1 hold its history, row `pos` is
+ * overwritten with this step's key/value, rows beyond pos are never read.
+ * logits: [vocab] fp32.  hidden: NULL or [n_layers+1][hidden] fp32, the residual
+ * after the embedding and after every layer. */
+KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
+                                    int32_t token, int32_t pos,
+                                    uint16_t* k_cache, uint16_t* v_cache, int32_t cap,
+                                    float* logits, float* hidden) {
+    const int H = c->hidden, nkv = c->n_kv_heads, hd = c->head_dim;
+    const int V = c->vocab, L = c->n_layers;
+    if (token < 0 || token >= V || pos < 0 || pos >= cap) return -1;
+    double* x = malloc(sizeof(double) * H);
+    double* xn = malloc(sizeof(double) * H);
     double* lg = malloc(sizeof(double) * V);
 
     /* Embedding: the token's Q8_0 row, dequantised (exact in fp32). */
@@ -231,51 +278,20 @@ KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
     for (int i = 0; i < H; ++i) x[i] = round_float(x[i]);
     if (hidden) for (int i = 0; i < H; ++i) hidden[i] = (float)x[i];
 
-    for (int l = 0; l < L; ++l) {
-        uint16_t* Kl = k_cache + (size_t)l * nkv * cap * hd;
-        uint16_t* Vl = v_cache + (size_t)l * nkv * cap * hd;
-        /* attn_norm, then the q/k/v projections of the fp16 normed row. */
-        kdo_rmsnorm_f16(x, w->attn_norm[l], H, c->rms_eps, xn);
-        kdo_matvec_q8_0(w->wq[l], nh * hd, H, xn, q);
-        kdo_matvec_q8_0(w->wk[l], nkv * hd, H, xn, k);
-        kdo_matvec_q8_0(w->wv[l], nkv * hd, H, xn, v);
-        /* RoPE of q and k at this session's own position. */
-        for (int h = 0; h < nh; ++h) kdo_rope_neox(q + h * hd, hd, pos, c->rope_theta);
-        for (int h = 0; h < nkv; ++h) kdo_rope_neox(k + h * hd, hd, pos, c->rope_theta);
-        /* KV append: row `pos` of this session's cache, stored as fp16. */
-        for (int h = 0; h < nkv; ++h)
-            for (int i = 0; i < hd; ++i) {
-                Kl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(k[h * hd + i]);
-                Vl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(v[h * hd + i]);
-            }
-        /* Attention over keys 0..pos (t_kv = pos + 1), GQA head mapping h -> h / group. */
-#pragma omp parallel for schedule(static)
-        for (int h = 0; h < nh; ++h) {
-            int kh = h / group;
-            kdo_attention_head(q + h * hd, Kl + (size_t)kh * cap * hd, Vl + (size_t)kh * cap * hd,
-                               pos + 1, hd, hd, scale, att + h * hd);
-        }
-        for (int i = 0; i < nh * hd; ++i) att[i] = round_half(att[i]);
-        /* o-projection and residual add (fp32 residual). */
-        kdo_matvec_q8_0(w->wo[l], H, nh * hd, att, o);
-        for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
-        /* ffn_norm, SwiGLU, down-projection, residual add. */
-        kdo_rmsnorm_f16(x, w->ffn_norm[l], H, c->rms_eps, xn);
-        kdo_matvec_q8_0(w->w_gate[l], F, H, xn, g);
-        kdo_matvec_q8_0(w->w_up[l], F, H, xn, u);
-        for (int i = 0; i < F; ++i) act[i] = round_half(kdo_silu(g[i]) * u[i]);
-        kdo_matvec_q8_0(w->w_down[l], H, F, act, o);
-        for (int i = 0; i < H; ++i) x[i] = round_float(x[i] + o[i]);
+    int32_t rc = 0;
+    for (int l = 0; l < L && rc == 0; ++l) {
+        rc = kdo_layer_step(c, w, l, pos, k_cache + (size_t)l * nkv * cap * hd,
+                            v_cache + (size_t)l * nkv * cap * hd, cap, x);
         if (hidden) for (int i = 0; i < H; ++i) hidden[(size_t)(l + 1) * H + i] = (float)x[i];
     }
-    /* Head: output_norm, lm_head, fp32 logits. */
-    kdo_rmsnorm_f16(x, w->output_norm, H, c->rms_eps, xn);
-    kdo_matvec_q8_0(w->output, V, H, xn, lg);
-    for (int i = 0; i < V; ++i) logits[i] = (float)lg[i];
-
-    free(x); free(xn); free(q); free(k); free(v); free(att); free(o);
-    free(g); free(u); free(act); free(lg);
-    return 0;
+    if (rc == 0) {
+        /* Head: output_norm, lm_head, fp32 logits. */
+        kdo_rmsnorm_f16(x, w->output_norm, H, c->rms_eps, xn);
+        kdo_matvec_q8_0(w->output, V, H, xn, lg);
+        for (int i = 0; i < V; ++i) logits[i] = (float)lg[i];
+    }
+    free(x); free(xn); free(lg);
+    return rc;
 }
 
 /* B sessions, one step each: the batched step is B independent single-session

@@ -1,0 +1,760 @@
+// kd_api.cu -- the C ABI (include/kd.h): model load and repack, the session
+// slot arena, and the batched decode step's launch train.
+//
+// Structure of one step (memra-engine decode_batch.rs, `decode_step_batch_lean_masked`
+// and `decode_batch_layers`): stage the [B] session slots, tokens and positions
+// (one host-to-device copy), gather the B embedding rows, then per layer
+//   RMSNorm -> QKV mmvq (+RoPE at each row's position, +KV append) ->
+//   split-K flash-decode -> combine -> O mmvq (+residual) -> RMSNorm ->
+//   gate|up mmvq (+SwiGLU) -> down mmvq (+residual),
+// then the final RMSNorm, the lm_head mmvq and the device argmax.  The launch
+// train is captured once per (B, output buffers) as a CUDA graph and replayed;
+// consecutive kernels overlap through programmatic dependent launch (each
+// kernel's weight prefetch runs before it waits for its predecessor).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "kd.h"
+#include "kd_kernels.h"
+
+using kd::PackedQ8;
+
+namespace {
+
+thread_local std::string g_err;
+
+kd_status fail(kd_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define KD_CK(call)                                                                               \
+    do {                                                                                          \
+        cudaError_t e_ = (call);                                                                  \
+        if (e_ != cudaSuccess)                                                                    \
+            return fail(e_ == cudaErrorMemoryAllocation ? KD_ERR_OOM : KD_ERR_CUDA, "%s: %s (%s:%d)", \
+                        #call, cudaGetErrorString(e_), __FILE__, __LINE__);                      \
+    } while (0)
+
+std::once_flag g_attr_once[64];
+cudaError_t g_attr_err[64];
+
+cudaError_t init_device_attributes(int dev) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(g_attr_once[dev], [dev] {
+        cudaError_t e = kd::mmvq_init_attributes();
+        if (e == cudaSuccess) e = kd::attn_init_attributes();
+        g_attr_err[dev] = e;
+    });
+    return g_attr_err[dev];
+}
+
+constexpr int RING = 4;        // pinned staging slots for the per-step descriptor
+constexpr int DESC_INTS = 3 * KD_MAX_BATCH;  // slot[16], token[16], pos[16]
+
+// Source-row maps of the packed tiles (see the layout note in kd_kernels.h).
+std::vector<int> tiles_natural(int rows) {
+    std::vector<int> t(rows / kd::TILE_ROWS);
+    for (size_t i = 0; i < t.size(); ++i) t[i] = (int)i * kd::TILE_ROWS;
+    return t;
+}
+std::vector<int> tiles_swiglu(int ffn) {  // group g = (gate tile g, up tile g)
+    std::vector<int> t;
+    for (int g = 0; g < ffn / kd::TILE_ROWS; ++g) {
+        t.push_back(g * kd::TILE_ROWS);
+        t.push_back(ffn + g * kd::TILE_ROWS);
+    }
+    return t;
+}
+std::vector<int> tiles_qkv(int heads, int hd) {  // group = (dims 16j.., dims hd/2 + 16j..) of one head
+    std::vector<int> t;
+    for (int h = 0; h < heads; ++h)
+        for (int j = 0; j < hd / kd::GROUP_ROWS; ++j) {
+            t.push_back(h * hd + j * kd::TILE_ROWS);
+            t.push_back(h * hd + hd / 2 + j * kd::TILE_ROWS);
+        }
+    return t;
+}
+
+size_t q8_row_bytes(int K) { return (size_t)(K / 32) * 34; }
+
+// Upload canonical Q8_0 parts (stacked by rows) through `staging`, then repack.
+kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, int K,
+                        const std::vector<int>& tile_src, uint8_t* staging, int* d_tiles,
+                        PackedQ8& out) {
+    size_t off = 0;
+    int rows = 0;
+    for (auto& p : parts) {
+        if (!p.first) return fail(KD_ERR_INVALID_ARG, "null weight matrix");
+        const size_t bytes = (size_t)p.second * q8_row_bytes(K);
+        KD_CK(cudaMemcpy(staging + off, p.first, bytes, cudaMemcpyHostToDevice));
+        off += bytes;
+        rows += p.second;
+    }
+    out.K = K;
+    out.rows = rows;
+    out.G = (int)tile_src.size() / kd::MT;
+    out.KG = K / kd::KGROUP;
+    kd::choose_split(out);
+    KD_CK(cudaMalloc(&out.w, out.bytes()));
+    KD_CK(cudaMemcpy(d_tiles, tile_src.data(), tile_src.size() * sizeof(int), cudaMemcpyHostToDevice));
+    KD_CK(kd::launch_repack(staging, K, d_tiles, out.G, out.w, 0));
+    KD_CK(cudaDeviceSynchronize());
+    return KD_OK;
+}
+
+}  // namespace
+
+struct kd_model {
+    kd_config cfg{};
+    int dev = 0, num_sms = 0, attn_grid = 0;
+    bool pdl = true;
+    uint8_t* tok_embd = nullptr;
+    std::vector<PackedQ8> qkv, wo, gu, down;
+    PackedQ8 head;
+    float* norms = nullptr;   // [2L+1][H]: attn_norm l, ffn_norm l, then output_norm
+    float2* rope = nullptr;   // [max_ctx][hd/2]
+    __half* kc = nullptr;     // [L][slots][nkv][cap][hd]
+    __half* vc = nullptr;
+    size_t layer_kv = 0;      // elements per layer of one arena
+    float* x = nullptr;       // [16][H] residual stream
+    __half* xn = nullptr;     // [16][H] normed activations
+    float* q = nullptr;       // [16][nh][hd]
+    __half* attn = nullptr;   // [16][nh*hd]
+    __half* act = nullptr;    // [16][F]
+    float* part = nullptr;    // mmvq split-K partials
+    int* cnt = nullptr;       // mmvq arrival counters
+    float* apart = nullptr;   // attention split partials
+    int max_splits = 0;
+    float* logits_ws = nullptr;
+    int* err = nullptr;
+    int* desc = nullptr;      // device [slot16 | token16 | pos16]
+    int32_t* pinned = nullptr;
+    cudaEvent_t ring_ev[RING] = {};
+    int ring_i = 0;
+    cudaEvent_t last_step = nullptr;
+    cudaStream_t cap_stream = nullptr;
+    std::vector<uint8_t> bound;
+    std::vector<int32_t> len;
+    std::map<std::tuple<int, float*, int*>, cudaGraphExec_t> graphs;
+    float* hidden_dbg = nullptr;
+    std::vector<void*> allocs;
+    // measurement: (kernel class, start, end) of every bracketed launch since the last read
+    bool prof = false;
+    std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> prof_marks;
+    std::vector<cudaEvent_t> ev_pool;
+
+    template <class T>
+    cudaError_t alloc(T** p, size_t bytes) {
+        cudaError_t e = cudaMalloc((void**)p, std::max<size_t>(bytes, 16));
+        if (e == cudaSuccess) allocs.push_back((void*)*p);
+        return e;
+    }
+    void release() {
+        for (auto& g : graphs) cudaGraphExecDestroy(g.second);
+        graphs.clear();
+        for (void* p : allocs) cudaFree(p);
+        allocs.clear();
+        for (auto* v : {&qkv, &wo, &gu, &down})
+            for (auto& p : *v) cudaFree(p.w);
+        cudaFree(head.w);
+        if (pinned) cudaFreeHost(pinned);
+        for (auto& e : ring_ev)
+            if (e) cudaEventDestroy(e);
+        for (auto& t : prof_marks) {
+            cudaEventDestroy(std::get<1>(t));
+            cudaEventDestroy(std::get<2>(t));
+        }
+        for (auto e : ev_pool) cudaEventDestroy(e);
+        if (last_step) cudaEventDestroy(last_step);
+        if (cap_stream) cudaStreamDestroy(cap_stream);
+    }
+};
+
+static kd_status check_config(const kd_config* c) {
+    if (c->n_layers < 1 || c->hidden < 128 || c->n_heads < 1 || c->n_kv_heads < 1 ||
+        c->head_dim < 1 || c->ffn < 128 || c->vocab < 32 || c->max_sessions < 1 || c->max_ctx < 1)
+        return fail(KD_ERR_INVALID_ARG, "kd_config: sizes must be positive (got L=%d H=%d nh=%d nkv=%d "
+                    "hd=%d F=%d V=%d S=%d ctx=%d)", c->n_layers, c->hidden, c->n_heads, c->n_kv_heads,
+                    c->head_dim, c->ffn, c->vocab, c->max_sessions, c->max_ctx);
+    if (!(c->rms_eps >= 0.0f) || !(c->rope_theta > 0.0f))
+        return fail(KD_ERR_INVALID_ARG, "kd_config: rms_eps must be >= 0 and rope_theta > 0");
+    if (c->hidden % 128 || c->ffn % 128 || c->vocab % 32 || (c->n_heads * c->head_dim) % 128 ||
+        c->n_heads % c->n_kv_heads || !kd::attn_supported(c->head_dim, c->n_heads / c->n_kv_heads))
+        return fail(KD_ERR_UNSUPPORTED,
+                    "kd_config: need hidden, ffn, n_heads*head_dim multiples of 128, vocab a multiple "
+                    "of 32, head_dim in {64,128}, n_heads/n_kv_heads in {1,2,4,8}");
+    return KD_OK;
+}
+
+static kd_status load_impl(kd_model* m, const kd_weights* w) {
+    const kd_config& c = m->cfg;
+    const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
+    const int F = c.ffn, V = c.vocab, S = c.max_sessions, cap = c.max_ctx;
+    KD_CK(cudaGetDevice(&m->dev));
+    KD_CK(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->dev));
+    KD_CK(init_device_attributes(m->dev));
+    m->attn_grid = kd::attn_split_grid(m->num_sms, hd, nh / nkv);
+    m->pdl = true;
+
+    // ---- weights: canonical bytes in through a staging buffer, repacked on the device
+    const size_t stage_bytes = std::max({(size_t)V * q8_row_bytes(H), (size_t)2 * F * q8_row_bytes(H),
+                                         (size_t)(nh + 2 * nkv) * hd * q8_row_bytes(H),
+                                         (size_t)H * q8_row_bytes(F), (size_t)H * q8_row_bytes(nh * hd)});
+    uint8_t* staging = nullptr;
+    int* d_tiles = nullptr;
+    KD_CK(cudaMalloc(&staging, stage_bytes));
+    const size_t max_tiles = std::max({(size_t)V, (size_t)2 * F, (size_t)(nh + 2 * nkv) * hd}) / kd::TILE_ROWS;
+    if (cudaMalloc(&d_tiles, max_tiles * sizeof(int)) != cudaSuccess) {
+        cudaFree(staging);
+        return fail(KD_ERR_OOM, "tile map allocation failed");
+    }
+    kd_status st = KD_OK;
+    m->qkv.resize(L);
+    m->wo.resize(L);
+    m->gu.resize(L);
+    m->down.resize(L);
+    for (int l = 0; l < L && st == KD_OK; ++l) {
+        st = upload_packed({{w->wq[l], nh * hd}, {w->wk[l], nkv * hd}, {w->wv[l], nkv * hd}}, H,
+                           tiles_qkv(nh + 2 * nkv, hd), staging, d_tiles, m->qkv[l]);
+        if (st == KD_OK)
+            st = upload_packed({{w->wo[l], H}}, nh * hd, tiles_natural(H), staging, d_tiles, m->wo[l]);
+        if (st == KD_OK)
+            st = upload_packed({{w->w_gate[l], F}, {w->w_up[l], F}}, H, tiles_swiglu(F), staging, d_tiles,
+                               m->gu[l]);
+        if (st == KD_OK)
+            st = upload_packed({{w->w_down[l], H}}, F, tiles_natural(H), staging, d_tiles, m->down[l]);
+    }
+    if (st == KD_OK) st = upload_packed({{w->output, V}}, H, tiles_natural(V), staging, d_tiles, m->head);
+    cudaFree(staging);
+    cudaFree(d_tiles);
+    if (st != KD_OK) return st;
+
+    KD_CK(m->alloc(&m->tok_embd, (size_t)V * q8_row_bytes(H)));
+    KD_CK(cudaMemcpy(m->tok_embd, w->tok_embd, (size_t)V * q8_row_bytes(H), cudaMemcpyHostToDevice));
+    KD_CK(m->alloc(&m->norms, (size_t)(2 * L + 1) * H * sizeof(float)));
+    for (int l = 0; l < L; ++l) {
+        if (!w->attn_norm[l] || !w->ffn_norm[l]) return fail(KD_ERR_INVALID_ARG, "null norm weight");
+        KD_CK(cudaMemcpy(m->norms + (size_t)(2 * l) * H, w->attn_norm[l], H * sizeof(float), cudaMemcpyHostToDevice));
+        KD_CK(cudaMemcpy(m->norms + (size_t)(2 * l + 1) * H, w->ffn_norm[l], H * sizeof(float), cudaMemcpyHostToDevice));
+    }
+    KD_CK(cudaMemcpy(m->norms + (size_t)(2 * L) * H, w->output_norm, H * sizeof(float), cudaMemcpyHostToDevice));
+
+    // ---- RoPE table in fp64 on the host, stored fp32: angle = p * theta^(-2i/hd)
+    {
+        const int half = hd / 2;
+        std::vector<float2> tab((size_t)cap * half);
+        std::vector<double> inv(half);
+        for (int i = 0; i < half; ++i) inv[i] = std::pow((double)c.rope_theta, -2.0 * i / hd);
+        for (int p = 0; p < cap; ++p)
+            for (int i = 0; i < half; ++i) {
+                const double a = (double)p * inv[i];
+                tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+        KD_CK(m->alloc(&m->rope, tab.size() * sizeof(float2)));
+        KD_CK(cudaMemcpy(m->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    }
+
+    // ---- KV arena and workspaces
+    m->layer_kv = (size_t)S * nkv * cap * hd;
+    KD_CK(m->alloc(&m->kc, (size_t)L * m->layer_kv * sizeof(__half)));
+    KD_CK(m->alloc(&m->vc, (size_t)L * m->layer_kv * sizeof(__half)));
+    KD_CK(cudaMemset(m->kc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
+    KD_CK(cudaMemset(m->vc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
+    const int MB = KD_MAX_BATCH;
+    KD_CK(m->alloc(&m->x, (size_t)MB * H * sizeof(float)));
+    KD_CK(m->alloc(&m->xn, (size_t)MB * H * sizeof(__half)));
+    KD_CK(m->alloc(&m->q, (size_t)MB * nh * hd * sizeof(float)));
+    KD_CK(m->alloc(&m->attn, (size_t)MB * nh * hd * sizeof(__half)));
+    KD_CK(m->alloc(&m->act, (size_t)MB * F * sizeof(__half)));
+    size_t part = m->head.part_floats();
+    int max_g = m->head.G;
+    for (auto* v : {&m->qkv, &m->wo, &m->gu, &m->down})
+        for (auto& p : *v) {
+            part = std::max(part, p.part_floats());
+            max_g = std::max(max_g, p.G);
+        }
+    KD_CK(m->alloc(&m->part, part * sizeof(float)));
+    KD_CK(m->alloc(&m->cnt, (size_t)max_g * sizeof(int)));
+    KD_CK(cudaMemset(m->cnt, 0, (size_t)max_g * sizeof(int)));
+    m->max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
+    KD_CK(m->alloc(&m->apart, (size_t)MB * nh * m->max_splits * (hd + 2) * sizeof(float)));
+    KD_CK(m->alloc(&m->logits_ws, (size_t)MB * V * sizeof(float)));
+    KD_CK(m->alloc(&m->err, sizeof(int)));
+    KD_CK(cudaMemset(m->err, 0, sizeof(int)));
+    KD_CK(m->alloc(&m->desc, DESC_INTS * sizeof(int)));
+    KD_CK(cudaMemset(m->desc, 0, DESC_INTS * sizeof(int)));
+    KD_CK(cudaMallocHost(&m->pinned, (size_t)RING * DESC_INTS * sizeof(int32_t)));
+    for (auto& e : m->ring_ev) KD_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    KD_CK(cudaEventCreateWithFlags(&m->last_step, cudaEventDisableTiming));
+    KD_CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    m->bound.assign(S, 0);
+    m->len.assign(S, 0);
+    KD_CK(cudaDeviceSynchronize());
+    return KD_OK;
+}
+
+// The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
+static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s) {
+    const kd_config& c = m->cfg;
+    const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
+    const int F = c.ffn, V = c.vocab;
+    const int* slot = m->desc;
+    const int* tok = m->desc + KD_MAX_BATCH;
+    const int* pos = m->desc + 2 * KD_MAX_BATCH;
+    const bool pdl = m->pdl && !m->prof;
+    cudaError_t e;
+    // With measurement on, every launch is bracketed by two events (no host wait).
+    cudaEvent_t ev0 = nullptr;
+    auto mark0 = [&]() -> cudaError_t {
+        if (!m->prof) return cudaSuccess;
+        if (m->ev_pool.empty()) {
+            cudaEvent_t x;
+            cudaError_t r = cudaEventCreate(&x);
+            if (r != cudaSuccess) return r;
+            m->ev_pool.push_back(x);
+        }
+        ev0 = m->ev_pool.back();
+        m->ev_pool.pop_back();
+        return cudaEventRecord(ev0, s);
+    };
+    auto mark1 = [&](int cls) -> cudaError_t {
+        if (!m->prof) return cudaSuccess;
+        cudaEvent_t x;
+        if (m->ev_pool.empty()) {
+            cudaError_t r = cudaEventCreate(&x);
+            if (r != cudaSuccess) return r;
+        } else {
+            x = m->ev_pool.back();
+            m->ev_pool.pop_back();
+        }
+        m->prof_marks.emplace_back(cls, ev0, x);
+        return cudaEventRecord(x, s);
+    };
+#define KD_RUN(cls, launch)                                 \
+    do {                                                    \
+        if ((e = mark0()) != cudaSuccess) return e;         \
+        if ((e = (launch)) != cudaSuccess) return e;        \
+        if ((e = mark1(cls)) != cudaSuccess) return e;      \
+    } while (0)
+
+    auto mm = [&](const PackedQ8& p, const __half* x, int epi) {
+        kd::MmvqArgs a{};
+        a.w = p.w; a.G = p.G; a.KG = p.KG; a.kpt = p.kpt; a.S = p.S; a.K = p.K;
+        a.x = x; a.B = B; a.part = m->part; a.cnt = m->cnt; a.err = m->err;
+        return a;
+    };
+    KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, pdl, s));
+    if (m->hidden_dbg &&
+        (e = cudaMemcpyAsync(m->hidden_dbg, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return e;
+    for (int l = 0; l < L; ++l) {
+        __half* kc = m->kc + (size_t)l * m->layer_kv;
+        __half* vc = m->vc + (size_t)l * m->layer_kv;
+        KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * l) * H, m->xn, B, H, c.rms_eps, pdl, s));
+        kd::MmvqArgs a = mm(m->qkv[l], m->xn, kd::EPI_QKV);
+        a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
+        a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
+        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, kd::EPI_QKV, m->num_sms, pdl, s));
+        kd::AttnArgs t{};
+        t.q = m->q; t.kc = kc; t.vc = vc; t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
+        t.hd = hd; t.cap = c.max_ctx; t.scale = 1.0f / std::sqrt((float)hd); t.part = m->apart;
+        t.max_splits = m->max_splits; t.out = m->attn; t.err = m->err;
+        KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->attn_grid, pdl, s));
+        KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
+        a = mm(m->wo[l], m->attn, kd::EPI_RESID);
+        a.y = m->x; a.ld = H;
+        KD_RUN(KD_K_WO, kd::launch_mmvq(a, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * l + 1) * H, m->xn, B, H, c.rms_eps, pdl, s));
+        a = mm(m->gu[l], m->xn, kd::EPI_SWIGLU);
+        a.act = m->act; a.ld = F;
+        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, kd::EPI_SWIGLU, m->num_sms, pdl, s));
+        a = mm(m->down[l], m->act, kd::EPI_RESID);
+        a.y = m->x; a.ld = H;
+        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, kd::EPI_RESID, m->num_sms, pdl, s));
+        if (m->hidden_dbg &&
+            (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)(l + 1) * B * H, m->x, (size_t)B * H * 4,
+                                 cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+            return e;
+    }
+    KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * L) * H, m->xn, B, H, c.rms_eps, pdl, s));
+    kd::MmvqArgs a = mm(m->head, m->xn, kd::EPI_STORE);
+    a.y = lg; a.ld = V;
+    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, kd::EPI_STORE, m->num_sms, pdl, s));
+    if (am) KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, pdl, s));
+#undef KD_RUN
+    return cudaSuccess;
+}
+
+static kd_status get_graph(kd_model* m, int B, float* lg, int* am, cudaGraphExec_t* out) {
+    auto key = std::make_tuple(B, lg, am);
+    auto it = m->graphs.find(key);
+    if (it != m->graphs.end()) {
+        *out = it->second;
+        return KD_OK;
+    }
+    if (m->graphs.size() >= 64) {  // bound the cache: drop everything, recapture on demand
+        KD_CK(cudaStreamSynchronize(m->cap_stream));
+        KD_CK(cudaEventSynchronize(m->last_step));
+        for (auto& g : m->graphs) cudaGraphExecDestroy(g.second);
+        m->graphs.clear();
+    }
+    cudaGraph_t graph = nullptr;
+    KD_CK(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = enqueue_step(m, B, lg, am, m->cap_stream);
+    cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return fail(KD_ERR_CUDA, "capturing the step graph failed: %s",
+                    cudaGetErrorString(e != cudaSuccess ? e : e2));
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    KD_CK(e);
+    m->graphs[key] = exec;
+    *out = exec;
+    return KD_OK;
+}
+
+extern "C" {
+
+const char* kd_last_error(void) { return g_err.c_str(); }
+
+kd_status kd_model_load(const kd_config* cfg, const kd_weights* w, kd_model** out) {
+    if (!cfg || !w || !out) return fail(KD_ERR_INVALID_ARG, "kd_model_load: null argument");
+    *out = nullptr;
+    kd_status st = check_config(cfg);
+    if (st != KD_OK) return st;
+    if (!w->tok_embd || !w->output || !w->output_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+        !w->w_gate || !w->w_up || !w->w_down || !w->attn_norm || !w->ffn_norm)
+        return fail(KD_ERR_INVALID_ARG, "kd_model_load: null weight pointer");
+    kd_model* m = new (std::nothrow) kd_model();
+    if (!m) return fail(KD_ERR_OOM, "kd_model_load: host allocation failed");
+    m->cfg = *cfg;
+    st = load_impl(m, w);
+    if (st != KD_OK) {
+        m->release();
+        delete m;
+        return st;
+    }
+    g_err.clear();
+    *out = m;
+    return KD_OK;
+}
+
+kd_status kd_model_free(kd_model* m) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_model_free: null model");
+    cudaSetDevice(m->dev);
+    cudaEventSynchronize(m->last_step);
+    cudaStreamSynchronize(m->cap_stream);
+    m->release();
+    delete m;
+    return KD_OK;
+}
+
+kd_status kd_session_bind(kd_model* m, int32_t* id_out) {
+    if (!m || !id_out) return fail(KD_ERR_INVALID_ARG, "kd_session_bind: null argument");
+    for (size_t i = 0; i < m->bound.size(); ++i)
+        if (!m->bound[i]) {
+            m->bound[i] = 1;
+            m->len[i] = 0;
+            *id_out = (int32_t)i;
+            return KD_OK;
+        }
+    return fail(KD_ERR_NO_FREE_SLOT, "kd_session_bind: all %zu slots are bound", m->bound.size());
+}
+
+static kd_status check_session(const kd_model* m, int32_t id) {
+    if (id < 0 || id >= (int32_t)m->bound.size() || !m->bound[id])
+        return fail(KD_ERR_BAD_SESSION, "session %d is not bound", id);
+    return KD_OK;
+}
+
+kd_status kd_session_free(kd_model* m, int32_t id) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_session_free: null model");
+    kd_status st = check_session(m, id);
+    if (st != KD_OK) return st;
+    KD_CK(cudaSetDevice(m->dev));
+    KD_CK(cudaEventSynchronize(m->last_step));
+    m->bound[id] = 0;
+    m->len[id] = 0;
+    return KD_OK;
+}
+
+kd_status kd_session_length(const kd_model* m, int32_t id, int32_t* len_out) {
+    if (!m || !len_out) return fail(KD_ERR_INVALID_ARG, "kd_session_length: null argument");
+    kd_status st = check_session(m, id);
+    if (st != KD_OK) return st;
+    *len_out = m->len[id];
+    return KD_OK;
+}
+
+kd_status kd_session_load_kv(kd_model* m, int32_t id, const void* k, const void* v, int32_t len,
+                             kd_stream stream) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_session_load_kv: null model");
+    kd_status st = check_session(m, id);
+    if (st != KD_OK) return st;
+    if (len < 0 || len > m->cfg.max_ctx)
+        return fail(KD_ERR_POSITION, "kd_session_load_kv: len %d outside [0, %d]", len, m->cfg.max_ctx);
+    if (len > 0 && (!k || !v)) return fail(KD_ERR_INVALID_ARG, "kd_session_load_kv: null cache");
+    KD_CK(cudaSetDevice(m->dev));
+    cudaStream_t s = (cudaStream_t)stream;
+    KD_CK(cudaStreamWaitEvent(s, m->last_step, 0));
+    const kd_config& c = m->cfg;
+    const size_t row = (size_t)c.head_dim * sizeof(__half);
+    for (int l = 0; l < c.n_layers && len > 0; ++l) {
+        const size_t dst = (size_t)l * m->layer_kv + (size_t)id * c.n_kv_heads * c.max_ctx * c.head_dim;
+        const size_t src = (size_t)l * c.n_kv_heads * len * c.head_dim;
+        KD_CK(cudaMemcpy2DAsync(m->kc + dst, c.max_ctx * row, (const __half*)k + src, len * row, len * row,
+                                c.n_kv_heads, cudaMemcpyDefault, s));
+        KD_CK(cudaMemcpy2DAsync(m->vc + dst, c.max_ctx * row, (const __half*)v + src, len * row, len * row,
+                                c.n_kv_heads, cudaMemcpyDefault, s));
+    }
+    KD_CK(cudaEventRecord(m->last_step, s));
+    m->len[id] = len;
+    return KD_OK;
+}
+
+kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
+                         int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null model");
+    if (B < 1 || B > KD_MAX_BATCH)
+        return fail(KD_ERR_BATCH, "kd_decode_step: B=%d outside [1, %d]", B, KD_MAX_BATCH);
+    if (!ids || !tokens || !positions) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
+    const kd_config& c = m->cfg;
+    for (int b = 0; b < B; ++b) {
+        kd_status st = check_session(m, ids[b]);
+        if (st != KD_OK) return st;
+        for (int j = 0; j < b; ++j)
+            if (ids[j] == ids[b]) return fail(KD_ERR_BAD_SESSION, "session %d appears twice in one step", ids[b]);
+        if (tokens[b] < 0 || tokens[b] >= c.vocab)
+            return fail(KD_ERR_INVALID_ARG, "token %d of row %d outside [0, %d)", tokens[b], b, c.vocab);
+        if (positions[b] < 0 || positions[b] > m->len[ids[b]] || positions[b] >= c.max_ctx)
+            return fail(KD_ERR_POSITION, "position %d of session %d: length is %d, capacity %d", positions[b],
+                        ids[b], m->len[ids[b]], c.max_ctx);
+    }
+    KD_CK(cudaSetDevice(m->dev));
+    cudaStream_t s = (cudaStream_t)stream;
+    // Stage the descriptor through a pinned ring slot no earlier copy still reads.
+    const int ri = m->ring_i;
+    KD_CK(cudaEventSynchronize(m->ring_ev[ri]));
+    int32_t* d = m->pinned + (size_t)ri * DESC_INTS;
+    std::memset(d, 0, DESC_INTS * sizeof(int32_t));
+    for (int b = 0; b < B; ++b) {
+        d[b] = ids[b];
+        d[KD_MAX_BATCH + b] = tokens[b];
+        d[2 * KD_MAX_BATCH + b] = positions[b];
+    }
+    KD_CK(cudaStreamWaitEvent(s, m->last_step, 0));
+    KD_CK(cudaMemcpyAsync(m->desc, d, DESC_INTS * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    KD_CK(cudaEventRecord(m->ring_ev[ri], s));
+    m->ring_i = (ri + 1) % RING;
+
+    float* lg = logits_out ? logits_out : m->logits_ws;
+    if (m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH)) {
+        KD_CK(enqueue_step(m, B, lg, argmax_out, s));
+    } else {
+        cudaGraphExec_t g = nullptr;
+        kd_status st = get_graph(m, B, lg, argmax_out, &g);
+        if (st != KD_OK) return st;
+        KD_CK(cudaGraphLaunch(g, s));
+    }
+    KD_CK(cudaEventRecord(m->last_step, s));
+    for (int b = 0; b < B; ++b) m->len[ids[b]] = positions[b] + 1;
+    return KD_OK;
+}
+
+kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_debug_capture_hidden: null model");
+    m->hidden_dbg = dev_buf;
+    return KD_OK;
+}
+
+kd_status kd_profile_enable(kd_model* m, int32_t on) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_profile_enable: null model");
+    m->prof = on != 0;
+    return KD_OK;
+}
+
+kd_status kd_profile_read(kd_model* m, int32_t* launches, double* ms) {
+    if (!m || !launches || !ms) return fail(KD_ERR_INVALID_ARG, "kd_profile_read: null argument");
+    KD_CK(cudaSetDevice(m->dev));
+    KD_CK(cudaEventSynchronize(m->last_step));
+    for (int i = 0; i < KD_K_COUNT; ++i) {
+        launches[i] = 0;
+        ms[i] = 0.0;
+    }
+    cudaError_t first = cudaSuccess;
+    for (auto& t : m->prof_marks) {
+        float x = 0.0f;
+        cudaError_t e = cudaEventElapsedTime(&x, std::get<1>(t), std::get<2>(t));
+        if (e != cudaSuccess && first == cudaSuccess) first = e;
+        launches[std::get<0>(t)] += 1;
+        ms[std::get<0>(t)] += x;
+        m->ev_pool.push_back(std::get<1>(t));
+        m->ev_pool.push_back(std::get<2>(t));
+    }
+    m->prof_marks.clear();
+    KD_CK(first);
+    return KD_OK;
+}
+
+kd_status kd_device_status(kd_model* m, int32_t* flags_out) {
+    if (!m || !flags_out) return fail(KD_ERR_INVALID_ARG, "kd_device_status: null argument");
+    KD_CK(cudaSetDevice(m->dev));
+    KD_CK(cudaEventSynchronize(m->last_step));
+    int v = 0;
+    KD_CK(cudaMemcpy(&v, m->err, sizeof(int), cudaMemcpyDeviceToHost));
+    KD_CK(cudaMemset(m->err, 0, sizeof(int)));
+    *flags_out = v;
+    if (v) return fail(KD_ERR_DEVICE, "a kernel gave up a bounded wait (flags 0x%x)", v);
+    return KD_OK;
+}
+
+// ------------------------------------------------------------- op level ----
+struct kd_q8_matrix {
+    PackedQ8 p;
+    float* part = nullptr;
+    int* cnt = nullptr;
+    int* err = nullptr;
+    int dev = 0, num_sms = 0;
+};
+
+kd_status kd_q8_matrix_create(const void* host, int32_t rows, int32_t cols, kd_q8_matrix** out) {
+    if (!host || !out) return fail(KD_ERR_INVALID_ARG, "kd_q8_matrix_create: null argument");
+    *out = nullptr;
+    if (rows < kd::GROUP_ROWS || rows % kd::GROUP_ROWS || cols < kd::KGROUP || cols % kd::KGROUP)
+        return fail(KD_ERR_UNSUPPORTED, "kd_q8_matrix_create: need rows %% 32 == 0 and cols %% 128 == 0 (got %d x %d)",
+                    rows, cols);
+    kd_q8_matrix* w = new (std::nothrow) kd_q8_matrix();
+    if (!w) return fail(KD_ERR_OOM, "host allocation failed");
+    auto cleanup = [&](kd_status st) {
+        cudaFree(w->p.w);
+        cudaFree(w->part);
+        cudaFree(w->cnt);
+        cudaFree(w->err);
+        delete w;
+        return st;
+    };
+    uint8_t* staging = nullptr;
+    int* d_tiles = nullptr;
+    if (cudaGetDevice(&w->dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&w->num_sms, cudaDevAttrMultiProcessorCount, w->dev) != cudaSuccess ||
+        init_device_attributes(w->dev) != cudaSuccess)
+        return cleanup(fail(KD_ERR_CUDA, "kd_q8_matrix_create: no usable CUDA device"));
+    if (cudaMalloc(&staging, (size_t)rows * q8_row_bytes(cols)) != cudaSuccess ||
+        cudaMalloc(&d_tiles, (size_t)rows / kd::TILE_ROWS * sizeof(int)) != cudaSuccess) {
+        cudaFree(staging);
+        return cleanup(fail(KD_ERR_OOM, "kd_q8_matrix_create: device allocation failed"));
+    }
+    kd_status st = upload_packed({{host, rows}}, cols, tiles_natural(rows), staging, d_tiles, w->p);
+    cudaFree(staging);
+    cudaFree(d_tiles);
+    if (st != KD_OK) return cleanup(st);
+    if (cudaMalloc(&w->part, std::max<size_t>(w->p.part_floats(), 4) * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&w->cnt, (size_t)w->p.G * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&w->err, sizeof(int)) != cudaSuccess)
+        return cleanup(fail(KD_ERR_OOM, "kd_q8_matrix_create: workspace allocation failed"));
+    if (cudaMemset(w->cnt, 0, (size_t)w->p.G * sizeof(int)) != cudaSuccess ||
+        cudaMemset(w->err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return cleanup(fail(KD_ERR_CUDA, "kd_q8_matrix_create: workspace init failed"));
+    *out = w;
+    return KD_OK;
+}
+
+kd_status kd_q8_matrix_free(kd_q8_matrix* w) {
+    if (!w) return fail(KD_ERR_INVALID_ARG, "kd_q8_matrix_free: null matrix");
+    cudaDeviceSynchronize();
+    cudaFree(w->p.w);
+    cudaFree(w->part);
+    cudaFree(w->cnt);
+    cudaFree(w->err);
+    delete w;
+    return KD_OK;
+}
+
+kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y, kd_stream stream) {
+    if (!w || !x || !y) return fail(KD_ERR_INVALID_ARG, "kd_mmvq: null argument");
+    if (m < 1 || m > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_mmvq: m=%d outside [1, %d]", m, KD_MAX_BATCH);
+    kd::MmvqArgs a{};
+    a.w = w->p.w; a.G = w->p.G; a.KG = w->p.KG; a.kpt = w->p.kpt; a.S = w->p.S; a.K = w->p.K;
+    a.x = reinterpret_cast<const __half*>(x); a.B = m; a.part = w->part; a.cnt = w->cnt; a.err = w->err;
+    a.y = y; a.ld = w->p.rows;
+    KD_CK(kd::launch_mmvq(a, kd::EPI_STORE, w->num_sms, false, (cudaStream_t)stream));
+    return KD_OK;
+}
+
+size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap) {
+    if (B < 1 || n_heads < 1 || head_dim < 1 || cap < 1) return 0;
+    const size_t splits = (size_t)(cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
+    return 256 + (size_t)B * n_heads * splits * (head_dim + 2) * sizeof(float);
+}
+
+kd_status kd_attn_append_decode(const float* q, const float* k_new, const float* v_new, uint16_t* k_cache,
+                                uint16_t* v_cache, const int32_t* slots, const int32_t* positions, int32_t B,
+                                int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t n_slots,
+                                int32_t cap, uint16_t* out, void* workspace, size_t workspace_bytes,
+                                kd_stream stream) {
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !slots || !positions || !out || !workspace)
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: null argument");
+    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_attn_append_decode: B=%d", B);
+    if (n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads || !kd::attn_supported(head_dim, n_heads / n_kv_heads))
+        return fail(KD_ERR_UNSUPPORTED, "kd_attn_append_decode: head_dim %d, group %d", head_dim,
+                    n_kv_heads > 0 ? n_heads / n_kv_heads : 0);
+    if (n_slots < 1 || cap < 1) return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: n_slots/cap");
+    if (workspace_bytes < kd_attn_workspace_bytes(B, n_heads, head_dim, cap))
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: workspace too small");
+    if (((uintptr_t)workspace | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: buffers must be 16-byte aligned");
+    int32_t desc[2 * KD_MAX_BATCH] = {};
+    for (int b = 0; b < B; ++b) {
+        if (slots[b] < 0 || slots[b] >= n_slots) return fail(KD_ERR_BAD_SESSION, "slot %d", slots[b]);
+        for (int j = 0; j < b; ++j)
+            if (slots[j] == slots[b]) return fail(KD_ERR_BAD_SESSION, "slot %d repeated", slots[b]);
+        if (positions[b] < 0 || positions[b] >= cap)
+            return fail(KD_ERR_POSITION, "position %d outside [0, %d)", positions[b], cap);
+        desc[b] = slots[b];
+        desc[KD_MAX_BATCH + b] = positions[b];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0, sms = 0;
+    KD_CK(cudaGetDevice(&dev));
+    KD_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    KD_CK(init_device_attributes(dev));
+    int* d_desc = (int*)workspace;
+    int* d_err = d_desc + 2 * KD_MAX_BATCH;
+    KD_CK(cudaMemcpyAsync(d_desc, desc, sizeof desc, cudaMemcpyHostToDevice, s));
+    KD_CK(cudaMemsetAsync(d_err, 0, sizeof(int), s));
+    KD_CK(kd::launch_kv_append(k_new, v_new, (__half*)k_cache, (__half*)v_cache, d_desc, d_desc + KD_MAX_BATCH, B,
+                               n_kv_heads, head_dim, cap, s));
+    kd::AttnArgs t{};
+    t.q = q; t.kc = (const __half*)k_cache; t.vc = (const __half*)v_cache; t.slot = d_desc;
+    t.pos = d_desc + KD_MAX_BATCH; t.B = B; t.nh = n_heads; t.nkv = n_kv_heads; t.hd = head_dim; t.cap = cap;
+    t.scale = 1.0f / std::sqrt((float)head_dim);
+    t.part = (float*)((char*)workspace + 256);
+    t.max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
+    t.out = (__half*)out;
+    t.err = d_err;
+    KD_CK(kd::launch_attn_split(t, kd::attn_split_grid(sms, head_dim, n_heads / n_kv_heads), false, s));
+    KD_CK(kd::launch_attn_combine(t, false, s));
+    return KD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+"""The whole batched decode step through the C ABI, on the tiny model.
+
+Workload: the tiny oracle model (1 layer, hidden 256, 4/2 heads of 64, FFN 768,
+vocab 512, RoPE theta 1e4, Q8_0 weights as generated), B = 2 sessions with 17
+and 40 pre-filled fp16 positions, 4 greedy steps, seed 0.
+
+Gates: teacher-forced logits within 5e-2 (max abs) of the oracle and per-layer
+hidden states within 1e-3 relative L2; every session's greedy stream and logits
+bit-identical to its isolated B = 1 run; graph replay identical to the direct
+launch train."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+LOGIT_TOL = 5e-2
+HIDDEN_REL_L2 = 1e-3
+
+
+def load(kd, shape, w, max_sessions, cap, flags=0):
+    return kd.kd_model_load(kd.make_config(shape, max_sessions, cap, flags), w)
+
+
+def bind_prefilled(kd, m, shape, lens, seed=0, first_session=0):
+    ids = []
+    for i, n in enumerate(lens):
+        k, v = synth.kv_prefill(shape, seed, first_session + i, n)
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, k, v, n)
+        ids.append(sid)
+    return ids
+
+
+def gpu_step(kd, m, ids, tok, pos, V):
+    B = len(ids)
+    lg = torch.empty(B, V, device="cuda", dtype=torch.float32)
+    am = torch.empty(B, device="cuda", dtype=torch.int32)
+    kd.kd_decode_step(m, ids, tok, pos, lg, am)
+    torch.cuda.synchronize()
+    return lg.cpu().numpy(), am.cpu().numpy()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    shape = synth.TINY
+    return shape, synth.model_weights(shape, 0)
+
+
+def test_tiny_teacher_forced_against_oracle(kdlib, tiny):
+    kd = kdlib
+    shape, w = tiny
+    case = synth.TINY_CASE
+    cap = 64
+    m = load(kd, shape, w, 4, cap)
+    try:
+        lens = list(case["prefill"])
+        ids = bind_prefilled(kd, m, shape, lens)
+        om = oracle.OracleModel(shape, w)
+        caches = [om.new_cache(cap, *synth.kv_prefill(shape, 0, i, n)) for i, n in enumerate(lens)]
+        B, L, H = len(lens), shape.n_layers, shape.hidden
+        hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+        kd.kd_debug_capture_hidden(m, hid)
+        tok = synth.tokens(0, "tiny-steps", B, shape.vocab)
+        for step in range(case["steps"]):
+            pos = [n + step for n in lens]
+            lg, am = gpu_step(kd, m, ids, tok, pos, shape.vocab)
+            ref, ref_am, ref_h = om.step(tok, pos, caches, cap, want_hidden=True)
+            assert np.abs(lg - ref).max() <= LOGIT_TOL, (step, float(np.abs(lg - ref).max()))
+            gh = hid.cpu().numpy()
+            for b in range(B):
+                for l in range(L + 1):
+                    rel = np.linalg.norm(gh[l, b] - ref_h[b, l]) / np.linalg.norm(ref_h[b, l])
+                    assert rel <= HIDDEN_REL_L2, (step, b, l, rel)
+            for b in range(B):
+                assert kd.kd_session_length(m, ids[b]) == pos[b] + 1
+            tok = ref_am  # teacher forcing: the oracle's greedy token feeds the next step
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
+def greedy_stream(kd, m, ids, lens, tok0, steps, V):
+    tok = np.array(tok0, np.int32)
+    toks, logits = [], []
+    for s in range(steps):
+        lg, am = gpu_step(kd, m, ids, tok, [n + s for n in lens], V)
+        toks.append(am.copy())
+        logits.append(lg.copy())
+        tok = am
+    return np.array(toks), np.array(logits)
+
+
+@pytest.mark.parametrize("flags", [0, 1])  # CUDA-graph replay, then kernel-by-kernel launches
+def test_tiny_batch_invariance(kdlib, tiny, flags):
+    kd = kdlib
+    shape, w = tiny
+    cap, steps = 64, 8
+    lens = [17, 40, 3, 9, 25]
+    tok0 = synth.tokens(0, "tiny-inv", len(lens), shape.vocab)
+    m = load(kd, shape, w, 8, cap, flags)
+    try:
+        ids = bind_prefilled(kd, m, shape, lens)
+        batch_t, batch_l = greedy_stream(kd, m, ids, lens, tok0, steps, shape.vocab)
+        for b in range(len(lens)):
+            kd.kd_session_free(m, ids[b])
+        for b in range(len(lens)):
+            (sid,) = bind_prefilled(kd, m, shape, [lens[b]], first_session=b)
+            t1, l1 = greedy_stream(kd, m, [sid], [lens[b]], tok0[b:b + 1], steps, shape.vocab)
+            assert np.array_equal(t1[:, 0], batch_t[:, b]), b
+            assert np.array_equal(l1[:, 0].view(np.uint32), batch_l[:, b].view(np.uint32)), b
+            kd.kd_session_free(m, sid)
+    finally:
+        kd.kd_model_free(m)
+
+
+def test_tiny_graph_equals_direct_and_rewind(kdlib, tiny):
+    kd = kdlib
+    shape, w = tiny
+    cap, lens = 64, [17, 40]
+    tok = synth.tokens(0, "tiny-gd", 2, shape.vocab)
+    out = []
+    for flags in (0, 1):
+        m = load(kd, shape, w, 4, cap, flags)
+        try:
+            ids = bind_prefilled(kd, m, shape, lens)
+            a = gpu_step(kd, m, ids, tok, lens, shape.vocab)
+            gpu_step(kd, m, ids, tok[::-1].copy(), [n + 1 for n in lens], shape.vocab)
+            # rewind both sessions to their first decode position: same inputs, same bits
+            b = gpu_step(kd, m, ids, tok, lens, shape.vocab)
+            assert np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32))
+            assert kd.kd_session_length(m, ids[0]) == lens[0] + 1
+            out.append(a[0])
+        finally:
+            kd.kd_model_free(m)
+    assert np.array_equal(out[0].view(np.uint32), out[1].view(np.uint32))
+
+
+def test_tiny_errors_change_no_state(kdlib, tiny):
+    kd = kdlib
+    shape, w = tiny
+    m = load(kd, shape, w, 2, 32)
+    try:
+        a = kd.kd_session_bind(m)
+        b = kd.kd_session_bind(m)
+        with pytest.raises(kd.KdError) as e:
+            kd.kd_session_bind(m)
+        assert e.value.name == "KD_ERR_NO_FREE_SLOT"
+        cases = [
+            (dict(session_ids=[a, a], tokens=[1, 2], positions=[0, 0]), "KD_ERR_BAD_SESSION"),
+            (dict(session_ids=[a, 7], tokens=[1, 2], positions=[0, 0]), "KD_ERR_BAD_SESSION"),
+            (dict(session_ids=[a], tokens=[shape.vocab], positions=[0]), "KD_ERR_INVALID_ARG"),
+            (dict(session_ids=[a], tokens=[-1], positions=[0]), "KD_ERR_INVALID_ARG"),
+            (dict(session_ids=[a], tokens=[1], positions=[1]), "KD_ERR_POSITION"),
+            (dict(session_ids=[a], tokens=[1], positions=[-1]), "KD_ERR_POSITION"),
+            (dict(session_ids=list(range(17)), tokens=[1] * 17, positions=[0] * 17), "KD_ERR_BATCH"),
+            (dict(session_ids=[], tokens=[], positions=[]), "KD_ERR_BATCH"),
+        ]
+        for kw, name in cases:
+            with pytest.raises(kd.KdError) as e:
+                kd.kd_decode_step(m, **kw)
+            assert e.value.name == name, (kw, e.value)
+        assert kd.kd_session_length(m, a) == 0 and kd.kd_session_length(m, b) == 0
+        kd.kd_decode_step(m, [a, b], [1, 2], [0, 0])
+        assert kd.kd_session_length(m, a) == 1
+        with pytest.raises(kd.KdError) as e:  # capacity 32: position 32 is out of range
+            kd.kd_session_load_kv(m, a, None, None, 33)
+        assert e.value.name == "KD_ERR_POSITION"
+        kd.kd_session_free(m, a)
+        with pytest.raises(kd.KdError):
+            kd.kd_session_length(m, a)
+        assert kd.kd_session_bind(m) == a  # lowest free slot, length 0 again
+        assert kd.kd_session_length(m, a) == 0
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
