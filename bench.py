@@ -55,7 +55,8 @@ def step_bytes(s, positions):
 
 
 def kernels_per_step(s, with_argmax=True):
-    return 1 + s.n_layers * 8 + 2 + (1 if with_argmax else 0)
+    # embed; per layer qkv, attention split, combine, o-proj, norm, gate|up, down, norm; lm_head; argmax
+    return 1 + s.n_layers * 8 + 1 + (1 if with_argmax else 0)
 
 
 def read_peaks():
@@ -303,6 +304,88 @@ def cpu_baseline(shape, w, B):
                       f"OpenMP over rows), {dt:.1f} s"}
 
 
+# --------------------------------------------------------------- op-level modes
+def run_op_mmvq(args):
+    """Isolated Q8_0 mmvq (rows x cols weights, m fp16 activation rows ~N(0,1)).
+    Distinct weight copies totalling more than 4x L2 are rotated, so every launch
+    streams its weights from HBM."""
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    R, K, m = args.rows, args.cols, args.m
+    wbytes = R * K * 34 // 32
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = max(2, -(-4 * l2 // wbytes))
+    base = synth.q8_0_matrix(0, f"op-{R}x{K}", R, K)
+    hs = []
+    for c in range(copies):  # distinct bytes per copy: rotate the quants, keep the scales
+        w = base.copy()
+        w[:, :, 2:] = np.roll(base[:, :, 2:], c, axis=2)
+        hs.append(kd.kd_q8_matrix_create(w))
+    x = torch.from_numpy(synth.activations_fp16(0, "op-x", m, K).view(np.int16)).cuda()
+    y = torch.empty(m, R, device="cuda", dtype=torch.float32)
+    st = torch.cuda.current_stream()
+    for i in range(max(3, args.warmup)):
+        kd.kd_mmvq(hs[i % copies], x, m, y, st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        kd.kd_mmvq(hs[i % copies], x, m, y, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    alg = wbytes + m * K * 2 + m * R * 4
+    peak, kind = read_peaks()
+    for h in hs:
+        kd.kd_q8_matrix_free(h)
+    return {"op": "mmvq", "rows": R, "cols": K, "m": m, "copies": copies, "launches": args.steps,
+            "avg_us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1), "peak": peak,
+            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4)}
+
+
+def run_op_attn(args):
+    """Isolated KV append + ragged split-K flash-decode: 32/8 heads of 128, B sessions with
+    attended lengths uniform in [1, cap] (seeded), fp16 KV ~N(0,1)."""
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    c = synth.RAGGED_ATTN_CASE
+    nh, nkv, hd, cap, B = c["n_heads"], c["n_kv_heads"], c["head_dim"], args.cap, args.m
+    lens = synth.ragged_lengths(0, "attn-config", B, 1, cap)
+    kc = torch.randn(B, nkv, cap, hd, device="cuda", dtype=torch.float32).to(torch.float16)
+    vc = torch.randn(B, nkv, cap, hd, device="cuda", dtype=torch.float32).to(torch.float16)
+    q = torch.randn(B, nh, hd, device="cuda")
+    kn = torch.randn(B, nkv, hd, device="cuda")
+    vn = torch.randn(B, nkv, hd, device="cuda")
+    out = torch.empty(B, nh * hd, dtype=torch.float16, device="cuda")
+    ws = torch.empty(kd.kd_attn_workspace_bytes(B, nh, hd, cap), dtype=torch.uint8, device="cuda")
+    slots = np.arange(B, dtype=np.int32)
+    pos = (lens - 1).astype(np.int32)
+    st = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    alg = int(lens.sum()) * nkv * hd * 2 * 2 + B * nkv * hd * 2 * 2
+    peak, kind = read_peaks()
+    return {"op": "attn_append_decode", "B": B, "cap": cap, "sum_t_kv": int(lens.sum()), "launches": args.steps,
+            "avg_us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1), "peak": peak,
+            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4)}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The oracle timed as it stands on the host cores, one layer of one session per step."""
@@ -353,7 +436,16 @@ def main():
     ap.add_argument("--impl", default="kd", choices=["kd", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["mmvq", "attn"], help="time one kernel family in isolation")
+    ap.add_argument("--rows", type=int, default=4096)
+    ap.add_argument("--cols", type=int, default=14336)
+    ap.add_argument("--m", type=int, default=8)
+    ap.add_argument("--cap", type=int, default=32768)
     args = ap.parse_args()
+    if args.op:
+        r = run_op_mmvq(args) if args.op == "mmvq" else run_op_attn(args)
+        print(json.dumps(r), flush=True)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

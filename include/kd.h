@@ -57,8 +57,9 @@ typedef struct kd_model kd_model; /* opaque, library-owned */
 
 /* Model shape.  Requirements (else KD_ERR_UNSUPPORTED): hidden, ffn and
  * n_heads*head_dim are multiples of 128; head_dim is 64 or 128; n_heads is
- * 1, 2, 4 or 8 times n_kv_heads; vocab is a multiple of 32.  All sizes and
- * max_sessions, max_ctx are >= 1 (else KD_ERR_INVALID_ARG).
+ * 1, 2, 4 or 8 times n_kv_heads; vocab is a multiple of 32; max_ctx is at
+ * most 65536.  All sizes and max_sessions, max_ctx are >= 1 (else
+ * KD_ERR_INVALID_ARG).
  * rope_theta is the NeoX RoPE base; rms_eps the RMSNorm epsilon. */
 typedef struct {
     int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
@@ -69,6 +70,11 @@ typedef struct {
 } kd_config;
 
 #define KD_FLAG_NO_GRAPH 1  /* launch each kernel every step instead of replaying a CUDA graph */
+/* Force one projection schedule for every matrix (coverage testing; results stay
+ * exact per row for every B, but the fp32 summation order differs between the
+ * two schedules).  Default: chosen per matrix from its shape and the SM count. */
+#define KD_FLAG_SCHEDULE_STREAM 2
+#define KD_FLAG_SCHEDULE_GROUP 4
 
 /* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
  * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the
@@ -142,6 +148,17 @@ kd_status kd_decode_step(kd_model* m, const int32_t* session_ids, const int32_t*
  * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off. */
 kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf);
 
+/* Debug: run decoder layer `layer` alone on the residual rows x_in (device or
+ * host fp32 [B][hidden]) for the given sessions at the given positions (same
+ * rules as kd_decode_step), writing the layer's output rows to x_out (device or
+ * host fp32 [B][hidden]).  Writes that layer's K/V row at each position; does
+ * not change any session's length.  The same kernels as a step run, so a layer
+ * can be checked on its own against a reference, without errors carried in from
+ * the layers before it.  Enqueued on `stream`. */
+kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* session_ids,
+                         const int32_t* positions, int32_t B, const float* x_in,
+                         float* x_out, kd_stream stream);
+
 /* Wait for the model's work, then read and clear its device fault word.
  * *flags_out = 0 when no kernel gave up a bounded wait; KD_ERR_DEVICE is
  * returned when one did. */
@@ -153,6 +170,8 @@ kd_status kd_device_status(kd_model* m, int32_t* flags_out);
  * step's stream.  kd_profile_read waits for the model's work, then returns per
  * kernel class (KD_K_*) the number of launches and their summed device time in
  * milliseconds since the previous read, and resets the sums. */
+/* (KD_K_RMSNORM: the elementwise norm between a residual writer and the next
+ * projection; its row reductions are fused into the residual writer.) */
 enum {
     KD_K_EMBED = 0, KD_K_RMSNORM, KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO,
     KD_K_GATE_UP, KD_K_DOWN, KD_K_LM_HEAD, KD_K_ARGMAX, KD_K_COUNT

@@ -70,6 +70,7 @@ def lib():
             "kd_session_length": [_vp, i32, i32p],
             "kd_decode_step": [_vp, i32p, i32p, i32p, i32, _vp, _vp, _vp],
             "kd_debug_capture_hidden": [_vp, _vp],
+            "kd_debug_layer": [_vp, i32, i32p, i32p, i32, _vp, _vp, _vp],
             "kd_device_status": [_vp, i32p],
             "kd_profile_enable": [_vp, i32],
             "kd_profile_read": [_vp, i32p, C.POINTER(C.c_double)],
@@ -210,6 +211,14 @@ def kd_decode_step(m, session_ids, tokens, positions, logits_out=None, argmax_ou
 
 def kd_debug_capture_hidden(m, buf):
     _check(lib().kd_debug_capture_hidden(m, _ptr(buf)))
+
+
+def kd_debug_layer(m, layer: int, session_ids, positions, x_in, x_out, stream=None):
+    ids = _i32(session_ids)
+    pos = _i32(positions, ids.size)
+    i32p = C.POINTER(C.c_int32)
+    _check(lib().kd_debug_layer(m, int(layer), ids.ctypes.data_as(i32p), pos.ctypes.data_as(i32p), ids.size,
+                                _ptr(x_in), _ptr(x_out), _stream(stream)))
 
 
 def kd_device_status(m) -> int:

@@ -60,6 +60,7 @@ cudaError_t init_device_attributes(int dev) {
     std::call_once(g_attr_once[dev], [dev] {
         cudaError_t e = kd::mmvq_init_attributes();
         if (e == cudaSuccess) e = kd::attn_init_attributes();
+        if (e == cudaSuccess) e = kd::rowops_init_attributes();
         g_attr_err[dev] = e;
     });
     return g_attr_err[dev];
@@ -96,8 +97,8 @@ size_t q8_row_bytes(int K) { return (size_t)(K / 32) * 34; }
 
 // Upload canonical Q8_0 parts (stacked by rows) through `staging`, then repack.
 kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, int K,
-                        const std::vector<int>& tile_src, uint8_t* staging, int* d_tiles,
-                        PackedQ8& out) {
+                        const std::vector<int>& tile_src, uint8_t* staging, int* d_tiles, int num_sms,
+                        PackedQ8& out, int force_mode = -1) {
     size_t off = 0;
     int rows = 0;
     for (auto& p : parts) {
@@ -111,7 +112,7 @@ kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, i
     out.rows = rows;
     out.G = (int)tile_src.size() / kd::MT;
     out.KG = K / kd::KGROUP;
-    kd::choose_split(out);
+    kd::plan_split(out, num_sms, force_mode);
     KD_CK(cudaMalloc(&out.w, out.bytes()));
     KD_CK(cudaMemcpy(d_tiles, tile_src.data(), tile_src.size() * sizeof(int), cudaMemcpyHostToDevice));
     KD_CK(kd::launch_repack(staging, K, d_tiles, out.G, out.w, 0));
@@ -133,8 +134,10 @@ struct kd_model {
     __half* kc = nullptr;     // [L][slots][nkv][cap][hd]
     __half* vc = nullptr;
     size_t layer_kv = 0;      // elements per layer of one arena
+    kd::AttnMaps kmaps{};     // tensor maps over the K arena
     float* x = nullptr;       // [16][H] residual stream
-    __half* xn = nullptr;     // [16][H] normed activations
+    __half* xn = nullptr;     // [16][H] normed activations (written by the fused RMSNorm)
+    float* ssq = nullptr;     // [H/32][16] per-group sums of squares of the residual rows
     float* q = nullptr;       // [16][nh][hd]
     __half* attn = nullptr;   // [16][nh*hd]
     __half* act = nullptr;    // [16][F]
@@ -226,22 +229,24 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
         return fail(KD_ERR_OOM, "tile map allocation failed");
     }
     kd_status st = KD_OK;
+    const int fm = (c.flags & KD_FLAG_SCHEDULE_STREAM) ? kd::MMVQ_STREAM
+                 : (c.flags & KD_FLAG_SCHEDULE_GROUP) ? kd::MMVQ_GROUP : -1;
     m->qkv.resize(L);
     m->wo.resize(L);
     m->gu.resize(L);
     m->down.resize(L);
     for (int l = 0; l < L && st == KD_OK; ++l) {
         st = upload_packed({{w->wq[l], nh * hd}, {w->wk[l], nkv * hd}, {w->wv[l], nkv * hd}}, H,
-                           tiles_qkv(nh + 2 * nkv, hd), staging, d_tiles, m->qkv[l]);
+                           tiles_qkv(nh + 2 * nkv, hd), staging, d_tiles, m->num_sms, m->qkv[l], fm);
         if (st == KD_OK)
-            st = upload_packed({{w->wo[l], H}}, nh * hd, tiles_natural(H), staging, d_tiles, m->wo[l]);
+            st = upload_packed({{w->wo[l], H}}, nh * hd, tiles_natural(H), staging, d_tiles, m->num_sms, m->wo[l], fm);
         if (st == KD_OK)
             st = upload_packed({{w->w_gate[l], F}, {w->w_up[l], F}}, H, tiles_swiglu(F), staging, d_tiles,
-                               m->gu[l]);
+                               m->num_sms, m->gu[l], fm);
         if (st == KD_OK)
-            st = upload_packed({{w->w_down[l], H}}, F, tiles_natural(H), staging, d_tiles, m->down[l]);
+            st = upload_packed({{w->w_down[l], H}}, F, tiles_natural(H), staging, d_tiles, m->num_sms, m->down[l], fm);
     }
-    if (st == KD_OK) st = upload_packed({{w->output, V}}, H, tiles_natural(V), staging, d_tiles, m->head);
+    if (st == KD_OK) st = upload_packed({{w->output, V}}, H, tiles_natural(V), staging, d_tiles, m->num_sms, m->head, fm);
     cudaFree(staging);
     cudaFree(d_tiles);
     if (st != KD_OK) return st;
@@ -277,9 +282,12 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->vc, (size_t)L * m->layer_kv * sizeof(__half)));
     KD_CK(cudaMemset(m->kc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
     KD_CK(cudaMemset(m->vc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
+    KD_CK(kd::make_attn_maps(m->kc, (long)L * S * nkv * cap, hd, &m->kmaps));
     const int MB = KD_MAX_BATCH;
     KD_CK(m->alloc(&m->x, (size_t)MB * H * sizeof(float)));
     KD_CK(m->alloc(&m->xn, (size_t)MB * H * sizeof(__half)));
+    KD_CK(m->alloc(&m->ssq, (size_t)(H / kd::GROUP_ROWS) * kd::MAX_NORM_SLOTS * sizeof(float)));
+
     KD_CK(m->alloc(&m->q, (size_t)MB * nh * hd * sizeof(float)));
     KD_CK(m->alloc(&m->attn, (size_t)MB * nh * hd * sizeof(__half)));
     KD_CK(m->alloc(&m->act, (size_t)MB * F * sizeof(__half)));
@@ -294,7 +302,9 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->cnt, (size_t)max_g * sizeof(int)));
     KD_CK(cudaMemset(m->cnt, 0, (size_t)max_g * sizeof(int)));
     m->max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
-    KD_CK(m->alloc(&m->apart, (size_t)MB * nh * m->max_splits * (hd + 2) * sizeof(float)));
+    if (m->max_splits > kd::ATT_MAX_SPLITS)
+        return fail(KD_ERR_UNSUPPORTED, "max_ctx %d exceeds %d positions", cap, kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
+    KD_CK(m->alloc(&m->apart, (size_t)MB * nh * m->max_splits * kd::ATT_REC(hd) * sizeof(float)));
     KD_CK(m->alloc(&m->logits_ws, (size_t)MB * V * sizeof(float)));
     KD_CK(m->alloc(&m->err, sizeof(int)));
     KD_CK(cudaMemset(m->err, 0, sizeof(int)));
@@ -311,7 +321,9 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
 }
 
 // The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
-static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s) {
+// With only_layer >= 0: that layer alone, on residual rows already in m->x whose
+// full-row sums of squares are in m->ssq (one group); no embedding, no head.
+static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1) {
     const kd_config& c = m->cfg;
     const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
     const int F = c.ffn, V = c.vocab;
@@ -354,49 +366,63 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         if ((e = mark1(cls)) != cudaSuccess) return e;      \
     } while (0)
 
-    auto mm = [&](const PackedQ8& p, const __half* x, int epi) {
+    auto mm = [&](const PackedQ8& p, const __half* x) {
         kd::MmvqArgs a{};
-        a.w = p.w; a.G = p.G; a.KG = p.KG; a.kpt = p.kpt; a.S = p.S; a.K = p.K;
+        a.w = p.w; a.G = p.G; a.KG = p.KG; a.W = p.W; a.maxc = p.maxc; a.K = p.K;
         a.x = x; a.B = B; a.part = m->part; a.cnt = m->cnt; a.err = m->err;
         return a;
     };
-    KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, pdl, s));
-    if (m->hidden_dbg &&
+    // RMSNorm: the embedding writes the first normed input itself; the residual
+    // writers (o-proj, down) leave per-group sums of squares, and an elementwise
+    // kernel forms the next projection's normed fp16 input m->xn from them.
+    auto resid = [&](kd::MmvqArgs& a) {
+        a.y = m->x; a.ld = H; a.ssq_out = m->ssq;
+    };
+    auto norm = [&](const float* w) {
+        return kd::launch_norm_from_ssq(m->x, m->ssq, B, H, w, c.rms_eps, m->xn, pdl, s);
+    };
+    const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
+    const bool whole = only_layer < 0;
+    if (whole)
+        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, pdl, s));
+    if (whole && m->hidden_dbg &&
         (e = cudaMemcpyAsync(m->hidden_dbg, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
-    for (int l = 0; l < L; ++l) {
+    for (int l = l0; l < l1; ++l) {
         __half* kc = m->kc + (size_t)l * m->layer_kv;
         __half* vc = m->vc + (size_t)l * m->layer_kv;
-        KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * l) * H, m->xn, B, H, c.rms_eps, pdl, s));
-        kd::MmvqArgs a = mm(m->qkv[l], m->xn, kd::EPI_QKV);
+        kd::MmvqArgs a = mm(m->qkv[l], m->xn);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
-        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, kd::EPI_QKV, m->num_sms, pdl, s));
+        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
         kd::AttnArgs t{};
-        t.q = m->q; t.kc = kc; t.vc = vc; t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
+        t.q = m->q; t.kc = kc; t.vc = vc; t.row0 = (long)l * c.max_sessions * nkv * c.max_ctx;
+        t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
         t.hd = hd; t.cap = c.max_ctx; t.scale = 1.0f / std::sqrt((float)hd); t.part = m->apart;
         t.max_splits = m->max_splits; t.out = m->attn; t.err = m->err;
-        KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->attn_grid, pdl, s));
+        KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->kmaps, m->attn_grid, pdl, s));
         KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
-        a = mm(m->wo[l], m->attn, kd::EPI_RESID);
-        a.y = m->x; a.ld = H;
-        KD_RUN(KD_K_WO, kd::launch_mmvq(a, kd::EPI_RESID, m->num_sms, pdl, s));
-        KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * l + 1) * H, m->xn, B, H, c.rms_eps, pdl, s));
-        a = mm(m->gu[l], m->xn, kd::EPI_SWIGLU);
+        a = mm(m->wo[l], m->attn);
+        resid(a);
+        KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * l + 1) * H));  // the FFN norm
+        a = mm(m->gu[l], m->xn);
         a.act = m->act; a.ld = F;
-        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, kd::EPI_SWIGLU, m->num_sms, pdl, s));
-        a = mm(m->down[l], m->act, kd::EPI_RESID);
-        a.y = m->x; a.ld = H;
-        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, kd::EPI_RESID, m->num_sms, pdl, s));
-        if (m->hidden_dbg &&
+        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
+        a = mm(m->down[l], m->act);
+        resid(a);
+        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        if (whole || l + 1 < l1)  // next layer's attention norm, or the output norm
+            KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H));
+        if (whole && m->hidden_dbg &&
             (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)(l + 1) * B * H, m->x, (size_t)B * H * 4,
                                  cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
             return e;
     }
-    KD_RUN(KD_K_RMSNORM, kd::launch_rmsnorm(m->x, m->norms + (size_t)(2 * L) * H, m->xn, B, H, c.rms_eps, pdl, s));
-    kd::MmvqArgs a = mm(m->head, m->xn, kd::EPI_STORE);
+    if (!whole) return cudaSuccess;
+    kd::MmvqArgs a = mm(m->head, m->xn);
     a.y = lg; a.ld = V;
-    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, kd::EPI_STORE, m->num_sms, pdl, s));
+    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
     if (am) KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, pdl, s));
 #undef KD_RUN
     return cudaSuccess;
@@ -532,40 +558,56 @@ kd_status kd_session_load_kv(kd_model* m, int32_t id, const void* k, const void*
     return KD_OK;
 }
 
-kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
-                         int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
-    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null model");
-    if (B < 1 || B > KD_MAX_BATCH)
-        return fail(KD_ERR_BATCH, "kd_decode_step: B=%d outside [1, %d]", B, KD_MAX_BATCH);
-    if (!ids || !tokens || !positions) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
+static kd_status check_rows(kd_model* m, const char* fn, const int32_t* ids, const int32_t* tokens,
+                            const int32_t* positions, int32_t B) {
+    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "%s: B=%d outside [1, %d]", fn, B, KD_MAX_BATCH);
+    if (!ids || !positions) return fail(KD_ERR_INVALID_ARG, "%s: null host array", fn);
     const kd_config& c = m->cfg;
     for (int b = 0; b < B; ++b) {
         kd_status st = check_session(m, ids[b]);
         if (st != KD_OK) return st;
         for (int j = 0; j < b; ++j)
             if (ids[j] == ids[b]) return fail(KD_ERR_BAD_SESSION, "session %d appears twice in one step", ids[b]);
-        if (tokens[b] < 0 || tokens[b] >= c.vocab)
+        if (tokens && (tokens[b] < 0 || tokens[b] >= c.vocab))
             return fail(KD_ERR_INVALID_ARG, "token %d of row %d outside [0, %d)", tokens[b], b, c.vocab);
         if (positions[b] < 0 || positions[b] > m->len[ids[b]] || positions[b] >= c.max_ctx)
             return fail(KD_ERR_POSITION, "position %d of session %d: length is %d, capacity %d", positions[b],
                         ids[b], m->len[ids[b]], c.max_ctx);
     }
-    KD_CK(cudaSetDevice(m->dev));
-    cudaStream_t s = (cudaStream_t)stream;
-    // Stage the descriptor through a pinned ring slot no earlier copy still reads.
+    return KD_OK;
+}
+
+// Stage the [slot | token | pos] descriptor through a pinned ring slot no earlier
+// copy still reads, ordered after the model's previous step.
+static kd_status stage_descriptor(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
+                                  int32_t B, cudaStream_t s) {
     const int ri = m->ring_i;
     KD_CK(cudaEventSynchronize(m->ring_ev[ri]));
     int32_t* d = m->pinned + (size_t)ri * DESC_INTS;
     std::memset(d, 0, DESC_INTS * sizeof(int32_t));
     for (int b = 0; b < B; ++b) {
         d[b] = ids[b];
-        d[KD_MAX_BATCH + b] = tokens[b];
+        d[KD_MAX_BATCH + b] = tokens ? tokens[b] : 0;
         d[2 * KD_MAX_BATCH + b] = positions[b];
     }
     KD_CK(cudaStreamWaitEvent(s, m->last_step, 0));
     KD_CK(cudaMemcpyAsync(m->desc, d, DESC_INTS * sizeof(int32_t), cudaMemcpyHostToDevice, s));
     KD_CK(cudaEventRecord(m->ring_ev[ri], s));
     m->ring_i = (ri + 1) % RING;
+    return KD_OK;
+}
+
+kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
+                         int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null model");
+    if (!tokens && B >= 1 && B <= KD_MAX_BATCH) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
+    kd_status st0 = check_rows(m, "kd_decode_step", ids, tokens, positions, B);
+    if (st0 != KD_OK) return st0;
+    const kd_config& c = m->cfg;
+    KD_CK(cudaSetDevice(m->dev));
+    cudaStream_t s = (cudaStream_t)stream;
+    st0 = stage_descriptor(m, ids, tokens, positions, B, s);
+    if (st0 != KD_OK) return st0;
 
     float* lg = logits_out ? logits_out : m->logits_ws;
     if (m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH)) {
@@ -578,6 +620,31 @@ kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens,
     }
     KD_CK(cudaEventRecord(m->last_step, s));
     for (int b = 0; b < B; ++b) m->len[ids[b]] = positions[b] + 1;
+    return KD_OK;
+}
+
+kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const int32_t* positions, int32_t B,
+                         const float* x_in, float* x_out, kd_stream stream) {
+    if (!m || !x_in || !x_out) return fail(KD_ERR_INVALID_ARG, "kd_debug_layer: null argument");
+    if (layer < 0 || layer >= m->cfg.n_layers)
+        return fail(KD_ERR_INVALID_ARG, "kd_debug_layer: layer %d outside [0, %d)", layer, m->cfg.n_layers);
+    kd_status st = check_rows(m, "kd_debug_layer", ids, nullptr, positions, B);
+    if (st != KD_OK) return st;
+    KD_CK(cudaSetDevice(m->dev));
+    cudaStream_t s = (cudaStream_t)stream;
+    st = stage_descriptor(m, ids, nullptr, positions, B, s);
+    if (st != KD_OK) return st;
+    const size_t bytes = (size_t)B * m->cfg.hidden * sizeof(float);
+    KD_CK(cudaMemcpyAsync(m->x, x_in, bytes, cudaMemcpyDefault, s));
+    KD_CK(kd::launch_row_norm(m->x, B, m->cfg.hidden, m->norms + (size_t)(2 * layer) * m->cfg.hidden,
+                              m->cfg.rms_eps, m->xn, s));
+    const bool prof = m->prof;
+    m->prof = false;
+    cudaError_t e = enqueue_step(m, B, nullptr, nullptr, s, layer);
+    m->prof = prof;
+    KD_CK(e);
+    KD_CK(cudaMemcpyAsync(x_out, m->x, bytes, cudaMemcpyDefault, s));
+    KD_CK(cudaEventRecord(m->last_step, s));
     return KD_OK;
 }
 
@@ -664,7 +731,7 @@ kd_status kd_q8_matrix_create(const void* host, int32_t rows, int32_t cols, kd_q
         cudaFree(staging);
         return cleanup(fail(KD_ERR_OOM, "kd_q8_matrix_create: device allocation failed"));
     }
-    kd_status st = upload_packed({{host, rows}}, cols, tiles_natural(rows), staging, d_tiles, w->p);
+    kd_status st = upload_packed({{host, rows}}, cols, tiles_natural(rows), staging, d_tiles, w->num_sms, w->p);
     cudaFree(staging);
     cudaFree(d_tiles);
     if (st != KD_OK) return cleanup(st);
@@ -694,17 +761,17 @@ kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
     if (!w || !x || !y) return fail(KD_ERR_INVALID_ARG, "kd_mmvq: null argument");
     if (m < 1 || m > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_mmvq: m=%d outside [1, %d]", m, KD_MAX_BATCH);
     kd::MmvqArgs a{};
-    a.w = w->p.w; a.G = w->p.G; a.KG = w->p.KG; a.kpt = w->p.kpt; a.S = w->p.S; a.K = w->p.K;
+    a.w = w->p.w; a.G = w->p.G; a.KG = w->p.KG; a.W = w->p.W; a.maxc = w->p.maxc; a.K = w->p.K;
     a.x = reinterpret_cast<const __half*>(x); a.B = m; a.part = w->part; a.cnt = w->cnt; a.err = w->err;
     a.y = y; a.ld = w->p.rows;
-    KD_CK(kd::launch_mmvq(a, kd::EPI_STORE, w->num_sms, false, (cudaStream_t)stream));
+    KD_CK(kd::launch_mmvq(a, w->p.mode, kd::EPI_STORE, w->num_sms, false, (cudaStream_t)stream));
     return KD_OK;
 }
 
 size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap) {
     if (B < 1 || n_heads < 1 || head_dim < 1 || cap < 1) return 0;
     const size_t splits = (size_t)(cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
-    return 256 + (size_t)B * n_heads * splits * (head_dim + 2) * sizeof(float);
+    return 256 + (size_t)B * n_heads * splits * kd::ATT_REC(head_dim) * sizeof(float);
 }
 
 kd_status kd_attn_append_decode(const float* q, const float* k_new, const float* v_new, uint16_t* k_cache,
@@ -719,6 +786,9 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
         return fail(KD_ERR_UNSUPPORTED, "kd_attn_append_decode: head_dim %d, group %d", head_dim,
                     n_kv_heads > 0 ? n_heads / n_kv_heads : 0);
     if (n_slots < 1 || cap < 1) return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: n_slots/cap");
+    if ((cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK > kd::ATT_MAX_SPLITS)
+        return fail(KD_ERR_UNSUPPORTED, "kd_attn_append_decode: cap %d exceeds %d", cap,
+                    kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
     if (workspace_bytes < kd_attn_workspace_bytes(B, n_heads, head_dim, cap))
         return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: workspace too small");
     if (((uintptr_t)workspace | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
@@ -744,15 +814,17 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
     KD_CK(cudaMemsetAsync(d_err, 0, sizeof(int), s));
     KD_CK(kd::launch_kv_append(k_new, v_new, (__half*)k_cache, (__half*)v_cache, d_desc, d_desc + KD_MAX_BATCH, B,
                                n_kv_heads, head_dim, cap, s));
+    kd::AttnMaps maps;
+    KD_CK(kd::make_attn_maps((const __half*)k_cache, (long)n_slots * n_kv_heads * cap, head_dim, &maps));
     kd::AttnArgs t{};
-    t.q = q; t.kc = (const __half*)k_cache; t.vc = (const __half*)v_cache; t.slot = d_desc;
+    t.q = q; t.kc = (const __half*)k_cache; t.vc = (const __half*)v_cache; t.row0 = 0; t.slot = d_desc;
     t.pos = d_desc + KD_MAX_BATCH; t.B = B; t.nh = n_heads; t.nkv = n_kv_heads; t.hd = head_dim; t.cap = cap;
     t.scale = 1.0f / std::sqrt((float)head_dim);
     t.part = (float*)((char*)workspace + 256);
     t.max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
     t.out = (__half*)out;
     t.err = d_err;
-    KD_CK(kd::launch_attn_split(t, kd::attn_split_grid(sms, head_dim, n_heads / n_kv_heads), false, s));
+    KD_CK(kd::launch_attn_split(t, maps, kd::attn_split_grid(sms, head_dim, n_heads / n_kv_heads), false, s));
     KD_CK(kd::launch_attn_combine(t, false, s));
     return KD_OK;
 }

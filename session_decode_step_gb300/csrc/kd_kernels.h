@@ -1,5 +1,6 @@
 // kd_kernels.h -- host-side launch interface of the decode-step kernels (library internal).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -39,17 +40,28 @@ enum Epilogue : int {
     EPI_QKV = 3,     // RoPE q and k at each row's position, q to fp32, k/v appended as fp16
 };
 
+constexpr int MAX_NORM_SLOTS = 16;  // sum-of-squares tables hold one entry per session slot 0..15
+
+enum MmvqMode : int {
+    MMVQ_STREAM = 0,  // warps stream equal contiguous shares; partials of shared groups via global memory
+    MMVQ_GROUP = 1,   // a CTA owns whole row groups; its warps split K and reduce in shared memory
+};
+
 struct PackedQ8 {
     uint8_t* w = nullptr;   // packed bytes
     int rows = 0, K = 0;    // logical shape
     int G = 0, KG = 0;      // groups of 32 rows, k-groups of 128 columns
-    int kpt = 1, S = 1;     // k-groups per task, k-splits (S = KG / kpt)
+    int mode = MMVQ_STREAM; // schedule (depends on the shape and SM count only)
+    int W = 1;              // stream: warps streaming it (one contiguous stage range each)
+    int maxc = 1;           // stream: most warps sharing one row group
     size_t bytes() const { return (size_t)G * KG * STAGE_BYTES; }
-    size_t part_floats() const { return S > 1 ? (size_t)G * S * GROUP_ROWS * 16 : 0; }
+    size_t part_floats() const { return mode == MMVQ_STREAM && maxc > 1 ? (size_t)G * maxc * GROUP_ROWS * 16 : 0; }
 };
 
-// Pick the split of K into tasks for an N x K matrix; depends on the shape only.
-void choose_split(PackedQ8& m);
+// Split a matrix's stages over the warps of a grid of num_sms CTAs; depends on
+// the shape and the SM count only.
+// force_mode: -1 = choose from the shape, else MMVQ_STREAM / MMVQ_GROUP.
+void plan_split(PackedQ8& m, int num_sms, int force_mode = -1);
 
 // Repack a canonical Q8_0 matrix already on the device.  tile_src[t] is the
 // first source row of packed tile t (G * MT entries, device memory).
@@ -58,11 +70,15 @@ cudaError_t launch_repack(const uint8_t* src, int K, const int* tile_src, int G,
 
 struct MmvqArgs {
     const uint8_t* w;
-    int G, KG, kpt, S, K;
+    int G, KG, W, maxc, K;
     const __half* x;     // [B][K] fp16 activations
     int B;
+    // EPI_RESID: each group's writer also leaves sum(x_new^2) of its 32 rows per
+    // session in ssq_out[g][n], so the next RMSNorm needs no row reduction.
+    float* ssq_out;      // [G][16]
     float* part;         // split-K partials
     int* cnt;            // [G] arrival counters, zero between launches
+                         // (part: [G][maxc][32 rows][16 columns] fp32)
     int* err;            // device fault word
     int ld;              // row stride (elements) of the epilogue output
     float* y;            // EPI_STORE / EPI_RESID target
@@ -77,29 +93,41 @@ struct MmvqArgs {
     int nh, nkv, hd, cap;
 };
 
-cudaError_t launch_mmvq(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s);
-size_t mmvq_smem_bytes();
+cudaError_t launch_mmvq(const MmvqArgs& a, int mode, int epi, int num_sms, bool pdl, cudaStream_t s);
+// Smallest dynamic shared memory any mmvq launch needs (for occupancy checks).
 cudaError_t mmvq_init_attributes();
 
 // ---- attention -------------------------------------------------------------
-constexpr int ATT_CHUNK = 128;  // keys per split; fixed, so a session's splits depend on its length only
+constexpr int ATT_CHUNK = 64;        // keys per split; fixed, so a session's splits depend on its length only
+constexpr int ATT_MAX_SPLITS = 1024;  // longest context: 1024 * 64 = 65536 positions
+// One split's partial result per (session, head): o[hd], then m, l, and padding
+// to a 16-byte multiple so every record starts 16-byte aligned.
+__host__ __device__ constexpr int ATT_REC(int hd) { return hd + 4; }
 
 struct AttnArgs {
     const float* q;       // [B][nh][hd] fp32, rotated
     const __half* kc;     // this layer's arenas [slots][nkv][cap][hd] fp16
     const __half* vc;
+    long row0;            // this layer's first row in the K tensor map ([rows][hd] over the whole arena)
     const int* slot;      // [B]
     const int* pos;       // [B]; the row attends keys 0..pos
     int B, nh, nkv, hd, cap;
     float scale;
-    float* part;          // [B][nh][max_splits][hd + 2]
+    float* part;          // [B][nh][max_splits][ATT_REC(hd)]
     int max_splits;
     __half* out;          // [B][nh*hd]
     int* err;
 };
 
+// Tensor maps over a K arena viewed as [rows][hd] fp16: 64-row boxes and 8-row
+// boxes (ragged tails) of 64-dim halves, 128-byte swizzle.
+struct AttnMaps {
+    CUtensorMap k, k8;
+};
+cudaError_t make_attn_maps(const __half* k_arena, long rows, int hd, AttnMaps* out);
+
 bool attn_supported(int hd, int group);
-cudaError_t launch_attn_split(const AttnArgs& a, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_attn_split(const AttnArgs& a, const AttnMaps& maps, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_attn_combine(const AttnArgs& a, bool pdl, cudaStream_t s);
 int attn_split_grid(int num_sms, int hd, int group);
 cudaError_t attn_init_attributes();
@@ -109,12 +137,17 @@ cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half*
                              const int* pos, int B, int nkv, int hd, int cap, cudaStream_t s);
 
 // ---- row ops -----------------------------------------------------------------
-// x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows)
-cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x,
-                         bool pdl, cudaStream_t s);
-// out[b][i] = fp16(x[b][i] / sqrt(mean(x[b]^2) + eps) * w[i])
-cudaError_t launch_rmsnorm(const float* x, const float* w, __half* out, int B, int H, float eps,
-                           bool pdl, cudaStream_t s);
+// x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and the first
+// layer's normed input xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w)
+cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
+                         float eps, __half* xn, bool pdl, cudaStream_t s);
+// xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w) for rows supplied from outside
+cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, cudaStream_t s);
+// The same norm from the per-group sums of squares ssq[g][b] (g < H/32) a
+// residual writer left: elementwise, spread over many CTAs.
+cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
+                                 __half* xn, bool pdl, cudaStream_t s);
+cudaError_t rowops_init_attributes();
 // out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none)
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, bool pdl, cudaStream_t s);
 

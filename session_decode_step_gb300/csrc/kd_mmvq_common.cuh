@@ -1,0 +1,119 @@
+// kd_mmvq_common.cuh -- device code shared by the two Q8_0 mmvq schedules
+// (kd_mmvq_stream.cu: warps stream equal contiguous shares of the matrix;
+// kd_mmvq_cta.cu: a CTA owns whole row groups and its warps split K).
+//
+// The arithmetic is identical in both and never depends on m (the number of
+// activation rows): per 32-column Q8_0 block, the int8 quants are converted to
+// fp16 exactly and multiplied on two m16n8k16 MMAs (fp32 accumulate) whose 8
+// columns are 8 sessions; the block result is scaled by its fp16 scale with an
+// fp32 FMA.  Only how many MMA columns are stored depends on m.
+#pragma once
+#include <cuda_fp16.h>
+
+#include "kd_device.cuh"
+#include "kd_kernels.h"
+
+namespace kd {
+
+constexpr int MMVQ_WARPS = 8;
+constexpr int RING = 3;        // weight stages in flight per warp
+constexpr int NORM_SLOTS = MAX_NORM_SLOTS;
+
+// One stage (one 128-column k-group of a 32-row group) into the accumulators.
+// x: this lane's activation fragments for the stage's 4 blocks (k permutation
+// of the packed layout); acc[mt][nt][i]: row mt*16 + gq (+8 for i >= 2),
+// session nt*8 + 2*cq + (i & 1).
+template <int NT>
+__device__ __forceinline__ void mma_stage(const uint8_t* st, int lane, int gq, const uint4 (&x)[4][NT],
+                                          float (&acc)[MT][NT][4]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const uint8_t* tb = st + mt * TILE_KG_BYTES;
+        const uint4 sc = lds_v4(tb + 2048 + gq * 16);
+        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            const uint4 wq = lds_v4(tb + kb * 512 + lane * 16);
+            // k-half 0: columns 8cq+0..3; k-half 1: columns 8cq+4..7
+            const uint32_t a00 = u8x2_lo_to_half2(wq.x), a01 = u8x2_lo_to_half2(wq.z);
+            const uint32_t a02 = u8x2_hi_to_half2(wq.x), a03 = u8x2_hi_to_half2(wq.z);
+            const uint32_t a10 = u8x2_lo_to_half2(wq.y), a11 = u8x2_lo_to_half2(wq.w);
+            const uint32_t a12 = u8x2_hi_to_half2(wq.y), a13 = u8x2_hi_to_half2(wq.w);
+            const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&scw[kb]));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float t[4];
+                mma_16816_zero(t, a00, a01, a02, a03, x[kb][nt].x, x[kb][nt].y);
+                mma_16816_acc(t, a10, a11, a12, a13, x[kb][nt].z, x[kb][nt].w);
+                acc[mt][nt][0] = __fmaf_rn(d.x, t[0], acc[mt][nt][0]);
+                acc[mt][nt][1] = __fmaf_rn(d.x, t[1], acc[mt][nt][1]);
+                acc[mt][nt][2] = __fmaf_rn(d.y, t[2], acc[mt][nt][2]);
+                acc[mt][nt][3] = __fmaf_rn(d.y, t[3], acc[mt][nt][3]);
+            }
+        }
+    }
+}
+
+// ---- activation fragments -------------------------------------------------
+// Lane (gq, cq) multiplies session n = gq + 8*nt at columns 8cq .. 8cq+7 of each
+// 32-column block.  Sessions >= B read as zeros.
+//
+// Plain fp16 activations [B][K]:
+template <int NT>
+__device__ __forceinline__ void load_x_f16(const MmvqArgs& a, int gq, int cq, int kg, uint4 (&xv)[4][NT]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = gq + 8 * nt;
+        const __half* p = a.x + (size_t)(n < a.B ? n : 0) * a.K + kg * KGROUP + cq * 8;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) xv[kb][nt] = n < a.B ? ldg_nc_v4(p + kb * 32) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// ---- epilogues on single outputs ------------------------------------------
+// Row r (0..31) of row group g, session n, value v.
+__device__ __forceinline__ void epi_store(const MmvqArgs& a, int g, int r, int n, float v) {
+    a.y[(size_t)n * a.ld + (size_t)g * GROUP_ROWS + r] = v;
+}
+// Residual add; returns the updated value.
+__device__ __forceinline__ float epi_resid(const MmvqArgs& a, int g, int r, int n, float v) {
+    float* p = a.y + (size_t)n * a.ld + (size_t)g * GROUP_ROWS + r;
+    const float x = __fadd_rn(*p, v);
+    *p = x;
+    return x;
+}
+// Pair epilogues: tile 0 row r with tile 1 row r (r = 0..15).
+//   SwiGLU: act = fp16(silu(gate) * up)
+__device__ __forceinline__ void epi_swiglu(const MmvqArgs& a, int g, int r, int n, float gt, float up) {
+    const float sg = __fdiv_rn(gt, __fadd_rn(1.0f, expf(-gt)));
+    a.act[(size_t)n * a.ld + (size_t)g * TILE_ROWS + r] = __float2half_rn(__fmul_rn(sg, up));
+}
+//   QKV: dims (i, i + hd/2) of one head; RoPE at the row's position for q and k;
+//   q to fp32, k and v appended to the session's slot at its position as fp16.
+__device__ __forceinline__ void epi_qkv(const MmvqArgs& a, int g, int r, int n, float x0, float x1) {
+    const int per_head = a.hd / GROUP_ROWS;
+    const int head = g / per_head;
+    const int dim = (g - head * per_head) * TILE_ROWS + r;
+    const int half = a.hd >> 1;
+    const int p = a.pos[n];
+    if (head < a.nh + a.nkv) {
+        const float2 cs = a.rope[(size_t)p * half + dim];
+        const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+        const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+        if (head < a.nh) {
+            float* q = a.q_out + ((size_t)n * a.nh + head) * a.hd;
+            q[dim] = y0;
+            q[dim + half] = y1;
+        } else {
+            __half* k = a.kc + (((size_t)a.slot[n] * a.nkv + (head - a.nh)) * a.cap + p) * a.hd;
+            k[dim] = __float2half_rn(y0);
+            k[dim + half] = __float2half_rn(y1);
+        }
+    } else {
+        __half* vv = a.vc + (((size_t)a.slot[n] * a.nkv + (head - a.nh - a.nkv)) * a.cap + p) * a.hd;
+        vv[dim] = __float2half_rn(x0);
+        vv[dim + half] = __float2half_rn(x1);
+    }
+}
+
+}  // namespace kd

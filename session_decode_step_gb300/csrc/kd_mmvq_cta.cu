@@ -1,0 +1,204 @@
+// kd_mmvq_cta.cu -- Q8_0 mmvq, "group" schedule: for matrices with about as
+// many 32-row groups as SMs (qkv, o-proj, down).
+//
+// CTA c owns row groups c, c + grid, ...; within a group its 8 warps split the
+// K range into 8 contiguous k-group ranges (fixed by the shape), each streamed
+// through the warp's own ring of shared-memory stages.  At the end of a group
+// the warps' fp32 partials meet in shared memory and are added in warp order;
+// no global partials, fences or atomics.  Nothing depends on m.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kd_mmvq_common.cuh"
+
+namespace kd {
+
+template <int NT>
+struct CtaSmem {
+    static constexpr int RS = NT == 1 ? 9 : 16;  // partial-row stride (floats), padded against bank conflicts
+    static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RING * STAGE_BYTES;
+    static constexpr size_t BAR_OFF = RING_BYTES;
+    static constexpr size_t RED_OFF = BAR_OFF + MMVQ_WARPS * RING * sizeof(uint64_t);
+    static constexpr size_t TOTAL = RED_OFF + (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
+};
+
+template <int NT, int EPI>
+__global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_kernel(const MmvqArgs a) {
+    using L = CtaSmem<NT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    uint8_t* ring = smem + (size_t)warp * RING * STAGE_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RING;
+    float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [warp][32 rows][RS]
+
+    const int kg0 = warp * a.KG / MMVQ_WARPS, nk = (warp + 1) * a.KG / MMVQ_WARPS - kg0;
+    const int ngrp = (int)blockIdx.x < a.G ? (a.G - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = ngrp * nk;
+
+    if (lane == 0) {
+        for (int i = 0; i < RING; ++i) mbar_init(&bar[i], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    const uint64_t policy = l2_policy_evict_first();
+    // Issue cursor: stage (group ii of this CTA, k-group kg0 + ikk).
+    int ii = 0, ikk = 0;
+    auto issue_next = [&](int slot_) {
+        const int g = blockIdx.x + ii * gridDim.x;
+        mbar_arrive_expect_tx(&bar[slot_], STAGE_BYTES);
+        bulk_g2s_hint(ring + slot_ * STAGE_BYTES, a.w + ((size_t)g * a.KG + kg0 + ikk) * STAGE_BYTES, STAGE_BYTES,
+                      &bar[slot_], policy);
+        if (++ikk == nk) { ikk = 0; ++ii; }
+    };
+    // The weights do not depend on earlier kernels: start streaming them before
+    // waiting for the producer of the activations.
+    if (lane == 0)
+        for (int i = 0; i < RING && i < total; ++i) issue_next(i);
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // Activation prefetch cursor two stages ahead (k-group kg0 + pkk, wrapping per group).
+    int pkk = 0;
+    uint4 x0[4][NT], x1[4][NT], x2[4][NT];
+    if (total > 0) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x0);
+    if (++pkk == nk) pkk = 0;
+    if (total > 1) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x1);
+    if (++pkk == nk) pkk = 0;
+
+    int sidx = 0, slot = 0;
+    uint32_t phase = 0;
+    bool failed = false;
+    for (int gi = 0; gi < ngrp; ++gi) {
+        const int g = blockIdx.x + gi * gridDim.x;
+        float acc[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.0f;
+        for (int kk = 0; kk < nk && !failed; ++kk, ++sidx) {
+            if (sidx + 2 < total) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x2);
+            if (++pkk == nk) pkk = 0;
+            const bool ok = mbar_wait_bounded(&bar[slot], phase);
+            if (__any_sync(FULL_MASK, !ok)) {
+                // Give up: flag it, let every copy already issued land, stop computing.
+                if (lane == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
+                for (int t = sidx; t < total && t < sidx + RING; ++t)
+                    (void)mbar_wait_bounded(&bar[t % RING], (uint32_t)(t / RING) & 1u);
+                failed = true;
+                break;
+            }
+            mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, x0, acc);
+            __syncwarp();
+            if (lane == 0 && sidx + RING < total) issue_next(slot);
+            if (++slot == RING) { slot = 0; phase ^= 1u; }
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    x0[kb][nt] = x1[kb][nt];
+                    x1[kb][nt] = x2[kb][nt];
+                }
+        }
+        // ---- the group's partials meet in shared memory (every warp takes part) ----
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int r0 = mt * TILE_ROWS + gq, c0 = nt * 8 + 2 * cq;
+                float* rw = red + ((size_t)warp * GROUP_ROWS) * L::RS;
+                rw[r0 * L::RS + c0] = acc[mt][nt][0];
+                rw[r0 * L::RS + c0 + 1] = acc[mt][nt][1];
+                rw[(r0 + 8) * L::RS + c0] = acc[mt][nt][2];
+                rw[(r0 + 8) * L::RS + c0 + 1] = acc[mt][nt][3];
+            }
+        __syncthreads();
+        auto sum_rows = [&](int row, int n) {  // warps 0..7 in order
+            float v = red[row * L::RS + n];
+#pragma unroll
+            for (int w = 1; w < MMVQ_WARPS; ++w) v = __fadd_rn(v, red[((size_t)w * GROUP_ROWS + row) * L::RS + n]);
+            return v;
+        };
+        if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+            for (int n = warp; n < a.B; n += MMVQ_WARPS) {  // a warp per session, a lane per row
+                const float v = sum_rows(lane, n);
+                if constexpr (EPI == EPI_STORE) {
+                    epi_store(a, g, lane, n, v);
+                } else {
+                    const float x = epi_resid(a, g, lane, n, v);
+                    float s = __fmul_rn(x, x);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+                    if (lane == 0) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
+                }
+            }
+        } else {
+            for (int e = tid; e < a.B * TILE_ROWS; e += MMVQ_WARPS * 32) {  // (row pair, session)
+                const int n = e >> 4, rr = e & 15;
+                const float v0 = sum_rows(rr, n), v1 = sum_rows(rr + TILE_ROWS, n);
+                if constexpr (EPI == EPI_SWIGLU)
+                    epi_swiglu(a, g, rr, n, v0, v1);
+                else
+                    epi_qkv(a, g, rr, n, v0, v1);
+            }
+        }
+        __syncthreads();  // the partial buffer is reused by the next group
+    }
+}
+
+template <int NT>
+size_t cta_smem_bytes() {
+    return CtaSmem<NT>::TOTAL;
+}
+
+template <int NT, int EPI>
+static cudaError_t cta_attr() {
+    cudaError_t e = cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)cta_smem_bytes<NT>());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+template <int NT, int EPI>
+static cudaError_t cta_launch(const MmvqArgs& a, int grid, bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(MMVQ_WARPS * 32);
+    cfg.dynamicSmemBytes = cta_smem_bytes<NT>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI>, a);
+}
+
+#define KD_CTA_CASES(X, NT_) X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID)
+
+cudaError_t mmvq_cta_init_attributes() {
+    cudaError_t e;
+#define KD_A(NT_, EPI_) \
+    if ((e = cta_attr<NT_, EPI_>()) != cudaSuccess) return e;
+    KD_CTA_CASES(KD_A, 1)
+    KD_CTA_CASES(KD_A, 2)
+#undef KD_A
+    return cudaSuccess;
+}
+
+cudaError_t launch_mmvq_cta(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s) {
+    const bool wide = a.B > 8;
+    const int grid = a.G < num_sms ? a.G : num_sms;
+#define KD_L(NT_, EPI_) \
+    if (epi == EPI_ && (NT_ == 2) == wide) return cta_launch<NT_, EPI_>(a, grid, pdl, s);
+    KD_CTA_CASES(KD_L, 1)
+    KD_CTA_CASES(KD_L, 2)
+#undef KD_L
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kd

@@ -1,0 +1,276 @@
+// kd_mmvq_stream.cu -- Q8_0 mmvq, "stream" schedule: for matrices with many
+// more 32-row groups than SMs (gate|up, lm_head).
+//
+// The matrix is a sequence of T = G * KG stages (one 128-column k-group of one
+// row group, contiguous in memory).  Warp w of W takes stages [w*T/W, (w+1)*T/W),
+// so every warp streams the same bytes (+-1 stage) as one contiguous range,
+// through its own ring of shared-memory stages filled by 1-D bulk copies.  A
+// row group split between warps is finished by the last of them to arrive (one
+// atomic per warp and group, no waiting): it adds the fp32 partials in warp
+// order and runs the epilogue.  W depends on the shape and SM count, never on m.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kd_mmvq_common.cuh"
+
+namespace kd {
+
+__device__ __forceinline__ int stage_owner(long t, long T, long W) { return (int)(((t + 1) * W - 1) / T); }
+
+// Epilogue over this lane's fragment of a finished row group.
+template <int NT, int EPI>
+__device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, int cq, float (&v)[MT][NT][4]) {
+    float ss[NT][2];  // RESID: this lane's share of sum(x_new^2) per column
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) ss[nt][0] = ss[nt][1] = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = nt * 8 + 2 * cq + (i & 1);
+            if (n >= a.B) continue;
+            const int r = gq + ((i >> 1) << 3);  // row within a 16-row tile
+            if constexpr (EPI == EPI_STORE) {
+                epi_store(a, g, r, n, v[0][nt][i]);
+                epi_store(a, g, r + TILE_ROWS, n, v[1][nt][i]);
+            } else if constexpr (EPI == EPI_RESID) {
+                const float x0 = epi_resid(a, g, r, n, v[0][nt][i]);
+                const float x1 = epi_resid(a, g, r + TILE_ROWS, n, v[1][nt][i]);
+                ss[nt][i & 1] = __fmaf_rn(x1, x1, __fmaf_rn(x0, x0, ss[nt][i & 1]));
+            } else if constexpr (EPI == EPI_SWIGLU) {
+                epi_swiglu(a, g, r, n, v[0][nt][i], v[1][nt][i]);
+            } else {
+                epi_qkv(a, g, r, n, v[0][nt][i], v[1][nt][i]);
+            }
+        }
+    if constexpr (EPI == EPI_RESID) {
+        // sum over the 8 row lanes (gq) of each column, fixed tree; gq == 0 writes
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float s = ss[nt][j];
+                s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 4));
+                s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 8));
+                s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 16));
+                const int n = nt * 8 + 2 * cq + j;
+                if (gq == 0 && n < a.B) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
+            }
+    }
+}
+
+template <int NT, int EPI>
+__global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const MmvqArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    uint8_t* ring = smem + (size_t)warp * RING * STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)MMVQ_WARPS * RING * STAGE_BYTES);
+    uint64_t* bar = bars + warp * RING;
+
+    const long T = (long)a.G * a.KG;
+    const int w = blockIdx.x * MMVQ_WARPS + warp;
+    const bool active = w < a.W;  // false only when the matrix has fewer stages than the grid has warps
+    const long s_begin = active ? (long)w * T / a.W : 0, s_end = active ? (long)(w + 1) * T / a.W : 0;
+    const int n = (int)(s_end - s_begin);
+
+    if (lane == 0) {
+        for (int i = 0; i < RING; ++i) mbar_init(&bar[i], 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    const uint64_t policy = l2_policy_evict_first();
+    const uint8_t* wsrc = a.w + (size_t)s_begin * STAGE_BYTES;  // this warp's contiguous range
+    // The weights do not depend on earlier kernels: start streaming them before
+    // waiting for the producer of the activations.
+    if (lane == 0)
+        for (int i = 0; i < RING && i < n; ++i) {
+            mbar_arrive_expect_tx(&bar[i], STAGE_BYTES);
+            bulk_g2s_hint(ring + i * STAGE_BYTES, wsrc + (size_t)i * STAGE_BYTES, STAGE_BYTES, &bar[i], policy);
+        }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // Compute cursor (g, kg) and an activation prefetch cursor two stages ahead.
+    int g = (int)(s_begin / a.KG), kg = (int)(s_begin - (long)g * a.KG);
+    int pkg = kg;
+    uint4 x0[4][NT], x1[4][NT], x2[4][NT];
+    if (n > 0) load_x_f16<NT>(a, gq, cq, pkg, x0);
+    if (++pkg == a.KG) pkg = 0;
+    if (n > 1) load_x_f16<NT>(a, gq, cq, pkg, x1);
+    if (++pkg == a.KG) pkg = 0;
+
+    float acc[MT][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.0f;
+
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < n; ++i) {
+        if (i + 2 < n) load_x_f16<NT>(a, gq, cq, pkg, x2);
+        if (++pkg == a.KG) pkg = 0;
+
+        const bool ok = mbar_wait_bounded(&bar[slot], phase);
+        if (__any_sync(FULL_MASK, !ok)) {
+            // Give up: flag it, let every copy already issued land, stop computing.
+            if (lane == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
+            for (int t = i; t < n && t < i + RING; ++t)
+                (void)mbar_wait_bounded(&bar[t % RING], (uint32_t)(t / RING) & 1u);
+            break;
+        }
+        mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, x0, acc);
+        __syncwarp();
+        if (lane == 0 && i + RING < n) {
+            mbar_arrive_expect_tx(&bar[slot], STAGE_BYTES);
+            bulk_g2s_hint(ring + slot * STAGE_BYTES, wsrc + (size_t)(i + RING) * STAGE_BYTES, STAGE_BYTES,
+                          &bar[slot], policy);
+        }
+        if (++slot == RING) { slot = 0; phase ^= 1u; }
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                x0[kb][nt] = x1[kb][nt];
+                x1[kb][nt] = x2[kb][nt];
+            }
+
+        const bool seg_end = (kg == a.KG - 1) || (i == n - 1);
+        if (!seg_end) {
+            ++kg;
+            continue;
+        }
+        // ---- this warp's part of row group g is done ----
+        const long gfirst = (long)g * a.KG;
+        const int w0 = stage_owner(gfirst, T, a.W), w1 = stage_owner(gfirst + a.KG - 1, T, a.W);
+        if (w0 == w1) {
+            frag_epilogue<NT, EPI>(a, g, gq, cq, acc);  // the whole group was this warp's
+        } else {
+            const int ncontrib = w1 - w0 + 1;
+            float* pt = a.part + ((size_t)g * a.maxc + (w - w0)) * (GROUP_ROWS * 16);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int r0 = mt * TILE_ROWS + gq, c0 = nt * 8 + 2 * cq;
+                    *reinterpret_cast<float2*>(pt + r0 * 16 + c0) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+                    *reinterpret_cast<float2*>(pt + (r0 + 8) * 16 + c0) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+                }
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = (atomicAdd(&a.cnt[g], 1) == ncontrib - 1);
+            last = __shfl_sync(FULL_MASK, last, 0);
+            if (last) {
+                __threadfence();
+                // Sum the slots in contributor order; loads are issued CH slots at a
+                // time so their latencies overlap.
+                constexpr int CH = NT == 1 ? 4 : 4;
+                float v[MT][NT][4];
+                const float* p0 = a.part + (size_t)g * a.maxc * (GROUP_ROWS * 16);
+                for (int s0 = 0; s0 < ncontrib; s0 += CH) {
+                    float2 lo[CH][MT][NT], hi[CH][MT][NT];
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        if (s0 + j >= ncontrib) break;
+                        const float* ps = p0 + (size_t)(s0 + j) * (GROUP_ROWS * 16);
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                const int r0 = mt * TILE_ROWS + gq, c0 = nt * 8 + 2 * cq;
+                                lo[j][mt][nt] = ldcg_f2(ps + r0 * 16 + c0);
+                                hi[j][mt][nt] = ldcg_f2(ps + (r0 + 8) * 16 + c0);
+                            }
+                    }
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        if (s0 + j >= ncontrib) break;
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                if (s0 + j == 0) {  // the first slot starts the sum
+                                    v[mt][nt][0] = lo[j][mt][nt].x;
+                                    v[mt][nt][1] = lo[j][mt][nt].y;
+                                    v[mt][nt][2] = hi[j][mt][nt].x;
+                                    v[mt][nt][3] = hi[j][mt][nt].y;
+                                } else {
+                                    v[mt][nt][0] = __fadd_rn(v[mt][nt][0], lo[j][mt][nt].x);
+                                    v[mt][nt][1] = __fadd_rn(v[mt][nt][1], lo[j][mt][nt].y);
+                                    v[mt][nt][2] = __fadd_rn(v[mt][nt][2], hi[j][mt][nt].x);
+                                    v[mt][nt][3] = __fadd_rn(v[mt][nt][3], hi[j][mt][nt].y);
+                                }
+                            }
+                    }
+                }
+                frag_epilogue<NT, EPI>(a, g, gq, cq, v);
+                if (lane == 0) a.cnt[g] = 0;  // ready for the next launch
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2) acc[mt][nt][i2] = 0.0f;
+        ++g;
+        kg = 0;
+    }
+}
+
+size_t mmvq_stream_smem_bytes() {
+    return (size_t)MMVQ_WARPS * RING * STAGE_BYTES + (size_t)MMVQ_WARPS * RING * sizeof(uint64_t);
+}
+
+template <int NT, int EPI>
+static cudaError_t stream_attr() {
+    cudaError_t e = cudaFuncSetAttribute(mmvq_stream_kernel<NT, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mmvq_stream_smem_bytes());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mmvq_stream_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+template <int NT, int EPI>
+static cudaError_t stream_launch(const MmvqArgs& a, bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.W + MMVQ_WARPS - 1) / MMVQ_WARPS);
+    cfg.blockDim = dim3(MMVQ_WARPS * 32);
+    cfg.dynamicSmemBytes = mmvq_stream_smem_bytes();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, mmvq_stream_kernel<NT, EPI>, a);
+}
+
+#define KD_STREAM_CASES(X, NT_) X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID)
+
+cudaError_t mmvq_stream_init_attributes() {
+    cudaError_t e;
+#define KD_A(NT_, EPI_) \
+    if ((e = stream_attr<NT_, EPI_>()) != cudaSuccess) return e;
+    KD_STREAM_CASES(KD_A, 1)
+    KD_STREAM_CASES(KD_A, 2)
+#undef KD_A
+    return cudaSuccess;
+}
+
+cudaError_t launch_mmvq_stream(const MmvqArgs& a, int epi, bool pdl, cudaStream_t s) {
+    const bool wide = a.B > 8;
+#define KD_L(NT_, EPI_) \
+    if (epi == EPI_ && (NT_ == 2) == wide) return stream_launch<NT_, EPI_>(a, pdl, s);
+    KD_STREAM_CASES(KD_L, 1)
+    KD_STREAM_CASES(KD_L, 2)
+#undef KD_L
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kd

@@ -100,7 +100,7 @@ def test_op_level_argument_checks(lib):
 
 def test_attention_workspace_size():
     n = kd.kd_attn_workspace_bytes(8, 32, 128, 32768)
-    assert n == 256 + 8 * 32 * 256 * 130 * 4
+    assert n == 256 + 8 * 32 * 512 * 132 * 4  # 64-key splits, 16-byte aligned records
     assert kd.kd_attn_workspace_bytes(0, 32, 128, 10) == 0
 
 

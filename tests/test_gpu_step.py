@@ -50,12 +50,15 @@ def tiny():
     return shape, synth.model_weights(shape, 0)
 
 
-def test_tiny_teacher_forced_against_oracle(kdlib, tiny):
+# 0: schedules chosen per matrix; 2 / 4: every projection forced onto the
+# stream / group schedule (the tiny model alone would only exercise one of them).
+@pytest.mark.parametrize("flags", [0, 2, 4])
+def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags):
     kd = kdlib
     shape, w = tiny
     case = synth.TINY_CASE
     cap = 64
-    m = load(kd, shape, w, 4, cap)
+    m = load(kd, shape, w, 4, cap, flags)
     try:
         lens = list(case["prefill"])
         ids = bind_prefilled(kd, m, shape, lens)
@@ -94,7 +97,8 @@ def greedy_stream(kd, m, ids, lens, tok0, steps, V):
     return np.array(toks), np.array(logits)
 
 
-@pytest.mark.parametrize("flags", [0, 1])  # CUDA-graph replay, then kernel-by-kernel launches
+# graph replay (auto schedules), kernel-by-kernel launches, and each schedule forced
+@pytest.mark.parametrize("flags", [0, 1, 2, 4])
 def test_tiny_batch_invariance(kdlib, tiny, flags):
     kd = kdlib
     shape, w = tiny
