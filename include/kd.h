@@ -226,6 +226,40 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
                                 int32_t cap, uint16_t* out, void* workspace,
                                 size_t workspace_bytes, kd_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free variant (no counterpart on the batched-decode pages: it
+ * exists for callers, not for the method).
+ *
+ * kd_attn_append_decode_noalloc computes exactly what kd_attn_append_decode
+ * computes, with the same kernels, but takes no workspace and allocates
+ * nothing: no cudaMalloc/cudaFree, no allocating library routine, no
+ * host-to-device copy (slots and positions are passed to the device as kernel
+ * arguments).  It is meant for callers that cannot allocate device memory
+ * where they decode -- e.g. code inside a memory pool or arena that owns the
+ * whole GPU, or a hot path where an allocation's implicit device
+ * synchronisation is not acceptable.
+ *
+ * Its scratch is one fixed device array of KD_ATTN_NOALLOC_SCRATCH_BYTES that
+ * every GPU using this entry point holds from library load to process exit.
+ * Requests whose partial results do not fit are refused with
+ * KD_ERR_UNSUPPORTED: they need
+ *   256 + B * n_heads * ceil(cap / 64) * (head_dim + 4) * 4  bytes
+ * (e.g. B = 8, 32 heads of 128, cap up to 7936 positions).
+ * All calls share the array, and it keeps the last call's contents (each call
+ * rewrites what it reads, so no clearing is needed between calls): calls that
+ * overlap on the GPU -- on different streams without ordering, or from
+ * different threads -- race on it and must not be issued.
+ * The first call on each device looks up the array's device address (once,
+ * with that device current); make that first call before any stream capture.
+ * Arguments, layouts and errors as for kd_attn_append_decode. */
+#define KD_ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+kd_status kd_attn_append_decode_noalloc(const float* q, const float* k_new, const float* v_new,
+                                        uint16_t* k_cache, uint16_t* v_cache,
+                                        const int32_t* slots, const int32_t* positions,
+                                        int32_t B, int32_t n_heads, int32_t n_kv_heads,
+                                        int32_t head_dim, int32_t n_slots, int32_t cap,
+                                        uint16_t* out, kd_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,7 @@ _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "libkd.so"
 
 KD_MAX_BATCH = 16
+KD_ATTN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 KD_FLAG_NO_GRAPH = 1
 STATUS = {0: "KD_OK", -1: "KD_ERR_INVALID_ARG", -2: "KD_ERR_OOM", -3: "KD_ERR_CUDA",
           -4: "KD_ERR_NO_FREE_SLOT", -5: "KD_ERR_BAD_SESSION", -6: "KD_ERR_POSITION",
@@ -79,6 +80,8 @@ def lib():
             "kd_mmvq": [_vp, _vp, i32, _vp, _vp],
             "kd_attn_append_decode": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                       i32, _vp, _vp, C.c_size_t, _vp],
+            "kd_attn_append_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
+                                              i32, _vp, _vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -276,3 +279,16 @@ def kd_attn_append_decode(q, k_new, v_new, k_cache, v_cache, slots, positions, n
                                        sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p), B, n_heads,
                                        n_kv_heads, head_dim, n_slots, cap, _ptr(out), _ptr(workspace),
                                        nbytes, _stream(stream)))
+
+
+def kd_attn_append_decode_noalloc(q, k_new, v_new, k_cache, v_cache, slots, positions, n_heads, n_kv_heads,
+                                  head_dim, n_slots, cap, out, stream=None):
+    """kd_attn_append_decode with its scratch in the library's fixed device array
+    (no workspace argument, no allocation); see include/kd.h for the limits."""
+    sl = _i32(slots)
+    B = sl.size
+    ps = _i32(positions, B)
+    i32p = C.POINTER(C.c_int32)
+    _check(lib().kd_attn_append_decode_noalloc(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                               sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p), B, n_heads,
+                                               n_kv_heads, head_dim, n_slots, cap, _ptr(out), _stream(stream)))

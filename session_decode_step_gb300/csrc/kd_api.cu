@@ -122,6 +122,9 @@ kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, i
 
 }  // namespace
 
+void kd::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+cudaError_t kd::ensure_device_attributes(int dev) { return init_device_attributes(dev); }
+
 struct kd_model {
     kd_config cfg{};
     int dev = 0, num_sms = 0, attn_grid = 0;

@@ -151,4 +151,9 @@ cudaError_t rowops_init_attributes();
 // out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none)
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, bool pdl, cudaStream_t s);
 
+// Set the calling thread's last-error message (what kd_last_error() returns).
+void set_last_error(const char* msg);
+// Kernel attributes (shared-memory sizes, carveouts) of device dev, set once.
+cudaError_t ensure_device_attributes(int dev);
+
 }  // namespace kd
