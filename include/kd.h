@@ -133,7 +133,8 @@ kd_status kd_session_length(const kd_model* m, int32_t session_id, int32_t* len_
  *     and positions[b] < max_ctx.  The token is written to the cache at
  *     positions[b] and attends keys 0..positions[b]; afterwards the session's
  *     length is positions[b] + 1 (a position below the length rewinds).
- *   logits_out: NULL or device fp32 [B][vocab]; row b belongs to session_ids[b].
+ *   logits_out: NULL or device fp32 [B][vocab], 16-byte aligned; row b belongs
+ *     to session_ids[b].
  *   argmax_out: NULL or device int32 [B]: the greedy next token (largest logit,
  *     ties to the lowest index, NaN never wins; -1 if a row is all NaN).
  * Enqueued on `stream` without a host wait; outputs are valid once the stream
@@ -206,6 +207,17 @@ kd_status kd_q8_matrix_free(kd_q8_matrix* w);
 kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
                   kd_stream stream);
 
+/* Greedy pick over logit rows, as the step's argmax (memra decode_batch.rs
+ * `decode_batch_epilogue`, a device argmax equal to the host one):
+ *   out[b] = the index of the largest logits[b][v]; equal values go to the
+ *   lowest index, -0 equals +0, NaN never wins; -1 if row b is all NaN.
+ * logits: device fp32 [B][V], 16-byte aligned, V a multiple of 4; out: device
+ * int32 [B]; B in [1, KD_MAX_BATCH]; workspace: device memory of
+ * KD_ARGMAX_WORKSPACE_BYTES, owned by the caller, used by one call at a time. */
+#define KD_ARGMAX_WORKSPACE_BYTES 256
+kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, void* workspace,
+                    kd_stream stream);
+
 /* Bytes of device workspace kd_attn_append_decode needs for these sizes. */
 size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap);
 
@@ -218,7 +230,9 @@ size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int
  * fp32 [B][n_kv_heads][head_dim]; k_cache, v_cache: device fp16
  * [n_slots][n_kv_heads][cap][head_dim]; slots, positions: host int32 [B] (slots
  * distinct, 0 <= positions[b] < cap); out: device fp16 [B][n_heads*head_dim];
- * workspace: device memory of kd_attn_workspace_bytes(B, n_heads, head_dim, cap). */
+ * workspace: device memory of kd_attn_workspace_bytes(B, n_heads, head_dim, cap).
+ * k_cache, v_cache and workspace must be 16-byte aligned and q 8-byte aligned
+ * (KD_ERR_INVALID_ARG otherwise). */
 kd_status kd_attn_append_decode(const float* q, const float* k_new, const float* v_new,
                                 uint16_t* k_cache, uint16_t* v_cache, const int32_t* slots,
                                 const int32_t* positions, int32_t B, int32_t n_heads,

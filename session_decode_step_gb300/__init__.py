@@ -78,6 +78,7 @@ def lib():
             "kd_q8_matrix_create": [_vp, i32, i32, C.POINTER(_vp)],
             "kd_q8_matrix_free": [_vp],
             "kd_mmvq": [_vp, _vp, i32, _vp, _vp],
+            "kd_argmax": [_vp, i32, i32, _vp, _vp, _vp],
             "kd_attn_append_decode": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                       i32, _vp, _vp, C.c_size_t, _vp],
             "kd_attn_append_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
@@ -262,6 +263,14 @@ def kd_q8_matrix_free(w):
 
 def kd_mmvq(w, x, m: int, y, stream=None):
     _check(lib().kd_mmvq(w, _ptr(x), int(m), _ptr(y), _stream(stream)))
+
+
+KD_ARGMAX_WORKSPACE_BYTES = 256
+
+
+def kd_argmax(logits, B: int, V: int, out, workspace, stream=None):
+    """logits: device fp32 [B][V]; out: device int32 [B]; workspace: KD_ARGMAX_WORKSPACE_BYTES of device memory."""
+    _check(lib().kd_argmax(_ptr(logits), int(B), int(V), _ptr(out), _ptr(workspace), _stream(stream)))
 
 
 def kd_attn_workspace_bytes(B: int, n_heads: int, head_dim: int, cap: int) -> int:

@@ -137,7 +137,7 @@ struct kd_model {
     __half* kc = nullptr;     // [L][slots][nkv][cap][hd]
     __half* vc = nullptr;
     size_t layer_kv = 0;      // elements per layer of one arena
-    kd::AttnMaps kmaps{};     // tensor maps over the K arena
+    kd::AttnMaps kmaps{};     // tensor maps over the K and V arenas
     float* x = nullptr;       // [16][H] residual stream
     __half* xn = nullptr;     // [16][H] normed activations (written by the fused RMSNorm)
     float* ssq = nullptr;     // [H/32][16] per-group sums of squares of the residual rows
@@ -150,6 +150,7 @@ struct kd_model {
     int max_splits = 0;
     float* logits_ws = nullptr;
     int* err = nullptr;
+    unsigned long long* amax_keys = nullptr;  // argmax scratch: [KD_MAX_BATCH] keys, then a counter (zero between launches)
     int* desc = nullptr;      // device [slot16 | token16 | pos16]
     int32_t* pinned = nullptr;
     cudaEvent_t ring_ev[RING] = {};
@@ -285,7 +286,7 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->vc, (size_t)L * m->layer_kv * sizeof(__half)));
     KD_CK(cudaMemset(m->kc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
     KD_CK(cudaMemset(m->vc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
-    KD_CK(kd::make_attn_maps(m->kc, (long)L * S * nkv * cap, hd, &m->kmaps));
+    KD_CK(kd::make_attn_maps(m->kc, m->vc, (long)L * S * nkv * cap, hd, &m->kmaps));
     const int MB = KD_MAX_BATCH;
     KD_CK(m->alloc(&m->x, (size_t)MB * H * sizeof(float)));
     KD_CK(m->alloc(&m->xn, (size_t)MB * H * sizeof(__half)));
@@ -310,6 +311,8 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->apart, (size_t)MB * nh * m->max_splits * kd::ATT_REC(hd) * sizeof(float)));
     KD_CK(m->alloc(&m->logits_ws, (size_t)MB * V * sizeof(float)));
     KD_CK(m->alloc(&m->err, sizeof(int)));
+    KD_CK(m->alloc(&m->amax_keys, (KD_MAX_BATCH + 1) * sizeof(unsigned long long)));
+    KD_CK(cudaMemset(m->amax_keys, 0, (KD_MAX_BATCH + 1) * sizeof(unsigned long long)));
     KD_CK(cudaMemset(m->err, 0, sizeof(int)));
     KD_CK(m->alloc(&m->desc, DESC_INTS * sizeof(int)));
     KD_CK(cudaMemset(m->desc, 0, DESC_INTS * sizeof(int)));
@@ -426,7 +429,9 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     kd::MmvqArgs a = mm(m->head, m->xn);
     a.y = lg; a.ld = V;
     KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
-    if (am) KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, pdl, s));
+    if (am)
+        KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, m->amax_keys,
+                                              reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s));
 #undef KD_RUN
     return cudaSuccess;
 }
@@ -606,6 +611,8 @@ kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens,
     if (!tokens && B >= 1 && B <= KD_MAX_BATCH) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
     kd_status st0 = check_rows(m, "kd_decode_step", ids, tokens, positions, B);
     if (st0 != KD_OK) return st0;
+    if (reinterpret_cast<uintptr_t>(logits_out) & 15)
+        return fail(KD_ERR_INVALID_ARG, "kd_decode_step: logits_out must be 16-byte aligned");
     const kd_config& c = m->cfg;
     KD_CK(cudaSetDevice(m->dev));
     cudaStream_t s = (cudaStream_t)stream;
@@ -771,6 +778,23 @@ kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
     return KD_OK;
 }
 
+kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, void* workspace, kd_stream stream) {
+    if (!logits || !out || !workspace) return fail(KD_ERR_INVALID_ARG, "kd_argmax: null argument");
+    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_argmax: B=%d outside [1, %d]", B, KD_MAX_BATCH);
+    if (V < 1 || V % 4) return fail(KD_ERR_INVALID_ARG, "kd_argmax: V=%d must be a positive multiple of 4", V);
+    if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(workspace)) & 15)
+        return fail(KD_ERR_INVALID_ARG, "kd_argmax: logits and workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0;
+    KD_CK(cudaGetDevice(&dev));
+    KD_CK(init_device_attributes(dev));
+    static_assert((KD_MAX_BATCH + 1) * sizeof(unsigned long long) <= KD_ARGMAX_WORKSPACE_BYTES, "argmax workspace");
+    auto* keys = reinterpret_cast<unsigned long long*>(workspace);
+    KD_CK(cudaMemsetAsync(keys, 0, (KD_MAX_BATCH + 1) * sizeof(unsigned long long), s));
+    KD_CK(kd::launch_argmax(logits, B, V, out, keys, reinterpret_cast<unsigned*>(keys + KD_MAX_BATCH), false, s));
+    return KD_OK;
+}
+
 size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap) {
     if (B < 1 || n_heads < 1 || head_dim < 1 || cap < 1) return 0;
     const size_t splits = (size_t)(cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
@@ -794,8 +818,8 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
                     kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
     if (workspace_bytes < kd_attn_workspace_bytes(B, n_heads, head_dim, cap))
         return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: workspace too small");
-    if (((uintptr_t)workspace | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
-        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: buffers must be 16-byte aligned");
+    if ((((uintptr_t)workspace | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15) || ((uintptr_t)q & 7))
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode: caches and workspace must be 16-byte aligned, q 8-byte");
     int32_t desc[2 * KD_MAX_BATCH] = {};
     for (int b = 0; b < B; ++b) {
         if (slots[b] < 0 || slots[b] >= n_slots) return fail(KD_ERR_BAD_SESSION, "slot %d", slots[b]);
@@ -818,7 +842,8 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
     KD_CK(kd::launch_kv_append(k_new, v_new, (__half*)k_cache, (__half*)v_cache, d_desc, d_desc + KD_MAX_BATCH, B,
                                n_kv_heads, head_dim, cap, s));
     kd::AttnMaps maps;
-    KD_CK(kd::make_attn_maps((const __half*)k_cache, (long)n_slots * n_kv_heads * cap, head_dim, &maps));
+    KD_CK(kd::make_attn_maps((const __half*)k_cache, (const __half*)v_cache, (long)n_slots * n_kv_heads * cap, head_dim,
+                              &maps));
     kd::AttnArgs t{};
     t.q = q; t.kc = (const __half*)k_cache; t.vc = (const __half*)v_cache; t.row0 = 0; t.slot = d_desc;
     t.pos = d_desc + KD_MAX_BATCH; t.B = B; t.nh = n_heads; t.nkv = n_kv_heads; t.hd = head_dim; t.cap = cap;

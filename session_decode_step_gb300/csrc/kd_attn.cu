@@ -9,11 +9,11 @@
 // with C fixed, so the number of splits and every split's arithmetic depend on
 // the session's own length only -- the result does not depend on what else is
 // in the batch.  A persistent CTA per SM walks its items through a ring of
-// shared-memory stages: the split's K rows arrive by tensor-map copies with the
-// 128-byte swizzle (conflict-free reads while q is broadcast), its V rows by a
-// plain bulk copy.  Per item: the GQA group's scores, a local softmax (max m,
-// sum l) and the weighted V sum, written as (o, m, l).  A second kernel merges
-// a session-head's splits in split order (online-softmax combine).
+// shared-memory stages, filled by tensor-map copies of the split's K and V rows
+// with the 128-byte swizzle; each item is computed by one warp.  Per item: the GQA group's scores and
+// the weighted V sum as tensor-core products, a local softmax (max m, sum l) in
+// between, written as (o, m, l).  A second kernel merges a session-head's
+// splits in split order (online-softmax combine).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -25,61 +25,72 @@
 
 namespace kd {
 
-constexpr int AT_THREADS = 256;  // 8 warps
-constexpr int AT_WARPS = AT_THREADS / 32;
-constexpr int AT_STAGES = 2;     // work items in flight per CTA (several CTAs per SM)
 constexpr int AT_C = ATT_CHUNK;  // keys per work item (split)
-static_assert(AT_C == 64, "the score pass maps 2 x 32 keys onto the 8 warps");
+constexpr int AT_WARPS = 8;      // consumer warps per CTA (two per SM sub-partition)
+static_assert(AT_C == 64, "a work item is 8 key tiles of 8 and 4 key steps of 16");
 
-// Shared memory of one CTA.  A stage holds one work item: its K rows as 64-dim
-// halves written by the tensor-map copy with the 128-byte swizzle (row r's
-// 16-byte chunk c sits at chunk c ^ (r & 7)), then its V rows as written by a
-// plain bulk copy ([key][head_dim] fp16).
-template <int HD, int GQ>
+// Shared memory of one CTA: a ring of STAGES stages shared by its warps.  A
+// stage holds one work item: its K tile, then its V tile, each as 64-dim halves
+// of [64 keys][128 B] written by tensor-map copies with the 128-byte swizzle
+// (row r's 16-byte chunk c sits at chunk c ^ (r & 7)), so the 8 rows an
+// ldmatrix phase reads always fall in 8 different bank groups.  Per stage: a
+// full barrier and the CTA-local index of the item last issued into it.
+template <int HD>
 struct AttnSmem {
-    static constexpr int NREG = HD / 64;                   // 128-byte K halves per row
-    static constexpr int KREG_BYTES = AT_C * 128;          // one half of the K tile
-    static constexpr int K_BYTES = NREG * KREG_BYTES;
-    static constexpr int V_BYTES = AT_C * HD * 2;
-    static constexpr int STAGE = K_BYTES + V_BYTES;        // 1024-byte multiple
-    static constexpr int Q_OFF = AT_STAGES * STAGE;        // q, double-buffered [2][GQ][HD]
-    static constexpr int SP_OFF = Q_OFF + 2 * GQ * HD * 4; // score partials [4][C][GQ]
-    static constexpr int SS_OFF = SP_OFF + 4 * AT_C * GQ * 4;  // probabilities [C][GQ]
-    static constexpr int BAR_OFF = (SS_OFF + AT_C * GQ * 4 + 15) / 16 * 16;
-    static constexpr int TOTAL = BAR_OFF + AT_STAGES * 8 + 1024;  // + alignment slack
+    static constexpr int NREG = HD / 64;                    // 64-dim halves of a row
+    static constexpr int HALF_BYTES = AT_C * 128;           // one half of a 64-key tile
+    static constexpr int K_BYTES = NREG * HALF_BYTES;
+    static constexpr int STAGE = 2 * K_BYTES;               // K tile, V tile
+    static constexpr int STAGES = 192 * 1024 / STAGE;       // 6 at hd 128, 12 at hd 64
+    static constexpr int BAR_OFF = STAGES * STAGE;
+    static constexpr int ITEM_OFF = BAR_OFF + STAGES * 8;
+    static constexpr int TOTAL = ITEM_OFF + STAGES * 4 + 16 + 1024;  // + flag, alignment slack
     static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    // byte offset of (row, 16-byte chunk along the head dim) inside a tile
+    static __device__ __forceinline__ uint32_t off(int row, int chunk) {
+        return (uint32_t)((chunk >> 3) * HALF_BYTES + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    }
 };
 
 // Work items are ordered session-major, then split, then KV head.
-__device__ __forceinline__ int attn_items(const AttnArgs& a) {
-    int n = 0;
-    for (int i = 0; i < a.B; ++i) n += (a.pos[i] + AT_C) / AT_C * a.nkv;
-    return n;
-}
-
 struct AttnItem {
-    int b, s, kvh, n, ns;  // session, split, KV head, keys in this split, splits of the session
+    int b, s, kvh, n, ns, slot;  // session, split, KV head, keys in this split, splits of the session, its slot
 };
 
-__device__ __forceinline__ AttnItem attn_item(const AttnArgs& a, int item) {
-    AttnItem it{0, 0, 0, 0, 0};
-    int base = 0;
-    for (int i = 0; i < a.B; ++i) {
-        const int ns = (a.pos[i] + AT_C) / AT_C;  // ceil((pos+1)/C)
-        const int cnt = ns * a.nkv;
-        if (item < base + cnt) {
-            const int r = item - base;
-            it.b = i;
-            it.s = r / a.nkv;
-            it.kvh = r - it.s * a.nkv;
-            it.n = min(AT_C, a.pos[i] + 1 - it.s * AT_C);
-            it.ns = ns;
-            return it;
+// The session table of a launch, held one session per lane (B <= 32): the
+// session's slot, position, split count and first item.  Built once per warp
+// from the step's descriptor; an item's session is then found by a ballot over
+// the lanes' first items, with no memory access.
+struct AttnTable {
+    int slot, pos, ns, base, n_items;
+    __device__ __forceinline__ void build(const AttnArgs& a, int lane) {
+        slot = lane < a.B ? a.slot[lane] : 0;
+        pos = lane < a.B ? a.pos[lane] : 0;
+        ns = lane < a.B ? (pos + ATT_CHUNK) / ATT_CHUNK : 0;  // ceil((pos+1)/C)
+        int incl = ns * a.nkv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += v;
         }
-        base += cnt;
+        base = incl - ns * a.nkv;
+        n_items = __shfl_sync(FULL_MASK, incl, 31);
     }
-    return it;
-}
+    // Warp-uniform item index (< n_items); every lane gets the same answer.
+    __device__ __forceinline__ AttnItem item(const AttnArgs& a, int lane, int x) const {
+        const unsigned m = __ballot_sync(FULL_MASK, lane < a.B && base <= x);
+        const int b = 31 - __clz(m);
+        AttnItem it;
+        it.b = b;
+        const int r = x - __shfl_sync(FULL_MASK, base, b);
+        it.s = r / a.nkv;
+        it.kvh = r - it.s * a.nkv;
+        it.n = min(ATT_CHUNK, __shfl_sync(FULL_MASK, pos, b) + 1 - it.s * ATT_CHUNK);
+        it.ns = __shfl_sync(FULL_MASK, ns, b);
+        it.slot = __shfl_sync(FULL_MASK, slot, b);
+        return it;
+    }
+};
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
     asm volatile(
@@ -89,288 +100,375 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
-template <int HD, int GQ>
-__global__ void __launch_bounds__(AT_THREADS, GQ <= 4 ? 3 : 2)
-    attn_split_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmk8) {
-    using L = AttnSmem<HD, GQ>;
-    extern __shared__ uint8_t smem_raw[];
-    // 1024-byte aligned base for the swizzled tiles
-    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    float* qsb = reinterpret_cast<float*>(smem + L::Q_OFF);  // [2][GQ][HD]
-    float* sp = reinterpret_cast<float*>(smem + L::SP_OFF);  // [4][C][GQ]
-    float* ss = reinterpret_cast<float*>(smem + L::SS_OFF);  // [C][GQ]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
 
-    if (tid == 0) {
-        for (int i = 0; i < AT_STAGES; ++i) mbar_init(&bar[i], 1);
+// fp32 pair -> fp16 pair (low half = first element), and the fp16 pair of what
+// that rounding left over: hi + lo carries about 22 significant bits.
+__device__ __forceinline__ uint32_t f2_hi(float x, float y) {
+    const __half2 h = __floats2half2_rn(x, y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t f2_lo(float x, float y) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(__fsub_rn(x, f.x), __fsub_rn(y, f.y));
+    return *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Bounded poll of a shared-memory word until it holds v (false: gave up).
+__device__ __forceinline__ bool wait_value(const volatile int* p, int v) {
+    if (*p == v) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0; i < WAIT_MAX_POLLS; ++i) {
+        if (*p == v) return true;
+        if ((i & 255u) == 255u && global_timer_ns() - t0 > WAIT_MAX_NS) break;
+    }
+    return false;
+}
+
+// A CTA takes the items blockIdx.x + k * gridDim.x, k = 0, 1, ...: item k goes
+// through stage k % STAGES and is computed by warp k % AT_WARPS, which then
+// refills that stage with item k + STAGES.  A consumer first waits until the
+// stage's item word says k (the copy of item k was issued, so the stage's
+// barrier is in item k's phase), then for the barrier.  The scores S = Q K^T
+// and the output O = P V are m16n8k16 tensor-core products: the A rows are the
+// group's heads, rows [0, GQ) with q (then p) rounded to fp16 and rows
+// [GQ, 2 GQ) with the remainder of that rounding (GQ = 8: rows g and g + 8), so
+// their sum is the fp32-accurate product; K tiles are the B operand of S as
+// stored, V tiles that of O through the transposing ldmatrix.
+template <int HD, int GQ>
+__global__ void __launch_bounds__(AT_WARPS * 32, 1)
+    attn_split_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmk8, const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ CUtensorMap tmv8) {
+    using L = AttnSmem<HD>;
+    constexpr int S = L::STAGES;
+    constexpr int KS = HD / 16;  // 16-dim k-steps of Q K^T
+    constexpr int NU = HD / 8;   // 8-dim output tiles of P V
+    static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "GQA group");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    volatile int* stage_item = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
+    volatile int* cta_failed = stage_item + S;
+    // Rows of the A operand this lane supplies: head qh rounded (hi) or its remainder (lo).
+    const int qh = GQ == 8 ? g : (g < 2 * GQ ? g % GQ : -1);
+    const bool lo_row = GQ < 8 && g >= GQ;
+    constexpr int PARTNER = GQ < 8 ? 4 * GQ : 0;  // lane xor that holds the other half of a row pair
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&bar[i], 1);
+            stage_item[i] = -1;
+        }
+        *cta_failed = 0;
         mbar_init_fence();
     }
     __syncthreads();
 
-    // Issue the copies of this CTA's j-th work item into stage j % AT_STAGES.
-    auto issue = [&](const AttnItem& it, int j) {
-        uint8_t* stg = smem + (j % AT_STAGES) * L::STAGE;
-        const int t0 = it.s * AT_C;
-        const long row = a.row0 + ((long)a.slot[it.b] * a.nkv + it.kvh) * a.cap + t0;
+    AttnTable tab;
+    tab.build(a, lane);
+    const int n_items = tab.n_items;
+    const int nk = (int)blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto gitem = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
+    // Issue the copies of the CTA's item k into stage k % S (lane 0).
+    auto issue = [&](const AttnItem& it, int k) {
+        const int st = k % S;
+        uint8_t* stg = smem + st * L::STAGE;
+        const int row = (int)(a.row0 + ((long)it.slot * a.nkv + it.kvh) * a.cap + (long)it.s * AT_C);
         const bool full = it.n == AT_C;
         const int krows = full ? AT_C : (it.n + 7) / 8 * 8;
-        const uint32_t bytes = (uint32_t)(L::NREG * krows * 128 + it.n * HD * 2);
-        uint64_t* b = &bar[j % AT_STAGES];
-        mbar_arrive_expect_tx(b, bytes);
+        uint64_t* b = &bar[st];
+        stage_item[st] = k;
+        mbar_arrive_expect_tx(b, (uint32_t)(2 * L::NREG * krows * 128));
         for (int r = 0; r < L::NREG; ++r) {
-            uint8_t* kdst = stg + r * L::KREG_BYTES;
+            uint8_t* kdst = stg + r * L::HALF_BYTES;
+            uint8_t* vdst = kdst + L::K_BYTES;
             if (full) {
-                tma_load_2d(kdst, &tmk, r * 64, (int)row, b);
+                tma_load_2d(kdst, &tmk, r * 64, row, b);
+                tma_load_2d(vdst, &tmv, r * 64, row, b);
             } else {
-                for (int k8 = 0; k8 < krows; k8 += 8) tma_load_2d(kdst + k8 * 128, &tmk8, r * 64, (int)(row + k8), b);
+                for (int k8 = 0; k8 < krows; k8 += 8) {
+                    tma_load_2d(kdst + k8 * 128, &tmk8, r * 64, row + k8, b);
+                    tma_load_2d(vdst + k8 * 128, &tmv8, r * 64, row + k8, b);
+                }
             }
         }
-        bulk_g2s(stg + L::K_BYTES, a.vc + (row - a.row0) * HD, (uint32_t)(it.n * HD * 2), b);
     };
 
-    // History rows (keys < pos) were written by earlier steps: the items that do
-    // not hold this step's new row can be fetched before waiting on the QKV kernel.
-    int n_items = attn_items(a);
-    int issued = 0;
-    if (tid == 0) {
-        for (int j = 0; j < AT_STAGES; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            const AttnItem it = attn_item(a, item);
-            if (it.s == it.ns - 1) break;  // holds the new row: after the wait
-            issue(it, j);
-            issued = j + 1;
+    // The first S items fill the ring.  History rows (keys < pos) were written by
+    // earlier steps: items that do not hold this step's new row are fetched before
+    // waiting on the QKV kernel.
+    unsigned early = 0;
+    for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS) {
+        const AttnItem it = tab.item(a, lane, gitem(k));
+        if (it.s != it.ns - 1) {
+            if (lane == 0) issue(it, k);
+            early |= 1u << i;
         }
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0)
-        for (int j = issued; j < AT_STAGES; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            issue(attn_item(a, item), j);
+    for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS)
+        if (!((early >> i) & 1u)) {
+            const AttnItem it = tab.item(a, lane, gitem(k));
+            if (lane == 0) issue(it, k);
         }
-    constexpr int QN = GQ * HD;                                 // q floats per item
-    constexpr int QPT = (QN + AT_THREADS - 1) / AT_THREADS;    // per thread (1..4)
-    if ((int)blockIdx.x < n_items) {  // q of the first item
-        const AttnItem it = attn_item(a, blockIdx.x);
-        const float* qg = a.q + ((size_t)it.b * a.nh + (size_t)it.kvh * GQ) * HD;
+
+    // q of the lane's head, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
+    float2 qv[KS][2];
+    auto load_q = [&](const AttnItem& it) {
+        if (qh >= 0) {
+            const float* qp = a.q + ((size_t)it.b * a.nh + (size_t)it.kvh * GQ + qh) * HD + 2 * c;
 #pragma unroll
-        for (int i = 0; i < QPT; ++i)
-            if (tid + i * AT_THREADS < QN) qsb[tid + i * AT_THREADS] = qg[tid + i * AT_THREADS];
-    }
-
-    constexpr int QCH = HD / 32;  // 16-byte K chunks per dim quarter
-    // PV mapping: warp -> (head, dim range); lane -> 8 dims x keys of one residue class.
-    constexpr int WPH = AT_WARPS / GQ;         // warps per head
-    constexpr int DPW = HD / WPH;              // dims per warp
-    constexpr int LPK = DPW / 8 < 1 ? 1 : DPW / 8;  // lanes per key
-    constexpr int KGR = 32 / LPK;              // key residue classes per warp
-    const int kh = warp & 1, qd = warp >> 1;
-    const int pv_h = warp / WPH, pv_d0 = (warp % WPH) * DPW + (lane % LPK) * 8, pv_kr = lane / LPK;
-    const bool pv_on = (lane % LPK) * 8 < DPW;
-
-    for (int j = 0;; ++j) {
-        const int item = blockIdx.x + j * gridDim.x;
-        if (item >= n_items) break;
-        const AttnItem it = attn_item(a, item);
-        uint8_t* stg = smem + (j % AT_STAGES) * L::STAGE;
-        const float* qs = qsb + (j & 1) * GQ * HD;
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bar[j % AT_STAGES], (uint32_t)(j / AT_STAGES) & 1u)) != 0;
-        if (!ok) {
-            // Flag it, let every copy already issued (items j .. j+STAGES-1) land, leave.
-            if (tid == 0) {
-                atomicOr(a.err, ERR_WAIT_TIMEOUT);
-                for (int t = j; t < j + AT_STAGES; ++t)
-                    if (blockIdx.x + t * gridDim.x < n_items)
-                        (void)mbar_wait_bounded(&bar[t % AT_STAGES], (uint32_t)(t / AT_STAGES) & 1u);
+            for (int ks = 0; ks < KS; ++ks) {
+                qv[ks][0] = *reinterpret_cast<const float2*>(qp + 16 * ks);
+                qv[ks][1] = *reinterpret_cast<const float2*>(qp + 16 * ks + 8);
             }
-            __syncthreads();
+        }
+    };
+    if (warp < nk) load_q(tab.item(a, lane, gitem(warp)));
+
+    for (int k = warp; k < nk; k += AT_WARPS) {
+        const AttnItem it = tab.item(a, lane, gitem(k));
+        const int st = k % S;
+        uint8_t* stg = smem + st * L::STAGE;
+        const uint32_t kbase = smem_u32(stg), vbase = kbase + L::K_BYTES;
+
+        uint32_t qa[KS][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const float2 u = qv[ks][0], w = qv[ks][1];
+            if constexpr (GQ == 8) {
+                qa[ks][0] = f2_hi(u.x, u.y);
+                qa[ks][1] = f2_lo(u.x, u.y);
+                qa[ks][2] = f2_hi(w.x, w.y);
+                qa[ks][3] = f2_lo(w.x, w.y);
+            } else {
+                qa[ks][0] = qh < 0 ? 0u : (lo_row ? f2_lo(u.x, u.y) : f2_hi(u.x, u.y));
+                qa[ks][2] = qh < 0 ? 0u : (lo_row ? f2_lo(w.x, w.y) : f2_hi(w.x, w.y));
+                qa[ks][1] = 0u;
+                qa[ks][3] = 0u;
+            }
+        }
+        if (k + AT_WARPS < nk) load_q(tab.item(a, lane, gitem(k + AT_WARPS)));  // lands during this item
+
+        bool ok = wait_value(stage_item + st, k);
+        ok = ok && mbar_wait_bounded(&bar[st], (uint32_t)(k / S) & 1u);
+        if (__any_sync(FULL_MASK, !ok)) {
+            if (lane == 0) {
+                atomicOr(a.err, ERR_WAIT_TIMEOUT);
+                *cta_failed = 1;
+            }
             break;
         }
-        // ---- scores: warp (kh, qd) takes keys 32kh + lane over dim quarter qd;
-        // q is read warp-uniformly (broadcast), K conflict-free through the swizzle.
-        {
-            const int k = 32 * kh + lane;
-            float dot[GQ];
+        const int n = it.n;
+        if (n < AT_C) {
+            // V rows [n, 16-key step end) enter the last P V step with p = 0: make
+            // them zero (they hold other positions or stale data, possibly NaN).
+            const int z = ((n + 15) & ~15) - n;
+            for (int e = lane; e < z * L::NREG * 8; e += 32) {
+                const int r = n + e / (L::NREG * 8), rem = e % (L::NREG * 8);
+                *reinterpret_cast<uint4*>(stg + L::K_BYTES + (rem >> 3) * L::HALF_BYTES + r * 128 + (rem & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // ---- S = Q K^T over the 8 key tiles
+        float sacc[8][4];
 #pragma unroll
-            for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
+        for (int t = 0; t < 8; ++t) {
 #pragma unroll
-            for (int jj = 0; jj < QCH; ++jj) {
-                const int c = qd * QCH + jj;
-                const uint8_t* kp = stg + (c >> 3) * L::KREG_BYTES + k * 128 + (((c & 7) ^ (k & 7)) << 4);
-                const uint4 kv = lds_v4(kp);
-                const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
-                const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
-                const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
-                const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
+            for (int i = 0; i < 4; ++i) sacc[t][i] = 0.0f;
 #pragma unroll
-                for (int h = 0; h < GQ; ++h) {
-                    const float4 qa = *reinterpret_cast<const float4*>(qs + h * HD + c * 8);
-                    const float4 qb = *reinterpret_cast<const float4*>(qs + h * HD + c * 8 + 4);
-                    float d = dot[h];
-                    d = __fmaf_rn(qa.x, k01.x, d);
-                    d = __fmaf_rn(qa.y, k01.y, d);
-                    d = __fmaf_rn(qa.z, k23.x, d);
-                    d = __fmaf_rn(qa.w, k23.y, d);
-                    d = __fmaf_rn(qb.x, k45.x, d);
-                    d = __fmaf_rn(qb.y, k45.y, d);
-                    d = __fmaf_rn(qb.z, k67.x, d);
-                    d = __fmaf_rn(qb.w, k67.y, d);
-                    dot[h] = d;
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + L::off(8 * t + (lane & 7), 4 * kp + (lane >> 3)), b0, b1, b2, b3);
+                mma_16816_acc(sacc[t], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+                mma_16816_acc(sacc[t], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3],
+                              b2, b3);
+            }
+        }
+        // ---- row pair sum, scale, mask, softmax over the item's keys (4 lanes per row)
+        float sv[8][2];
+        float m = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float s;
+                if constexpr (GQ == 8) {
+                    s = __fadd_rn(sacc[t][e], sacc[t][2 + e]);
+                } else {
+                    const float o = __shfl_xor_sync(FULL_MASK, sacc[t][e], PARTNER);
+                    s = lo_row ? __fadd_rn(o, sacc[t][e]) : __fadd_rn(sacc[t][e], o);
+                }
+                const int key = 8 * t + 2 * c + e;
+                sv[t][e] = key < n ? __fmul_rn(s, a.scale) : -INFINITY;
+                m = fmaxf(m, sv[t][e]);
+            }
+        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 2));
+        float l = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = 8 * t + 2 * c + e;
+                sv[t][e] = key < n ? expf(__fsub_rn(sv[t][e], m)) : 0.0f;
+                l = __fadd_rn(l, sv[t][e]);
+            }
+        l = __fadd_rn(l, __shfl_xor_sync(FULL_MASK, l, 1));
+        l = __fadd_rn(l, __shfl_xor_sync(FULL_MASK, l, 2));
+
+        // ---- O = P V over the 16-key steps that hold keys
+        float oacc[NU][4];
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) oacc[u][i] = 0.0f;
+        const int nsteps = (n + 15) >> 4;
+#pragma unroll
+        for (int js = 0; js < 4; ++js) {
+            if (js < nsteps) {
+                const float* p0 = sv[2 * js];
+                const float* p1 = sv[2 * js + 1];
+                uint32_t pa0, pa1, pa2, pa3;
+                if constexpr (GQ == 8) {
+                    pa0 = f2_hi(p0[0], p0[1]);
+                    pa1 = f2_lo(p0[0], p0[1]);
+                    pa2 = f2_hi(p1[0], p1[1]);
+                    pa3 = f2_lo(p1[0], p1[1]);
+                } else {
+                    pa0 = qh < 0 ? 0u : (lo_row ? f2_lo(p0[0], p0[1]) : f2_hi(p0[0], p0[1]));
+                    pa2 = qh < 0 ? 0u : (lo_row ? f2_lo(p1[0], p1[1]) : f2_hi(p1[0], p1[1]));
+                    pa1 = 0u;
+                    pa3 = 0u;
+                }
+#pragma unroll
+                for (int up = 0; up < NU / 2; ++up) {
+                    const int i = lane >> 3;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(vbase + L::off(16 * js + 8 * (i & 1) + (lane & 7), 2 * up + (i >> 1)), b0, b1, b2,
+                                  b3);
+                    mma_16816_acc(oacc[2 * up], pa0, pa1, pa2, pa3, b0, b1);
+                    mma_16816_acc(oacc[2 * up + 1], pa0, pa1, pa2, pa3, b2, b3);
                 }
             }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) sp[(qd * AT_C + k) * GQ + h] = dot[h];
         }
-        __syncthreads();
-        // ---- softmax over the item's keys: warp h takes head h (quarters summed in order)
-        float m_h = 0.0f, l_h = 0.0f;
-        if (warp < GQ) {
-            const int h = warp;
-            float v[2];
+        // ---- row pair sum; lanes holding a head's rounded row write (o, m, l)
+        float* dst = a.part + (((size_t)it.b * a.nh + (size_t)it.kvh * GQ + (qh < 0 ? 0 : qh)) * a.max_splits + it.s) *
+                                  ATT_REC(HD);
+        const bool writer = qh >= 0 && !lo_row;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int k = lane + 32 * u, i = k * GQ + h;
-                const float sum = __fadd_rn(__fadd_rn(__fadd_rn(sp[i], sp[AT_C * GQ + i]), sp[2 * AT_C * GQ + i]),
-                                            sp[3 * AT_C * GQ + i]);
-                v[u] = k < it.n ? __fmul_rn(sum, a.scale) : -INFINITY;
+        for (int u = 0; u < NU; ++u) {
+            float o0, o1;
+            if constexpr (GQ == 8) {
+                o0 = __fadd_rn(oacc[u][0], oacc[u][2]);
+                o1 = __fadd_rn(oacc[u][1], oacc[u][3]);
+            } else {
+                o0 = __fadd_rn(oacc[u][0], __shfl_xor_sync(FULL_MASK, oacc[u][0], PARTNER));
+                o1 = __fadd_rn(oacc[u][1], __shfl_xor_sync(FULL_MASK, oacc[u][1], PARTNER));
             }
-            float m = fmaxf(v[0], v[1]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, o));
-            const float p0 = lane < it.n ? expf(__fsub_rn(v[0], m)) : 0.0f;
-            const float p1 = lane + 32 < it.n ? expf(__fsub_rn(v[1], m)) : 0.0f;
-            float l = __fadd_rn(p0, p1);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(FULL_MASK, l, o));
-            ss[lane * GQ + h] = p0;
-            ss[(lane + 32) * GQ + h] = p1;
-            m_h = m;
-            l_h = l;
+            if (writer) *reinterpret_cast<float2*>(dst + 8 * u + 2 * c) = make_float2(o0, o1);
         }
-        __syncthreads();
-        // q of the next item: issue its loads now, land them after the PV loop.
-        float qn[QPT];
-        const int item_n = blockIdx.x + (j + 1) * gridDim.x;
-        if (item_n < n_items) {
-            const AttnItem nx = attn_item(a, item_n);
-            const float* qg = a.q + ((size_t)nx.b * a.nh + (size_t)nx.kvh * GQ) * HD;
-#pragma unroll
-            for (int i = 0; i < QPT; ++i) qn[i] = tid + i * AT_THREADS < QN ? qg[tid + i * AT_THREADS] : 0.0f;
-        }
-        // ---- o = sum_k p_k V_k for head pv_h, dims pv_d0 .. +7, keys k = pv_kr (mod KGR)
-        {
-            float o[8];
-#pragma unroll
-            for (int d = 0; d < 8; ++d) o[d] = 0.0f;
-            const __half* vs = reinterpret_cast<const __half*>(stg + L::K_BYTES);
-            if (pv_on)
-                for (int k = pv_kr; k < it.n; k += KGR) {
-                    const uint4 vv = lds_v4(vs + k * HD + pv_d0);
-                    const float pk = ss[k * GQ + pv_h];
-                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
-                    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
-                    const float2 v45 = __half22float2(*reinterpret_cast<const __half2*>(&vv.z));
-                    const float2 v67 = __half22float2(*reinterpret_cast<const __half2*>(&vv.w));
-                    o[0] = __fmaf_rn(pk, v01.x, o[0]);
-                    o[1] = __fmaf_rn(pk, v01.y, o[1]);
-                    o[2] = __fmaf_rn(pk, v23.x, o[2]);
-                    o[3] = __fmaf_rn(pk, v23.y, o[3]);
-                    o[4] = __fmaf_rn(pk, v45.x, o[4]);
-                    o[5] = __fmaf_rn(pk, v45.y, o[5]);
-                    o[6] = __fmaf_rn(pk, v67.x, o[6]);
-                    o[7] = __fmaf_rn(pk, v67.y, o[7]);
-                }
-            // sum the key residue classes (lanes LPK, 2*LPK, ... apart), fixed tree
-#pragma unroll
-            for (int off = LPK; off < 32; off <<= 1)
-#pragma unroll
-                for (int d = 0; d < 8; ++d) o[d] = __fadd_rn(o[d], __shfl_xor_sync(FULL_MASK, o[d], off));
-            float* dst = a.part + (((size_t)it.b * a.nh + it.kvh * GQ + pv_h) * a.max_splits + it.s) * ATT_REC(HD);
-            if (pv_on && pv_kr == 0) {
-                *reinterpret_cast<float4*>(dst + pv_d0) = make_float4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<float4*>(dst + pv_d0 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        if (writer && c == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(m, l);
+
+        __syncwarp();  // the stage is consumed: refill it
+        if (k + S < nk) {
+            const AttnItem nx = tab.item(a, lane, gitem(k + S));
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(nx, k + S);
             }
-        }
-        if (warp < GQ && lane == 0) {
-            float* dst = a.part + (((size_t)it.b * a.nh + it.kvh * GQ + warp) * a.max_splits + it.s) * ATT_REC(HD);
-            dst[HD] = m_h;
-            dst[HD + 1] = l_h;
-        }
-        if (item_n < n_items) {
-            float* qd_next = qsb + ((j + 1) & 1) * GQ * HD;
-#pragma unroll
-            for (int i = 0; i < QPT; ++i)
-                if (tid + i * AT_THREADS < QN) qd_next[tid + i * AT_THREADS] = qn[i];
-        }
-        __syncthreads();  // the stage is consumed: refill it
-        if (tid == 0) {
-            const int nxt = blockIdx.x + (j + AT_STAGES) * gridDim.x;
-            if (nxt < n_items) issue(attn_item(a, nxt), j + AT_STAGES);
         }
     }
+    // After a wait gave up, copies may still be in flight: before the CTA's shared
+    // memory is released, wait (bounded) for the last item issued into each stage.
+    __syncthreads();
+    if (threadIdx.x == 0 && *cta_failed)
+        for (int st = 0; st < S; ++st) {
+            const int k = stage_item[st];
+            if (k >= 0) (void)mbar_wait_bounded(&bar[st], (uint32_t)(k / S) & 1u);
+        }
 }
 
 // Merge a (session, head)'s splits in split order:
 //   M = max_s m_s,  out = fp16( sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s ).
-// The per-split (m, l) pairs are staged in shared memory by parallel loads; the
-// weights e^{m_s - M} are computed once; each thread then sums its dimension
-// over the splits with independent loads.
+// Thread d owns output dimension d and splits d, d + HD, ...: the loads of the
+// splits' (m, l) and of the first COMB_BATCH splits' o[d] go out together; the
+// denominator is a fixed tree over the threads (each summing its own splits in
+// order), the numerator a sum over the splits in order.  Both orders depend on
+// the split count only.
 constexpr int COMB_MAX_SPLITS = ATT_MAX_SPLITS;
+constexpr int COMB_BATCH = 16;
 
 template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __shared__ float wts[COMB_MAX_SPLITS];
-    __shared__ float ls[COMB_MAX_SPLITS];
-    __shared__ float red[HD / 32];
-    __shared__ float Msh, Lsh;
+    __shared__ float red_m[HD / 32], red_l[HD / 32];
     pdl_wait();
     pdl_launch_dependents();
-    const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x;
+    const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     if (b >= a.B) return;
     const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
+    float o[COMB_BATCH];
+#pragma unroll
+    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < ns ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
     float mloc = -INFINITY;
     for (int s = d; s < ns; s += HD) {
-        const float2 ml = *reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD);
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
         wts[s] = ml.x;
-        ls[s] = ml.y;
         mloc = fmaxf(mloc, ml.x);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(FULL_MASK, mloc, o));
-    if ((d & 31) == 0) red[d >> 5] = mloc;
+    for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(FULL_MASK, mloc, off));
+    if (lane == 0) red_m[warp] = mloc;
     __syncthreads();
-    if (d == 0) {
-        float M = red[0];
-        for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, red[w]);
-        Msh = M;
+    float M = red_m[0];
+#pragma unroll
+    for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, red_m[w]);
+    float den = 0.0f;
+    for (int s = d; s < ns; s += HD) {
+        const float l = __ldcg(p + (size_t)s * ATT_REC(HD) + HD + 1);
+        const float e = expf(__fsub_rn(wts[s], M));
+        wts[s] = e;
+        den = __fmaf_rn(e, l, den);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den = __fadd_rn(den, __shfl_xor_sync(FULL_MASK, den, off));
+    if (lane == 0) red_l[warp] = den;
     __syncthreads();
-    const float M = Msh;
-    for (int s = d; s < ns; s += HD) wts[s] = expf(__fsub_rn(wts[s], M));
-    __syncthreads();
-    if (d == 0) {
-        float den = 0.0f;
-        for (int s = 0; s < ns; ++s) den = __fmaf_rn(wts[s], ls[s], den);
-        Lsh = den;
-    }
+    float L = red_l[0];
+#pragma unroll
+    for (int w = 1; w < HD / 32; ++w) L = __fadd_rn(L, red_l[w]);
     float num = 0.0f;
-    int s = 0;
-    for (; s + 4 <= ns; s += 4) {
-        const float o0 = p[(size_t)(s + 0) * ATT_REC(HD) + d], o1 = p[(size_t)(s + 1) * ATT_REC(HD) + d];
-        const float o2 = p[(size_t)(s + 2) * ATT_REC(HD) + d], o3 = p[(size_t)(s + 3) * ATT_REC(HD) + d];
-        num = __fmaf_rn(wts[s + 0], o0, num);
-        num = __fmaf_rn(wts[s + 1], o1, num);
-        num = __fmaf_rn(wts[s + 2], o2, num);
-        num = __fmaf_rn(wts[s + 3], o3, num);
+#pragma unroll
+    for (int s = 0; s < COMB_BATCH; ++s)
+        if (s < ns) num = __fmaf_rn(wts[s], o[s], num);
+    for (int s0 = COMB_BATCH; s0 < ns; s0 += COMB_BATCH) {
+#pragma unroll
+        for (int s = 0; s < COMB_BATCH; ++s)
+            o[s] = s0 + s < ns ? __ldcg(p + (size_t)(s0 + s) * ATT_REC(HD) + d) : 0.0f;
+#pragma unroll
+        for (int s = 0; s < COMB_BATCH; ++s)
+            if (s0 + s < ns) num = __fmaf_rn(wts[s0 + s], o[s], num);
     }
-    for (; s < ns; ++s) num = __fmaf_rn(wts[s], p[(size_t)s * ATT_REC(HD) + d], num);
-    __syncthreads();
-    a.out[(size_t)b * a.nh * HD + (size_t)h * HD + d] = __float2half_rn(__fdiv_rn(num, Lsh));
+    a.out[(size_t)b * a.nh * HD + (size_t)h * HD + d] = __float2half_rn(__fdiv_rn(num, L));
 }
 
 // Standalone append (the op-level entry point; the step appends in the QKV epilogue).
@@ -403,7 +501,7 @@ cudaError_t attn_init_attributes() {
     cudaError_t e = cudaSuccess;
 #define KD_SET(HD_, GQ_)                                                                             \
     e = cudaFuncSetAttribute(attn_split_kernel<HD_, GQ_>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             AttnSmem<HD_, GQ_>::TOTAL);                                             \
+                             AttnSmem<HD_>::TOTAL);                                                  \
     if (e != cudaSuccess) return e;                                                                  \
     e = cudaFuncSetAttribute(attn_split_kernel<HD_, GQ_>, cudaFuncAttributePreferredSharedMemoryCarveout, \
                              cudaSharedmemCarveoutMaxShared);                                        \
@@ -427,7 +525,7 @@ int attn_split_grid(int num_sms, int hd, int group) {
     cudaError_t e = cudaSuccess;
 #define KD_OCC(HD_, GQ_)                                                                     \
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<HD_, GQ_>, \
-                                                      AT_THREADS, AttnSmem<HD_, GQ_>::TOTAL);
+                                                      AT_WARPS * 32, AttnSmem<HD_>::TOTAL);
     auto run = [&]() -> cudaError_t {
         if (hd == 64) { KD_ATT_DISPATCH(64, KD_OCC) } else { KD_ATT_DISPATCH(128, KD_OCC) }
         return e;
@@ -442,7 +540,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t make_attn_maps(const __half* k_arena, long rows, int hd, AttnMaps* out) {
+cudaError_t make_attn_maps(const __half* k_arena, const __half* v_arena, long rows, int hd, AttnMaps* out) {
     static EncodeTiledFn encode = nullptr;
     if (!encode) {
         void* fn = nullptr;
@@ -458,15 +556,19 @@ cudaError_t make_attn_maps(const __half* k_arena, long rows, int hd, AttnMaps* o
     const cuuint32_t estr[2] = {1, 1};
     const cuuint32_t box_full[2] = {64, (cuuint32_t)ATT_CHUNK};
     const cuuint32_t box_tail[2] = {64, 8};
-    void* base = const_cast<__half*>(k_arena);
-    CUresult r = encode(&out->k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box_full, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    r = encode(&out->k8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box_tail, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    struct {
+        CUtensorMap* map;
+        const __half* base;
+        const cuuint32_t* box;
+    } const todo[4] = {{&out->k, k_arena, box_full}, {&out->k8, k_arena, box_tail},
+                       {&out->v, v_arena, box_full}, {&out->v8, v_arena, box_tail}};
+    for (const auto& t : todo) {
+        const CUresult r = encode(t.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(t.base), dims, strides,
+                                  t.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
 }
 
 static cudaError_t launch_cfg(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pdl) {
@@ -483,11 +585,11 @@ cudaError_t launch_attn_split(const AttnArgs& a, const AttnMaps& maps, int grid,
     cudaLaunchAttribute attr[1];
     launch_cfg(cfg, attr, pdl);
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(AT_THREADS);
     cfg.stream = s;
-#define KD_LAUNCH(HD_, GQ_)                               \
-    cfg.dynamicSmemBytes = AttnSmem<HD_, GQ_>::TOTAL;     \
-    return cudaLaunchKernelEx(&cfg, attn_split_kernel<HD_, GQ_>, a, maps.k, maps.k8);
+#define KD_LAUNCH(HD_, GQ_)                                 \
+    cfg.blockDim = dim3(AT_WARPS * 32);                     \
+    cfg.dynamicSmemBytes = AttnSmem<HD_>::TOTAL;            \
+    return cudaLaunchKernelEx(&cfg, attn_split_kernel<HD_, GQ_>, a, maps.k, maps.k8, maps.v, maps.v8);
     if (a.hd == 64) { KD_ATT_DISPATCH(64, KD_LAUNCH) } else if (a.hd == 128) { KD_ATT_DISPATCH(128, KD_LAUNCH) }
 #undef KD_LAUNCH
     return cudaErrorInvalidValue;

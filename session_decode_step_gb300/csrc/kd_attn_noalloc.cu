@@ -76,8 +76,9 @@ extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* 
                     "kd_attn_append_decode_noalloc: B * n_heads * ceil(cap/64) * (head_dim + 4) * 4 + 256 = " +
                         std::to_string(need) + " bytes exceeds the fixed scratch of " +
                         std::to_string((size_t)KD_ATTN_NOALLOC_SCRATCH_BYTES) + " bytes");
-    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
-        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_noalloc: caches must be 16-byte aligned");
+    if (((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) ||
+        (reinterpret_cast<uintptr_t>(q) & 7))
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_noalloc: caches must be 16-byte aligned, q 8-byte");
     DescArgs d{};
     for (int b = 0; b < B; ++b) {
         if (slots[b] < 0 || slots[b] >= n_slots) return fail(KD_ERR_BAD_SESSION, "slot out of range");
@@ -103,8 +104,8 @@ extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* 
         kd::ensure_device_attributes(dev) != cudaSuccess)
         return fail(KD_ERR_CUDA, "kd_attn_append_decode_noalloc: device set-up failed");
     kd::AttnMaps maps;
-    if (kd::make_attn_maps(reinterpret_cast<const __half*>(k_cache), (long)n_slots * n_kv_heads * cap, head_dim,
-                           &maps) != cudaSuccess)
+    if (kd::make_attn_maps(reinterpret_cast<const __half*>(k_cache), reinterpret_cast<const __half*>(v_cache),
+                           (long)n_slots * n_kv_heads * cap, head_dim, &maps) != cudaSuccess)
         return fail(KD_ERR_CUDA, "kd_attn_append_decode_noalloc: tensor map encoding failed");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int* desc = reinterpret_cast<int*>(g_scratch_ptr[dev]);

@@ -68,6 +68,8 @@ void plan_split(PackedQ8& m, int num_sms, int force_mode = -1);
 cudaError_t launch_repack(const uint8_t* src, int K, const int* tile_src, int G, uint8_t* dst,
                           cudaStream_t s);
 
+constexpr int MMVQ_WARPS = 8;  // warps per mmvq CTA
+
 struct MmvqArgs {
     const uint8_t* w;
     int G, KG, W, maxc, K;
@@ -108,7 +110,7 @@ struct AttnArgs {
     const float* q;       // [B][nh][hd] fp32, rotated
     const __half* kc;     // this layer's arenas [slots][nkv][cap][hd] fp16
     const __half* vc;
-    long row0;            // this layer's first row in the K tensor map ([rows][hd] over the whole arena)
+    long row0;            // this layer's first row in the tensor maps ([rows][hd] over the whole arenas)
     const int* slot;      // [B]
     const int* pos;       // [B]; the row attends keys 0..pos
     int B, nh, nkv, hd, cap;
@@ -119,12 +121,12 @@ struct AttnArgs {
     int* err;
 };
 
-// Tensor maps over a K arena viewed as [rows][hd] fp16: 64-row boxes and 8-row
-// boxes (ragged tails) of 64-dim halves, 128-byte swizzle.
+// Tensor maps over the K and V arenas, each viewed as [rows][hd] fp16: 64-row
+// boxes and 8-row boxes (ragged tails) of 64-dim halves, 128-byte swizzle.
 struct AttnMaps {
-    CUtensorMap k, k8;
+    CUtensorMap k, k8, v, v8;
 };
-cudaError_t make_attn_maps(const __half* k_arena, long rows, int hd, AttnMaps* out);
+cudaError_t make_attn_maps(const __half* k_arena, const __half* v_arena, long rows, int hd, AttnMaps* out);
 
 bool attn_supported(int hd, int group);
 cudaError_t launch_attn_split(const AttnArgs& a, const AttnMaps& maps, int grid, bool pdl, cudaStream_t s);
@@ -148,8 +150,11 @@ cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float 
 cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
                                  __half* xn, bool pdl, cudaStream_t s);
 cudaError_t rowops_init_attributes();
-// out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none)
-cudaError_t launch_argmax(const float* logits, int B, int V, int* out, bool pdl, cudaStream_t s);
+// out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none).
+// keys [>= B] and done: device scratch that is zero before the first launch;
+// every launch leaves it zero again.  V must be a multiple of 4.
+cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
+                          bool pdl, cudaStream_t s);
 
 // Set the calling thread's last-error message (what kd_last_error() returns).
 void set_last_error(const char* msg);

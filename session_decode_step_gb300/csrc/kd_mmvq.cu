@@ -22,6 +22,7 @@ cudaError_t mmvq_cta_init_attributes();
 cudaError_t launch_mmvq_stream(const MmvqArgs& a, int epi, bool pdl, cudaStream_t s);
 cudaError_t launch_mmvq_cta(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s);
 
+
 void plan_split(PackedQ8& m, int num_sms, int force_mode) {
     m.mode = force_mode >= 0 ? force_mode : (m.G <= 2 * num_sms ? MMVQ_GROUP : MMVQ_STREAM);
     // stream: W warps, each a contiguous run of the T = G * KG stages; W never

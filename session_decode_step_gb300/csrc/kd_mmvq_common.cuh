@@ -15,8 +15,7 @@
 
 namespace kd {
 
-constexpr int MMVQ_WARPS = 8;
-constexpr int RING = 3;        // weight stages in flight per warp
+constexpr int RING = 4;        // weight stages in flight per warp
 constexpr int NORM_SLOTS = MAX_NORM_SLOTS;
 
 // One stage (one 128-column k-group of a 32-row group) into the accumulators.

@@ -13,23 +13,31 @@
 
 namespace kd {
 
-template <int NT>
+// PAIR: a launch with one CTA per group for SMs < G <= 2 * SMs (B <= 8): a
+// shallower ring and the partial buffer laid over it let two CTAs share an SM,
+// so no CTA waits for a second group while others idle.
+template <int NT, bool PAIR>
 struct CtaSmem {
+    static constexpr int RD = PAIR ? 3 : RING;     // weight stages in flight per warp
     static constexpr int RS = NT == 1 ? 9 : 16;  // partial-row stride (floats), padded against bank conflicts
-    static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RING * STAGE_BYTES;
+    static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
     static constexpr size_t BAR_OFF = RING_BYTES;
-    static constexpr size_t RED_OFF = BAR_OFF + MMVQ_WARPS * RING * sizeof(uint64_t);
-    static constexpr size_t TOTAL = RED_OFF + (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
+    static constexpr size_t RED_BYTES = (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
+    static constexpr size_t RED_OFF = PAIR ? 0 : BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
+    static constexpr size_t TOTAL = PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES;
+    static_assert(!PAIR || RED_BYTES <= RING_BYTES, "the partial buffer lies over the ring");
 };
 
-template <int NT, int EPI>
+template <int NT, int EPI, bool PAIR>
 __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_kernel(const MmvqArgs a) {
-    using L = CtaSmem<NT>;
+    using L = CtaSmem<NT, PAIR>;
+    constexpr int RD = L::RD;
+    static_assert(!PAIR || NT == 1, "two CTAs per SM need the one-tile register budget");
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
-    uint8_t* ring = smem + (size_t)warp * RING * STAGE_BYTES;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RING;
+    uint8_t* ring = smem + (size_t)warp * RD * STAGE_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
     float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [warp][32 rows][RS]
 
     const int kg0 = warp * a.KG / MMVQ_WARPS, nk = (warp + 1) * a.KG / MMVQ_WARPS - kg0;
@@ -37,7 +45,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
     const int total = ngrp * nk;
 
     if (lane == 0) {
-        for (int i = 0; i < RING; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < RD; ++i) mbar_init(&bar[i], 1);
         mbar_init_fence();
     }
     __syncwarp();
@@ -55,7 +63,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
     // The weights do not depend on earlier kernels: start streaming them before
     // waiting for the producer of the activations.
     if (lane == 0)
-        for (int i = 0; i < RING && i < total; ++i) issue_next(i);
+        for (int i = 0; i < RD && i < total; ++i) issue_next(i);
     pdl_wait();
     pdl_launch_dependents();
 
@@ -86,15 +94,15 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
             if (__any_sync(FULL_MASK, !ok)) {
                 // Give up: flag it, let every copy already issued land, stop computing.
                 if (lane == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
-                for (int t = sidx; t < total && t < sidx + RING; ++t)
-                    (void)mbar_wait_bounded(&bar[t % RING], (uint32_t)(t / RING) & 1u);
+                for (int t = sidx; t < total && t < sidx + RD; ++t)
+                    (void)mbar_wait_bounded(&bar[t % RD], (uint32_t)(t / RD) & 1u);
                 failed = true;
                 break;
             }
             mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, x0, acc);
             __syncwarp();
-            if (lane == 0 && sidx + RING < total) issue_next(slot);
-            if (++slot == RING) { slot = 0; phase ^= 1u; }
+            if (lane == 0 && sidx + RD < total) issue_next(slot);
+            if (++slot == RD) { slot = 0; phase ^= 1u; }
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
@@ -104,6 +112,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
                 }
         }
         // ---- the group's partials meet in shared memory (every warp takes part) ----
+        if constexpr (PAIR) __syncthreads();  // every warp is done with the ring the partials lie over
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -149,54 +158,61 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
     }
 }
 
-template <int NT>
-size_t cta_smem_bytes() {
-    return CtaSmem<NT>::TOTAL;
-}
-
-template <int NT, int EPI>
+template <int NT, int EPI, bool PAIR>
 static cudaError_t cta_attr() {
-    cudaError_t e = cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)cta_smem_bytes<NT>());
+    cudaError_t e = cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)CtaSmem<NT, PAIR>::TOTAL);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
-template <int NT, int EPI>
+template <int NT, int EPI, bool PAIR>
 static cudaError_t cta_launch(const MmvqArgs& a, int grid, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(MMVQ_WARPS * 32);
-    cfg.dynamicSmemBytes = cta_smem_bytes<NT>();
+    cfg.dynamicSmemBytes = CtaSmem<NT, PAIR>::TOTAL;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI>, a);
+    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI, PAIR>, a);
 }
 
-#define KD_CTA_CASES(X, NT_) X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID)
+#define KD_CTA_CASES(X, NT_, PAIR_) \
+    X(NT_, EPI_STORE, PAIR_) X(NT_, EPI_SWIGLU, PAIR_) X(NT_, EPI_QKV, PAIR_) X(NT_, EPI_RESID, PAIR_)
 
 cudaError_t mmvq_cta_init_attributes() {
     cudaError_t e;
-#define KD_A(NT_, EPI_) \
-    if ((e = cta_attr<NT_, EPI_>()) != cudaSuccess) return e;
-    KD_CTA_CASES(KD_A, 1)
-    KD_CTA_CASES(KD_A, 2)
+#define KD_A(NT_, EPI_, PAIR_) \
+    if ((e = cta_attr<NT_, EPI_, PAIR_>()) != cudaSuccess) return e;
+    KD_CTA_CASES(KD_A, 1, false)
+    KD_CTA_CASES(KD_A, 2, false)
+    KD_CTA_CASES(KD_A, 1, true)
 #undef KD_A
     return cudaSuccess;
 }
 
+// One CTA per group when the groups outnumber the SMs by at most 2x and the
+// one-tile kernel is used (two CTAs fit an SM); otherwise min(G, SMs) CTAs that
+// each take groups c, c + grid, ...
+int mmvq_cta_grid(int G, int B, int num_sms, bool* pair) {
+    *pair = B <= 8 && G > num_sms && G <= 2 * num_sms;
+    return *pair ? G : (G < num_sms ? G : num_sms);
+}
+
 cudaError_t launch_mmvq_cta(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s) {
     const bool wide = a.B > 8;
-    const int grid = a.G < num_sms ? a.G : num_sms;
-#define KD_L(NT_, EPI_) \
-    if (epi == EPI_ && (NT_ == 2) == wide) return cta_launch<NT_, EPI_>(a, grid, pdl, s);
-    KD_CTA_CASES(KD_L, 1)
-    KD_CTA_CASES(KD_L, 2)
+    bool pair = false;
+    const int grid = mmvq_cta_grid(a.G, a.B, num_sms, &pair);
+#define KD_L(NT_, EPI_, PAIR_) \
+    if (epi == EPI_ && (NT_ == 2) == wide && PAIR_ == pair) return cta_launch<NT_, EPI_, PAIR_>(a, grid, pdl, s);
+    KD_CTA_CASES(KD_L, 1, false)
+    KD_CTA_CASES(KD_L, 2, false)
+    KD_CTA_CASES(KD_L, 1, true)
 #undef KD_L
     return cudaErrorInvalidValue;
 }

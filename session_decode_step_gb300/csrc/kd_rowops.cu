@@ -35,7 +35,21 @@ __device__ __forceinline__ void norm_row(const float* x, int H, const float* w, 
     }
     __syncthreads();
     const float r = rsh;
-    for (int i = tid; i < H; i += EMBED_THREADS) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(x[i], r), w[i]));
+    constexpr int U = 16;  // loads issued together
+    for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
+        float xv[U], wv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + tid + EMBED_THREADS * u;
+            xv[u] = i < H ? x[i] : 0.0f;
+            wv[u] = i < H ? w[i] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + tid + EMBED_THREADS * u;
+            if (i < H) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(xv[u], r), wv[u]));
+        }
+    }
 }
 
 // x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), then the
@@ -49,15 +63,28 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
     const int b = blockIdx.x, tid = threadIdx.x;
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
     float* xr = x + (size_t)b * H;
+    constexpr int U = 16;  // elements per thread whose loads are issued together
     float s = 0.0f;
-    for (int i = tid; i < H; i += EMBED_THREADS) {
-        const uint8_t* blk = row + (i >> 5) * 34;
-        const __half_raw hr{(unsigned short)(blk[0] | (blk[1] << 8))};
-        const float d = __half2float(__half(hr));
-        const float q = (float)(int8_t)blk[2 + (i & 31)];
-        const float v = __fmul_rn(q, d);
-        xr[i] = v;
-        s = __fmaf_rn(v, v, s);
+    for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
+        int8_t q[U];
+        unsigned short dbits[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + tid + EMBED_THREADS * u;
+            const uint8_t* blk = row + (i >> 5) * 34;
+            q[u] = i < H ? (int8_t)blk[2 + (i & 31)] : (int8_t)0;
+            dbits[u] = i < H ? (unsigned short)(blk[0] | (blk[1] << 8)) : (unsigned short)0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + tid + EMBED_THREADS * u;
+            if (i < H) {
+                const __half_raw hr{dbits[u]};
+                const float v = __fmul_rn((float)q[u], __half2float(__half(hr)));
+                xr[i] = v;
+                s = __fmaf_rn(v, v, s);
+            }
+        }
     }
     norm_row(xr, H, w, eps, xn + (size_t)b * H, s);  // each thread re-reads only what it wrote
 }
@@ -93,16 +120,29 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float
     pdl_wait();
     pdl_launch_dependents();
     const int b = blockIdx.y, tid = threadIdx.x;
+    const int i = blockIdx.x * NORM_COLS + tid * 4;
+    const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
+    const float4 g = i < H ? *reinterpret_cast<const float4*>(w + i) : make_float4(0, 0, 0, 0);
     if (tid < 32) {
+        // lane l adds groups l, l + 32, l + 64, ... in order; the loads of 8 of
+        // them are issued together
+        const int ng = H / 32;
         float s = 0.0f;
-        for (int g = tid; g < H / 32; g += 32) s = __fadd_rn(s, ssq[(size_t)g * MAX_NORM_SLOTS + b]);
+        for (int g0 = 0; g0 < ng; g0 += 8 * 32) {
+            float part[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gi = g0 + tid + 32 * j;
+                part[j] = gi < ng ? ssq[(size_t)gi * MAX_NORM_SLOTS + b] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (g0 + tid + 32 * j < ng) s = __fadd_rn(s, part[j]);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
         if (tid == 0) rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
     }
-    const int i = blockIdx.x * NORM_COLS + tid * 4;
-    const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
-    const float4 g = i < H ? *reinterpret_cast<const float4*>(w + i) : make_float4(0, 0, 0, 0);
     __syncthreads();
     if (i >= H) return;
     const float r = rsh;
@@ -125,42 +165,64 @@ cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H,
     return cudaLaunchKernelEx(&cfg, norm_from_ssq_kernel, x, ssq, H, w, eps, xn);
 }
 
-constexpr int ARGMAX_THREADS = 1024;
+// Greedy argmax over many CTAs.  Each (value, index) maps to a 64-bit key whose
+// unsigned order is the pick order -- larger value first, then lower index; -0
+// counts as +0; NaN maps to 0 and never wins -- so every CTA can merge its best
+// key into keys[b] with an atomic maximum, in any order, with one result.  The
+// last CTA to finish turns keys into indices (-1 if nothing but NaN) and resets
+// keys and the counter for the next launch.
+constexpr int ARGMAX_THREADS = 256;
+constexpr int ARGMAX_CHUNK = ARGMAX_THREADS * 8;  // logits per CTA: two float4 per thread
 
-// (value, index) order for the greedy pick: larger value wins, equal values go
-// to the lower index, NaN never wins.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    if (v != v) return false;
-    if (bi < 0) return true;
-    return v > bv || (v == bv && i < bi);
+__device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
+    if (v != v) return 0ull;
+    if (v == 0.0f) v = 0.0f;
+    const unsigned u = __float_as_uint(v);
+    const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(~(unsigned)i);
 }
 
-__global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __restrict__ logits,
-                                                                int V, int* __restrict__ out) {
-    __shared__ float sv[ARGMAX_THREADS / 32];
-    __shared__ int si[ARGMAX_THREADS / 32];
+__global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __restrict__ logits, int V,
+                                                                unsigned long long* keys, unsigned* done,
+                                                                int* __restrict__ out) {
+    __shared__ unsigned long long wbest[ARGMAX_THREADS / 32];
+    __shared__ bool last;
     pdl_wait();
     pdl_launch_dependents();
-    const int b = blockIdx.x, tid = threadIdx.x;
+    const int b = blockIdx.y, tid = threadIdx.x;
     const float* row = logits + (size_t)b * V;
-    float bv = 0.0f;
-    int bi = -1;
-    for (int i = tid; i < V; i += ARGMAX_THREADS) {
-        const float v = row[i];
-        if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    const int i0 = blockIdx.x * ARGMAX_CHUNK + tid * 4;
+    float4 v[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = i0 + h * ARGMAX_THREADS * 4;
+        v[h] = i < V ? __ldcg(reinterpret_cast<const float4*>(row + i)) : make_float4(NAN, NAN, NAN, NAN);
+    }
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = i0 + h * ARGMAX_THREADS * 4;
+        best = max(best, argmax_key(v[h].x, i));
+        best = max(best, argmax_key(v[h].y, i + 1));
+        best = max(best, argmax_key(v[h].z, i + 2));
+        best = max(best, argmax_key(v[h].w, i + 3));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(FULL_MASK, bv, o);
-        const int oi = __shfl_xor_sync(FULL_MASK, bi, o);
-        if (oi >= 0 && better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if ((tid & 31) == 0) { sv[tid >> 5] = bv; si[tid >> 5] = bi; }
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(FULL_MASK, best, o));
+    if ((tid & 31) == 0) wbest[tid >> 5] = best;
     __syncthreads();
     if (tid == 0) {
-        for (int w = 1; w < ARGMAX_THREADS / 32; ++w)
-            if (si[w] >= 0 && better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
-        out[b] = bi;
+        for (int w = 1; w < ARGMAX_THREADS / 32; ++w) best = max(best, wbest[w]);
+        if (best) atomicMax(&keys[b], best);
+        __threadfence();
+        last = atomicAdd(done, 1u) == gridDim.x * gridDim.y - 1;
+    }
+    __syncthreads();
+    if (last && tid < (int)gridDim.y) {
+        __threadfence();
+        const unsigned long long k = atomicExch(&keys[tid], 0ull);
+        out[tid] = k ? (int)(~(unsigned)(k & 0xffffffffull)) : -1;
+        if (tid == 0) *done = 0u;
     }
 }
 
@@ -194,14 +256,16 @@ cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H
     return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn);
 }
 
-cudaError_t launch_argmax(const float* logits, int B, int V, int* out, bool pdl, cudaStream_t s) {
+cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
+                          bool pdl, cudaStream_t s) {
+    if (V % 4) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
-    cfg.gridDim = dim3(B);
+    cfg.gridDim = dim3((V + ARGMAX_CHUNK - 1) / ARGMAX_CHUNK, B);
     cfg.blockDim = dim3(ARGMAX_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, out);
+    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, keys, done, out);
 }
 
 }  // namespace kd

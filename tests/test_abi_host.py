@@ -72,6 +72,16 @@ def test_unsupported_model_shapes_fail_before_cuda(lib):
     assert not h.value
 
 
+def test_argmax_argument_checks(lib):
+    fake = C.c_void_p(1 << 20)  # never dereferenced: every check runs on the host first
+    assert lib.kd_argmax(None, 1, 8, fake, fake, None) == -1
+    assert lib.kd_argmax(fake, 0, 8, fake, fake, None) == -7
+    assert lib.kd_argmax(fake, 17, 8, fake, fake, None) == -7
+    assert lib.kd_argmax(fake, 1, 6, fake, fake, None) == -1
+    assert lib.kd_argmax(C.c_void_p((1 << 20) + 4), 1, 8, fake, fake, None) == -1
+    assert "aligned" in kd.kd_last_error()
+
+
 def test_op_level_argument_checks(lib):
     m = synth.q8_0_matrix(0, "abi", 48, 128)  # 48 rows: not a multiple of 32
     h = C.c_void_p()

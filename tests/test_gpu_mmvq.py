@@ -62,7 +62,9 @@ def test_mmvq_config_shapes_row_identity_and_oracle(kdlib, rows, cols):
         kd.kd_q8_matrix_free(h)
 
 
-@pytest.mark.parametrize("rows,cols", [(32, 128), (96, 384), (160, 1152), (4096, 14336)])
+# 6144 x 4096 (the fused q|k|v shape): more row groups than SMs, at most twice as
+# many -- one CTA per group, two per SM, for m <= 8; the 16-column kernel above.
+@pytest.mark.parametrize("rows,cols", [(32, 128), (96, 384), (160, 1152), (4096, 14336), (6144, 4096)])
 def test_mmvq_small_and_ragged(kdlib, rows, cols):
     kd = kdlib
     W = synth.q8_0_matrix(1, f"mmvq-s-{rows}x{cols}", rows, cols)
