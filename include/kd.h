@@ -201,7 +201,7 @@ kd_status kd_q8_matrix_free(kd_q8_matrix* w);
 /* Weight-only Q8_0 matrix-vector product for m = 1..16 rows (memra's batched
  * verify-tier mmvq, "bit-identical per (token,row) to m=1"):
  *   y[r][o] = sum over blocks b of d[o][b] * sum_j q[o][b][j] * x[r][32b+j]
- * x: device fp16 [m][cols]; y: device fp32 [m][rows].  Row r of y is
+ * x: device fp16 [m][cols], 16-byte aligned; y: device fp32 [m][rows].  Row r of y is
  * bit-identical for every m.  Calls on one matrix must be stream-ordered
  * (they share its workspace). */
 kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,

@@ -138,6 +138,7 @@ struct kd_model {
     __half* vc = nullptr;
     size_t layer_kv = 0;      // elements per layer of one arena
     kd::AttnMaps kmaps{};     // tensor maps over the K and V arenas
+    CUtensorMap map_xn{}, map_attn{}, map_act{};  // activation maps the projections read through
     float* x = nullptr;       // [16][H] residual stream
     __half* xn = nullptr;     // [16][H] normed activations (written by the fused RMSNorm)
     float* ssq = nullptr;     // [H/32][16] per-group sums of squares of the residual rows
@@ -295,6 +296,9 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->q, (size_t)MB * nh * hd * sizeof(float)));
     KD_CK(m->alloc(&m->attn, (size_t)MB * nh * hd * sizeof(__half)));
     KD_CK(m->alloc(&m->act, (size_t)MB * F * sizeof(__half)));
+    KD_CK(kd::make_x_map(m->xn, H, MB, &m->map_xn));
+    KD_CK(kd::make_x_map(m->attn, nh * hd, MB, &m->map_attn));
+    KD_CK(kd::make_x_map(m->act, F, MB, &m->map_act));
     size_t part = m->head.part_floats();
     int max_g = m->head.G;
     for (auto* v : {&m->qkv, &m->wo, &m->gu, &m->down})
@@ -400,7 +404,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
-        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
+        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->map_xn, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
         kd::AttnArgs t{};
         t.q = m->q; t.kc = kc; t.vc = vc; t.row0 = (long)l * c.max_sessions * nkv * c.max_ctx;
         t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
@@ -410,14 +414,14 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
         a = mm(m->wo[l], m->attn);
         resid(a);
-        KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
         KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * l + 1) * H));  // the FFN norm
         a = mm(m->gu[l], m->xn);
         a.act = m->act; a.ld = F;
-        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
+        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
         a = mm(m->down[l], m->act);
         resid(a);
-        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
         if (whole || l + 1 < l1)  // next layer's attention norm, or the output norm
             KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H));
         if (whole && m->hidden_dbg &&
@@ -428,7 +432,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     if (!whole) return cudaSuccess;
     kd::MmvqArgs a = mm(m->head, m->xn);
     a.y = lg; a.ld = V;
-    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
+    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->map_xn, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
     if (am)
         KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, m->amax_keys,
                                               reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s));
@@ -770,11 +774,14 @@ kd_status kd_q8_matrix_free(kd_q8_matrix* w) {
 kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y, kd_stream stream) {
     if (!w || !x || !y) return fail(KD_ERR_INVALID_ARG, "kd_mmvq: null argument");
     if (m < 1 || m > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_mmvq: m=%d outside [1, %d]", m, KD_MAX_BATCH);
+    if (reinterpret_cast<uintptr_t>(x) & 15) return fail(KD_ERR_INVALID_ARG, "kd_mmvq: x must be 16-byte aligned");
     kd::MmvqArgs a{};
     a.w = w->p.w; a.G = w->p.G; a.KG = w->p.KG; a.W = w->p.W; a.maxc = w->p.maxc; a.K = w->p.K;
     a.x = reinterpret_cast<const __half*>(x); a.B = m; a.part = w->part; a.cnt = w->cnt; a.err = w->err;
     a.y = y; a.ld = w->p.rows;
-    KD_CK(kd::launch_mmvq(a, w->p.mode, kd::EPI_STORE, w->num_sms, false, (cudaStream_t)stream));
+    CUtensorMap xmap;
+    KD_CK(kd::make_x_map(a.x, a.K, m, &xmap));
+    KD_CK(kd::launch_mmvq(a, xmap, w->p.mode, kd::EPI_STORE, w->num_sms, false, (cudaStream_t)stream));
     return KD_OK;
 }
 

@@ -92,14 +92,6 @@ struct AttnTable {
     }
 };
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -157,7 +149,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     constexpr int NU = HD / 8;   // 8-dim output tiles of P V
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "GQA group");
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t* smem = align1024(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -287,20 +279,28 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             __syncwarp();
         }
 
-        // ---- S = Q K^T over the 8 key tiles
+        // ---- S = Q K^T over the 8 key tiles.  k-steps outside, tiles inside: the
+        // MMAs issued back to back go to 8 different accumulators (each tile still
+        // adds its k-steps in order).
         float sacc[8][4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < 8; ++t)
 #pragma unroll
             for (int i = 0; i < 4; ++i) sacc[t][i] = 0.0f;
 #pragma unroll
-            for (int kp = 0; kp < KS / 2; ++kp) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + L::off(8 * t + (lane & 7), 4 * kp + (lane >> 3)), b0, b1, b2, b3);
-                mma_16816_acc(sacc[t], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+        for (int kp = 0; kp < KS / 2; ++kp) {
+            uint32_t kb[8][4];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                ldsm_x4(kbase + L::off(8 * t + (lane & 7), 4 * kp + (lane >> 3)), kb[t][0], kb[t][1], kb[t][2],
+                        kb[t][3]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                mma_16816_acc(sacc[t], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], kb[t][0], kb[t][1]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
                 mma_16816_acc(sacc[t], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3],
-                              b2, b3);
-            }
+                              kb[t][2], kb[t][3]);
         }
         // ---- row pair sum, scale, mask, softmax over the item's keys (4 lanes per row)
         float sv[8][2];
@@ -358,14 +358,17 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
                     pa1 = 0u;
                     pa3 = 0u;
                 }
+                uint32_t vb[NU / 2][4];
 #pragma unroll
                 for (int up = 0; up < NU / 2; ++up) {
                     const int i = lane >> 3;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(vbase + L::off(16 * js + 8 * (i & 1) + (lane & 7), 2 * up + (i >> 1)), b0, b1, b2,
-                                  b3);
-                    mma_16816_acc(oacc[2 * up], pa0, pa1, pa2, pa3, b0, b1);
-                    mma_16816_acc(oacc[2 * up + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    ldsm_x4_trans(vbase + L::off(16 * js + 8 * (i & 1) + (lane & 7), 2 * up + (i >> 1)), vb[up][0],
+                                  vb[up][1], vb[up][2], vb[up][3]);
+                }
+#pragma unroll
+                for (int up = 0; up < NU / 2; ++up) {
+                    mma_16816_acc(oacc[2 * up], pa0, pa1, pa2, pa3, vb[up][0], vb[up][1]);
+                    mma_16816_acc(oacc[2 * up + 1], pa0, pa1, pa2, pa3, vb[up][2], vb[up][3]);
                 }
             }
         }
@@ -418,7 +421,7 @@ constexpr int COMB_BATCH = 16;
 
 template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
-    __shared__ float wts[COMB_MAX_SPLITS];
+    __shared__ float wts[COMB_MAX_SPLITS], ls[COMB_MAX_SPLITS];
     __shared__ float red_m[HD / 32], red_l[HD / 32];
     pdl_wait();
     pdl_launch_dependents();
@@ -433,6 +436,7 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     for (int s = d; s < ns; s += HD) {
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
         wts[s] = ml.x;
+        ls[s] = ml.y;
         mloc = fmaxf(mloc, ml.x);
     }
 #pragma unroll
@@ -444,10 +448,9 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, red_m[w]);
     float den = 0.0f;
     for (int s = d; s < ns; s += HD) {
-        const float l = __ldcg(p + (size_t)s * ATT_REC(HD) + HD + 1);
         const float e = expf(__fsub_rn(wts[s], M));
         wts[s] = e;
-        den = __fmaf_rn(e, l, den);
+        den = __fmaf_rn(e, ls[s], den);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) den = __fadd_rn(den, __shfl_xor_sync(FULL_MASK, den, off));
@@ -540,7 +543,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t make_attn_maps(const __half* k_arena, const __half* v_arena, long rows, int hd, AttnMaps* out) {
+cudaError_t encode_fp16_2d(CUtensorMap* out, const void* base, long inner, long rows, int box_inner, int box_rows) {
     static EncodeTiledFn encode = nullptr;
     if (!encode) {
         void* fn = nullptr;
@@ -550,25 +553,25 @@ cudaError_t make_attn_maps(const __half* k_arena, const __half* v_arena, long ro
         if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (rows < 1 || rows > 0x7fffffffL || (hd != 64 && hd != 128)) return cudaErrorInvalidValue;
-    const cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
+    if (inner < 1 || rows < 1 || rows > 0x7fffffffL || (inner * 2) % 16 || (reinterpret_cast<uintptr_t>(base) & 15))
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
     const cuuint32_t estr[2] = {1, 1};
-    const cuuint32_t box_full[2] = {64, (cuuint32_t)ATT_CHUNK};
-    const cuuint32_t box_tail[2] = {64, 8};
-    struct {
-        CUtensorMap* map;
-        const __half* base;
-        const cuuint32_t* box;
-    } const todo[4] = {{&out->k, k_arena, box_full}, {&out->k8, k_arena, box_tail},
-                       {&out->v, v_arena, box_full}, {&out->v8, v_arena, box_tail}};
-    for (const auto& t : todo) {
-        const CUresult r = encode(t.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(t.base), dims, strides,
-                                  t.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    return cudaSuccess;
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+    const CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_attn_maps(const __half* k_arena, const __half* v_arena, long rows, int hd, AttnMaps* out) {
+    if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if ((e = encode_fp16_2d(&out->k, k_arena, hd, rows, 64, ATT_CHUNK)) != cudaSuccess) return e;
+    if ((e = encode_fp16_2d(&out->k8, k_arena, hd, rows, 64, 8)) != cudaSuccess) return e;
+    if ((e = encode_fp16_2d(&out->v, v_arena, hd, rows, 64, ATT_CHUNK)) != cudaSuccess) return e;
+    return encode_fp16_2d(&out->v8, v_arena, hd, rows, 64, 8);
 }
 
 static cudaError_t launch_cfg(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pdl) {

@@ -79,6 +79,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// 2-D tensor-map tile load (TMA): tile at element coordinates (x, y) of the map
+// (x innermost, x * element size a multiple of 16 bytes) into dst (aligned as the
+// map's swizzle requires), completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The first 1024-byte boundary at or after p (tiles written with the 128-byte
+// swizzle need it; dynamic shared memory is only guaranteed 16-byte alignment).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 // Same, with an L2 eviction-priority hint (for data read exactly once per step).
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
                                               uint64_t* bar, uint64_t policy) {

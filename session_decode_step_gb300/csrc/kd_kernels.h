@@ -70,10 +70,20 @@ cudaError_t launch_repack(const uint8_t* src, int K, const int* tile_src, int G,
 
 constexpr int MMVQ_WARPS = 8;  // warps per mmvq CTA
 
+// Tensor map of fp16 data viewed as [rows][inner] (128-byte swizzle, box of
+// box_rows x box_inner, zero fill outside); base 16-byte aligned, inner * 2 a
+// multiple of 16.
+cudaError_t encode_fp16_2d(CUtensorMap* out, const void* base, long inner, long rows, int box_inner, int box_rows);
+// The activation map an mmvq launch reads its input x [rows][K] through: boxes
+// of 8 rows x 64 columns (each stage loads 2 per 8 sessions).
+inline cudaError_t make_x_map(const __half* x, int K, int rows, CUtensorMap* out) {
+    return encode_fp16_2d(out, x, K, rows, 64, 8);
+}
+
 struct MmvqArgs {
     const uint8_t* w;
     int G, KG, W, maxc, K;
-    const __half* x;     // [B][K] fp16 activations
+    const __half* x;     // [B][K] fp16 activations (the kernels read them through the launch's map of x)
     int B;
     // EPI_RESID: each group's writer also leaves sum(x_new^2) of its 32 rows per
     // session in ssq_out[g][n], so the next RMSNorm needs no row reduction.
@@ -95,7 +105,9 @@ struct MmvqArgs {
     int nh, nkv, hd, cap;
 };
 
-cudaError_t launch_mmvq(const MmvqArgs& a, int mode, int epi, int num_sms, bool pdl, cudaStream_t s);
+// xmap: make_x_map of a.x with at least B rows.
+cudaError_t launch_mmvq(const MmvqArgs& a, const CUtensorMap& xmap, int mode, int epi, int num_sms, bool pdl,
+                        cudaStream_t s);
 // Smallest dynamic shared memory any mmvq launch needs (for occupancy checks).
 cudaError_t mmvq_init_attributes();
 

@@ -16,11 +16,10 @@
 
 namespace kd {
 
-size_t mmvq_stream_smem_bytes();
 cudaError_t mmvq_stream_init_attributes();
 cudaError_t mmvq_cta_init_attributes();
-cudaError_t launch_mmvq_stream(const MmvqArgs& a, int epi, bool pdl, cudaStream_t s);
-cudaError_t launch_mmvq_cta(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s);
+cudaError_t launch_mmvq_stream(const MmvqArgs& a, const CUtensorMap& xm, int epi, bool pdl, cudaStream_t s);
+cudaError_t launch_mmvq_cta(const MmvqArgs& a, const CUtensorMap& xm, int epi, int num_sms, bool pdl, cudaStream_t s);
 
 
 void plan_split(PackedQ8& m, int num_sms, int force_mode) {
@@ -102,9 +101,10 @@ cudaError_t mmvq_init_attributes() {
     return mmvq_cta_init_attributes();
 }
 
-cudaError_t launch_mmvq(const MmvqArgs& a, int mode, int epi, int num_sms, bool pdl, cudaStream_t s) {
-    if (mode == MMVQ_GROUP) return launch_mmvq_cta(a, epi, num_sms, pdl, s);
-    return launch_mmvq_stream(a, epi, pdl, s);
+cudaError_t launch_mmvq(const MmvqArgs& a, const CUtensorMap& xmap, int mode, int epi, int num_sms, bool pdl,
+                        cudaStream_t s) {
+    if (mode == MMVQ_GROUP) return launch_mmvq_cta(a, xmap, epi, num_sms, pdl, s);
+    return launch_mmvq_stream(a, xmap, epi, pdl, s);
 }
 
 }  // namespace kd

@@ -53,20 +53,32 @@ __device__ __forceinline__ void mma_stage(const uint8_t* st, int lane, int gq, c
     }
 }
 
-// ---- activation fragments -------------------------------------------------
-// Lane (gq, cq) multiplies session n = gq + 8*nt at columns 8cq .. 8cq+7 of each
-// 32-column block.  Sessions >= B read as zeros.
-//
-// Plain fp16 activations [B][K]:
+// ---- activation tiles -------------------------------------------------------
+// A stage's activations arrive with its weights: the tensor-map copy of the
+// [8 sessions][128 columns] fp16 tile for each 8 sessions, as two 64-column
+// halves of [8 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row r
+// at chunk c ^ r), 1024-byte aligned.  Rows past the map's end read as zeros;
+// rows >= B hold whatever the buffer holds and only feed MMA columns that are
+// never stored.
+constexpr int XTILE_BYTES = 2048;  // one stage, 8 sessions
+
 template <int NT>
-__device__ __forceinline__ void load_x_f16(const MmvqArgs& a, int gq, int cq, int kg, uint4 (&xv)[4][NT]) {
+__device__ __forceinline__ void tma_x_tile(uint8_t* xt, const void* xmap, int kg, uint64_t* bar) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = gq + 8 * nt;
-        const __half* p = a.x + (size_t)(n < a.B ? n : 0) * a.K + kg * KGROUP + cq * 8;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) xv[kb][nt] = n < a.B ? ldg_nc_v4(p + kb * 32) : make_uint4(0, 0, 0, 0);
-    }
+        for (int h = 0; h < 2; ++h) tma_load_2d(xt + (nt * 2 + h) * 1024, xmap, kg * KGROUP + 64 * h, 8 * nt, bar);
+}
+
+// Lane (gq, cq) multiplies session n = gq + 8*nt at columns 8cq .. 8cq+7 of each
+// 32-column block kb: the 16-byte chunk 4kb + cq of row gq.
+template <int NT>
+__device__ __forceinline__ void lds_x_tile(const uint8_t* xt, int gq, int cq, uint4 (&xv)[4][NT]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+            xv[kb][nt] = lds_v4(xt + (nt * 2 + (kb >> 1)) * 1024 + gq * 128 + ((((kb & 1) * 4 + cq) ^ gq) << 4));
 }
 
 // ---- epilogues on single outputs ------------------------------------------

@@ -16,27 +16,36 @@ namespace kd {
 // PAIR: a launch with one CTA per group for SMs < G <= 2 * SMs (B <= 8): a
 // shallower ring and the partial buffer laid over it let two CTAs share an SM,
 // so no CTA waits for a second group while others idle.
+// Shared memory: per warp a ring of RD stages, each the stage's weights and its
+// activation tiles; then the barriers and the partial-sum buffer.
 template <int NT, bool PAIR>
 struct CtaSmem {
-    static constexpr int RD = PAIR ? 3 : RING;     // weight stages in flight per warp
+    static constexpr int RD = PAIR ? 2 : (NT == 1 ? RING : RING - 1);  // stages in flight per warp
     static constexpr int RS = NT == 1 ? 9 : 16;  // partial-row stride (floats), padded against bank conflicts
+    static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * RD * NT * XTILE_BYTES;  // at a 1024-byte boundary
+    static constexpr size_t W_OFF = X_BYTES;
     static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
-    static constexpr size_t BAR_OFF = RING_BYTES;
+    static constexpr size_t BAR_OFF = W_OFF + RING_BYTES;
     static constexpr size_t RED_BYTES = (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
-    static constexpr size_t RED_OFF = PAIR ? 0 : BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
-    static constexpr size_t TOTAL = PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES;
+    static constexpr size_t RED_OFF = PAIR ? W_OFF : BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
+    static constexpr size_t TOTAL =
+        (PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES) + 1024;  // + alignment slack
     static_assert(!PAIR || RED_BYTES <= RING_BYTES, "the partial buffer lies over the ring");
 };
 
 template <int NT, int EPI, bool PAIR>
-__global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_kernel(const MmvqArgs a) {
+__global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
+    mmvq_cta_kernel(const MmvqArgs a, const __grid_constant__ CUtensorMap xm) {
     using L = CtaSmem<NT, PAIR>;
     constexpr int RD = L::RD;
+    constexpr uint32_t SB = STAGE_BYTES + NT * XTILE_BYTES;  // bytes a stage's barrier waits for
     static_assert(!PAIR || NT == 1, "two CTAs per SM need the one-tile register budget");
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
-    uint8_t* ring = smem + (size_t)warp * RD * STAGE_BYTES;
+    uint8_t* xring = smem + (size_t)warp * RD * NT * XTILE_BYTES;
+    uint8_t* ring = smem + L::W_OFF + (size_t)warp * RD * STAGE_BYTES;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
     float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [warp][32 rows][RS]
 
@@ -53,27 +62,23 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
     const uint64_t policy = l2_policy_evict_first();
     // Issue cursor: stage (group ii of this CTA, k-group kg0 + ikk).
     int ii = 0, ikk = 0;
-    auto issue_next = [&](int slot_) {
+    auto issue_w = [&](int slot_) {
         const int g = blockIdx.x + ii * gridDim.x;
-        mbar_arrive_expect_tx(&bar[slot_], STAGE_BYTES);
+        mbar_arrive_expect_tx(&bar[slot_], SB);
         bulk_g2s_hint(ring + slot_ * STAGE_BYTES, a.w + ((size_t)g * a.KG + kg0 + ikk) * STAGE_BYTES, STAGE_BYTES,
                       &bar[slot_], policy);
         if (++ikk == nk) { ikk = 0; ++ii; }
     };
     // The weights do not depend on earlier kernels: start streaming them before
-    // waiting for the producer of the activations.
+    // waiting for the producer of the activations.  Each barrier expects the
+    // stage's weights and activations; the activations follow after the wait.
     if (lane == 0)
-        for (int i = 0; i < RD && i < total; ++i) issue_next(i);
+        for (int i = 0; i < RD && i < total; ++i) issue_w(i);
     pdl_wait();
     pdl_launch_dependents();
-
-    // Activation prefetch cursor two stages ahead (k-group kg0 + pkk, wrapping per group).
-    int pkk = 0;
-    uint4 x0[4][NT], x1[4][NT], x2[4][NT];
-    if (total > 0) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x0);
-    if (++pkk == nk) pkk = 0;
-    if (total > 1) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x1);
-    if (++pkk == nk) pkk = 0;
+    if (lane == 0)
+        for (int i = 0; i < RD && i < total; ++i)
+            tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);
 
     int sidx = 0, slot = 0;
     uint32_t phase = 0;
@@ -88,8 +93,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.0f;
         for (int kk = 0; kk < nk && !failed; ++kk, ++sidx) {
-            if (sidx + 2 < total) load_x_f16<NT>(a, gq, cq, kg0 + pkk, x2);
-            if (++pkk == nk) pkk = 0;
             const bool ok = mbar_wait_bounded(&bar[slot], phase);
             if (__any_sync(FULL_MASK, !ok)) {
                 // Give up: flag it, let every copy already issued land, stop computing.
@@ -99,17 +102,15 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1) mmvq_cta_ker
                 failed = true;
                 break;
             }
-            mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, x0, acc);
+            uint4 xv[4][NT];
+            lds_x_tile<NT>(xring + slot * NT * XTILE_BYTES, gq, cq, xv);
+            mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, xv, acc);
             __syncwarp();
-            if (lane == 0 && sidx + RD < total) issue_next(slot);
+            if (lane == 0 && sidx + RD < total) {
+                issue_w(slot);
+                tma_x_tile<NT>(xring + slot * NT * XTILE_BYTES, &xm, kg0 + (sidx + RD) % nk, &bar[slot]);
+            }
             if (++slot == RD) { slot = 0; phase ^= 1u; }
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    x0[kb][nt] = x1[kb][nt];
-                    x1[kb][nt] = x2[kb][nt];
-                }
         }
         // ---- the group's partials meet in shared memory (every warp takes part) ----
         if constexpr (PAIR) __syncthreads();  // every warp is done with the ring the partials lie over
@@ -168,7 +169,7 @@ static cudaError_t cta_attr() {
 }
 
 template <int NT, int EPI, bool PAIR>
-static cudaError_t cta_launch(const MmvqArgs& a, int grid, bool pdl, cudaStream_t s) {
+static cudaError_t cta_launch(const MmvqArgs& a, const CUtensorMap& xm, int grid, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(MMVQ_WARPS * 32);
@@ -179,7 +180,7 @@ static cudaError_t cta_launch(const MmvqArgs& a, int grid, bool pdl, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI, PAIR>, a);
+    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI, PAIR>, a, xm);
 }
 
 #define KD_CTA_CASES(X, NT_, PAIR_) \
@@ -204,12 +205,12 @@ int mmvq_cta_grid(int G, int B, int num_sms, bool* pair) {
     return *pair ? G : (G < num_sms ? G : num_sms);
 }
 
-cudaError_t launch_mmvq_cta(const MmvqArgs& a, int epi, int num_sms, bool pdl, cudaStream_t s) {
+cudaError_t launch_mmvq_cta(const MmvqArgs& a, const CUtensorMap& xm, int epi, int num_sms, bool pdl, cudaStream_t s) {
     const bool wide = a.B > 8;
     bool pair = false;
     const int grid = mmvq_cta_grid(a.G, a.B, num_sms, &pair);
 #define KD_L(NT_, EPI_, PAIR_) \
-    if (epi == EPI_ && (NT_ == 2) == wide && PAIR_ == pair) return cta_launch<NT_, EPI_, PAIR_>(a, grid, pdl, s);
+    if (epi == EPI_ && (NT_ == 2) == wide && PAIR_ == pair) return cta_launch<NT_, EPI_, PAIR_>(a, xm, grid, pdl, s);
     KD_CTA_CASES(KD_L, 1, false)
     KD_CTA_CASES(KD_L, 2, false)
     KD_CTA_CASES(KD_L, 1, true)

@@ -4,7 +4,8 @@
 // The matrix is a sequence of T = G * KG stages (one 128-column k-group of one
 // row group, contiguous in memory).  Warp w of W takes stages [w*T/W, (w+1)*T/W),
 // so every warp streams the same bytes (+-1 stage) as one contiguous range,
-// through its own ring of shared-memory stages filled by 1-D bulk copies.  A
+// through its own ring of shared-memory stages: a 1-D bulk copy of the stage's
+// weights and tensor-map copies of its activation tiles, on one barrier.  A
 // row group split between warps is finished by the last of them to arrive (one
 // atomic per warp and group, no waiting): it adds the fp32 partials in warp
 // order and runs the epilogue.  W depends on the shape and SM count, never on m.
@@ -59,14 +60,30 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
     }
 }
 
+// Shared memory: per warp a ring of RD stages, each the stage's weights and its
+// activation tiles.
+template <int NT>
+struct StreamSmem {
+    static constexpr int RD = NT == 1 ? RING : RING - 1;  // stages in flight per warp
+    static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * RD * NT * XTILE_BYTES;  // at a 1024-byte boundary
+    static constexpr size_t W_OFF = X_BYTES;
+    static constexpr size_t BAR_OFF = W_OFF + (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
+    static constexpr size_t TOTAL = BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) + 1024;  // + alignment slack
+};
+
 template <int NT, int EPI>
-__global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const MmvqArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
+    mmvq_stream_kernel(const MmvqArgs a, const __grid_constant__ CUtensorMap xm) {
+    using L = StreamSmem<NT>;
+    constexpr int RD = L::RD;
+    constexpr uint32_t SB = STAGE_BYTES + NT * XTILE_BYTES;  // bytes a stage's barrier waits for
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
-    uint8_t* ring = smem + (size_t)warp * RING * STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)MMVQ_WARPS * RING * STAGE_BYTES);
-    uint64_t* bar = bars + warp * RING;
+    uint8_t* xring = smem + (size_t)warp * RD * NT * XTILE_BYTES;
+    uint8_t* ring = smem + L::W_OFF + (size_t)warp * RD * STAGE_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
 
     const long T = (long)a.G * a.KG;
     const int w = blockIdx.x * MMVQ_WARPS + warp;
@@ -75,7 +92,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const M
     const int n = (int)(s_end - s_begin);
 
     if (lane == 0) {
-        for (int i = 0; i < RING; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < RD; ++i) mbar_init(&bar[i], 1);
         mbar_init_fence();
     }
     __syncwarp();
@@ -83,23 +100,23 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const M
     const uint64_t policy = l2_policy_evict_first();
     const uint8_t* wsrc = a.w + (size_t)s_begin * STAGE_BYTES;  // this warp's contiguous range
     // The weights do not depend on earlier kernels: start streaming them before
-    // waiting for the producer of the activations.
+    // waiting for the producer of the activations.  Each barrier expects the
+    // stage's weights and activations; the activations follow after the wait.
     if (lane == 0)
-        for (int i = 0; i < RING && i < n; ++i) {
-            mbar_arrive_expect_tx(&bar[i], STAGE_BYTES);
+        for (int i = 0; i < RD && i < n; ++i) {
+            mbar_arrive_expect_tx(&bar[i], SB);
             bulk_g2s_hint(ring + i * STAGE_BYTES, wsrc + (size_t)i * STAGE_BYTES, STAGE_BYTES, &bar[i], policy);
         }
     pdl_wait();
     pdl_launch_dependents();
 
-    // Compute cursor (g, kg) and an activation prefetch cursor two stages ahead.
     int g = (int)(s_begin / a.KG), kg = (int)(s_begin - (long)g * a.KG);
-    int pkg = kg;
-    uint4 x0[4][NT], x1[4][NT], x2[4][NT];
-    if (n > 0) load_x_f16<NT>(a, gq, cq, pkg, x0);
-    if (++pkg == a.KG) pkg = 0;
-    if (n > 1) load_x_f16<NT>(a, gq, cq, pkg, x1);
-    if (++pkg == a.KG) pkg = 0;
+    int xkg = kg;  // k-group of the next stage whose activations are requested (lane 0)
+    if (lane == 0)
+        for (int i = 0; i < RD && i < n; ++i) {
+            tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, xkg, &bar[i]);
+            if (++xkg == a.KG) xkg = 0;
+        }
 
     float acc[MT][NT][4];
 #pragma unroll
@@ -112,32 +129,26 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const M
     int slot = 0;
     uint32_t phase = 0;
     for (int i = 0; i < n; ++i) {
-        if (i + 2 < n) load_x_f16<NT>(a, gq, cq, pkg, x2);
-        if (++pkg == a.KG) pkg = 0;
-
         const bool ok = mbar_wait_bounded(&bar[slot], phase);
         if (__any_sync(FULL_MASK, !ok)) {
             // Give up: flag it, let every copy already issued land, stop computing.
             if (lane == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
-            for (int t = i; t < n && t < i + RING; ++t)
-                (void)mbar_wait_bounded(&bar[t % RING], (uint32_t)(t / RING) & 1u);
+            for (int t = i; t < n && t < i + RD; ++t)
+                (void)mbar_wait_bounded(&bar[t % RD], (uint32_t)(t / RD) & 1u);
             break;
         }
-        mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, x0, acc);
+        uint4 xv[4][NT];
+        lds_x_tile<NT>(xring + slot * NT * XTILE_BYTES, gq, cq, xv);
+        mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, xv, acc);
         __syncwarp();
-        if (lane == 0 && i + RING < n) {
-            mbar_arrive_expect_tx(&bar[slot], STAGE_BYTES);
-            bulk_g2s_hint(ring + slot * STAGE_BYTES, wsrc + (size_t)(i + RING) * STAGE_BYTES, STAGE_BYTES,
+        if (lane == 0 && i + RD < n) {
+            mbar_arrive_expect_tx(&bar[slot], SB);
+            bulk_g2s_hint(ring + slot * STAGE_BYTES, wsrc + (size_t)(i + RD) * STAGE_BYTES, STAGE_BYTES,
                           &bar[slot], policy);
+            tma_x_tile<NT>(xring + slot * NT * XTILE_BYTES, &xm, xkg, &bar[slot]);
+            if (++xkg == a.KG) xkg = 0;
         }
-        if (++slot == RING) { slot = 0; phase ^= 1u; }
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                x0[kb][nt] = x1[kb][nt];
-                x1[kb][nt] = x2[kb][nt];
-            }
+        if (++slot == RD) { slot = 0; phase ^= 1u; }
 
         const bool seg_end = (kg == a.KG - 1) || (i == n - 1);
         if (!seg_end) {
@@ -223,32 +234,28 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1) mmvq_stream_kernel(const M
     }
 }
 
-size_t mmvq_stream_smem_bytes() {
-    return (size_t)MMVQ_WARPS * RING * STAGE_BYTES + (size_t)MMVQ_WARPS * RING * sizeof(uint64_t);
-}
-
 template <int NT, int EPI>
 static cudaError_t stream_attr() {
-    cudaError_t e = cudaFuncSetAttribute(mmvq_stream_kernel<NT, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mmvq_stream_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(mmvq_stream_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)StreamSmem<NT>::TOTAL);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(mmvq_stream_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
 template <int NT, int EPI>
-static cudaError_t stream_launch(const MmvqArgs& a, bool pdl, cudaStream_t s) {
+static cudaError_t stream_launch(const MmvqArgs& a, const CUtensorMap& xm, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.W + MMVQ_WARPS - 1) / MMVQ_WARPS);
     cfg.blockDim = dim3(MMVQ_WARPS * 32);
-    cfg.dynamicSmemBytes = mmvq_stream_smem_bytes();
+    cfg.dynamicSmemBytes = StreamSmem<NT>::TOTAL;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mmvq_stream_kernel<NT, EPI>, a);
+    return cudaLaunchKernelEx(&cfg, mmvq_stream_kernel<NT, EPI>, a, xm);
 }
 
 #define KD_STREAM_CASES(X, NT_) X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID)
@@ -263,10 +270,10 @@ cudaError_t mmvq_stream_init_attributes() {
     return cudaSuccess;
 }
 
-cudaError_t launch_mmvq_stream(const MmvqArgs& a, int epi, bool pdl, cudaStream_t s) {
+cudaError_t launch_mmvq_stream(const MmvqArgs& a, const CUtensorMap& xm, int epi, bool pdl, cudaStream_t s) {
     const bool wide = a.B > 8;
 #define KD_L(NT_, EPI_) \
-    if (epi == EPI_ && (NT_ == 2) == wide) return stream_launch<NT_, EPI_>(a, pdl, s);
+    if (epi == EPI_ && (NT_ == 2) == wide) return stream_launch<NT_, EPI_>(a, xm, pdl, s);
     KD_STREAM_CASES(KD_L, 1)
     KD_STREAM_CASES(KD_L, 2)
 #undef KD_L
