@@ -126,16 +126,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def sources_digest(paths):
+    """First 16 hex digits of the sha256 of the listed files' bytes, concatenated in order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources are unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d[kernel]
-        src = os.path.join(ROOT, e["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return e["dram_bytes_per_launch"] if h == e["source_sha256_16"] else None
+        return e["dram_bytes_per_launch"] if sources_digest(e["sources"]) == e["sources_sha256_16"] else None
     except (OSError, ValueError, KeyError):
         return None
 
