@@ -393,6 +393,58 @@ def run_op_attn(args):
             "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4)}
 
 
+def run_op_long(args):
+    """The long-context multi-tenant workload: 8 sessions in 32768-position slots, pre-filled to
+    25704 + 1000 i (i = 0..7) fp16 positions, each step at its own position (64 positions cycling)."""
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    c = synth.LONG_CTX_8B_CASE
+    shape, S, cap, win = c["shape"], c["sessions"], c["capacity"], c["steps"]
+    lens = [c["prefill_base"] + c["prefill_stagger"] * i for i in range(S)]
+    w = synth.model_weights(shape, seed=c["seed"])
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=S, max_ctx=cap), w)
+    ids = []
+    for i, n in enumerate(lens):
+        k, v = synth.kv_prefill(shape, c["seed"], 1000 + i, n)
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, k, v, n)
+        torch.cuda.synchronize()
+        ids.append(sid)
+        del k, v
+    tok = synth.tokens(c["seed"], "bench-long", S, shape.vocab)
+    am = torch.empty(S, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def pos(i):
+        return np.array([n + (i % win) for n in lens], np.int32)
+
+    for i in range(max(3, args.warmup)):
+        kd.kd_decode_step(m, ids, tok, pos(i), None, am, st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    byts = 0
+    e0.record(st)
+    for i in range(args.steps):
+        p = pos(i)
+        kd.kd_decode_step(m, ids, tok, p, None, am, st)
+        byts += step_bytes(shape, p)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, kind = read_peaks()
+    status = kd.kd_device_status(m)
+    kd.kd_model_free(m)
+    return {"op": "long_context_step", "B": S, "capacity": cap, "positions": f"{lens[0]}..{lens[-1] + win - 1}",
+            "steps": args.steps, "ms_per_step": round(ms, 4), "tok_s": round(S / (ms / 1e3), 1),
+            "alg_bytes_per_step": int(byts / args.steps), "gbs": round(byts / args.steps / (ms / 1e3) / 1e9, 1),
+            "peak": peak, "peak_source": kind, "frac": round(byts / args.steps / (ms / 1e3) / 1e9 / peak, 4),
+            "device_status": status}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     """The oracle timed as it stands on the host cores, one layer of one session per step."""
@@ -443,14 +495,15 @@ def main():
     ap.add_argument("--impl", default="kd", choices=["kd", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["mmvq", "attn"], help="time one kernel family in isolation")
+    ap.add_argument("--op", choices=["mmvq", "attn", "long"],
+                    help="time one kernel family in isolation, or the long-context step")
     ap.add_argument("--rows", type=int, default=4096)
     ap.add_argument("--cols", type=int, default=14336)
     ap.add_argument("--m", type=int, default=8)
     ap.add_argument("--cap", type=int, default=32768)
     args = ap.parse_args()
     if args.op:
-        r = run_op_mmvq(args) if args.op == "mmvq" else run_op_attn(args)
+        r = {"mmvq": run_op_mmvq, "attn": run_op_attn, "long": run_op_long}[args.op](args)
         print(json.dumps(r), flush=True)
         return
     args.warmup = max(args.warmup, 3)
