@@ -6,9 +6,9 @@
  * session owns a slot of the fp16 KV arena and sits at its own position; every
  * weight matrix is streamed from HBM once per step for all B rows.  This is
  * the batched decode step of memra-engine's `decode_batch.rs` (module header:
- * "B sequences share one fused pass", the bandwidth thesis and the EXACTNESS
- * CONTRACT; `decode_step_batch`) restated for one GB300: one process, one
- * GPU, no collectives.
+ * several sequences go through one fused pass that reads the weights once, and
+ * each row's result must not depend on the batch; `decode_step_batch`)
+ * restated for one GB300: one process, one GPU, no collectives.
  *
  * Conventions for every function:
  *   - Returns KD_OK (0) or a negative kd_status.  Nothing aborts, nothing
@@ -47,9 +47,9 @@ enum {
     KD_ERR_DEVICE = -9         /* a kernel reported a device-side fault (bounded wait ran out) */
 };
 
-/* The widest batch with an exact kernel class: memra refuses B > 16 because no
- * per-row-exact kernel exists above it (decode_batch.rs, module header,
- * "B > 16 crosses into GEMM/dp4a-tail numeric configs ... refused"). */
+/* The widest batch with an exact kernel class: memra refuses B > 16 because
+ * above it its kernels change numeric configuration and rows are no longer
+ * exact (decode_batch.rs, module header). */
 #define KD_MAX_BATCH 16
 
 typedef void* kd_stream;          /* cudaStream_t */
@@ -109,7 +109,7 @@ kd_status kd_model_free(kd_model* m);
 
 /* Claim a free slot (lowest free id) for a new session of length 0.
  * Slot ownership per session follows memra's per-sequence `Cache` (its own
- * position and KV) and hf2q ADR-040's slot-indexed KV ("per-slot KV offset"). */
+ * position and KV) and hf2q ADR-040's KV indexed by slot. */
 kd_status kd_session_bind(kd_model* m, int32_t* session_id_out);
 
 /* Release a session's slot.  Waits on the host for the last step that used the
@@ -199,7 +199,7 @@ kd_status kd_q8_matrix_create(const void* q8_0_host, int32_t rows, int32_t cols,
 kd_status kd_q8_matrix_free(kd_q8_matrix* w);
 
 /* Weight-only Q8_0 matrix-vector product for m = 1..16 rows (memra's batched
- * verify-tier mmvq, "bit-identical per (token,row) to m=1"):
+ * verify-tier mmvq, whose rows must equal their m = 1 results bit for bit):
  *   y[r][o] = sum over blocks b of d[o][b] * sum_j q[o][b][j] * x[r][32b+j]
  * x: device fp16 [m][cols], 16-byte aligned; y: device fp32 [m][rows].  Row r of y is
  * bit-identical for every m.  Calls on one matrix must be stream-ordered
@@ -221,8 +221,8 @@ kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, voi
 /* Bytes of device workspace kd_attn_append_decode needs for these sizes. */
 size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap);
 
-/* KV append then ragged GQA split-K flash-decode (memra decode_batch_layers,
- * "phase A appends all B rows ... phase B attends all B sequences"):
+/* KV append then ragged GQA split-K flash-decode (memra decode_batch_layers:
+ * first every row's K/V is appended, then every sequence attends):
  *   for each row b: K[slot_b][h][pos_b] = fp16(k_new[b][h]), same for V; then
  *   out[b][qh] = fp16(sum_{t<=pos_b} softmax_t(q[b][qh] . K_t / sqrt(head_dim)) V_t)
  *   over KV head qh / (n_heads / n_kv_heads).

@@ -1,7 +1,7 @@
 // kd_attn.cu -- ragged GQA split-K flash-decode over slot-indexed fp16 KV.
 //
-// Phase B of memra-engine decode_batch.rs `decode_batch_layers` ("phase B attends
-// all B sequences (one blockIdx.z launch + one combine)") and hf2q ADR-040's
+// The attention phase of memra-engine decode_batch.rs `decode_batch_layers` (all
+// sequences in one launch, then one combine) and hf2q ADR-040's
 // batched flash-vec kernel (one dispatch for N queries, each with its own slot
 // and kv_seq_len), for B sessions of unrelated lengths.
 //

@@ -1,12 +1,12 @@
 // kd_mmvq.cu -- Q8_0 weight-only matrix x (m <= 16) activations: the device
 // weight layout (repack), the choice of schedule per matrix, and dispatch.
 //
-// This is the batched mmvq of memra-engine's decode_batch.rs (module header:
-// every projection at m = B reads the weights once for all B rows; each row is
-// "bit-identical per (token,row) to m=1").  Two schedules share one arithmetic
-// (kd_mmvq_common.cuh): "group" (kd_mmvq_cta.cu) when a matrix has at most about
-// two 32-row groups per SM, "stream" (kd_mmvq_stream.cu) otherwise.  The choice,
-// and every split of K, depends on the matrix shape and the SM count only.
+// This is the batched mmvq of memra-engine's decode_batch.rs (module header):
+// every projection at m = B reads the weights once for all B rows, and each row
+// is bit-identical to its m = 1 result.  Two schedules share one arithmetic
+// (kd_mmvq_common.cuh): "group" (kd_mmvq_cta.cu) when a matrix's 32-row groups
+// spread evenly over the SMs, "stream" (kd_mmvq_stream.cu) otherwise.  The
+// choice, and every split of K, depends on the matrix shape and the SM count only.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -22,8 +22,19 @@ cudaError_t launch_mmvq_stream(const MmvqArgs& a, const CUtensorMap& xm, int epi
 cudaError_t launch_mmvq_cta(const MmvqArgs& a, const CUtensorMap& xm, int epi, int num_sms, bool pdl, cudaStream_t s);
 
 
+// The group schedule keeps a row group's reduction in one CTA's shared memory;
+// it is used when the groups spread evenly over the SMs: at most two per SM
+// (one CTA per group), or up to eight per SM when the busiest SM has at most 5%
+// more groups than the average.  Otherwise the stream schedule balances stages.
+static int choose_mode(int G, int num_sms) {
+    if (G <= 2 * num_sms) return MMVQ_GROUP;
+    const long most = (long)((G + num_sms - 1) / num_sms) * num_sms;  // groups the busiest SM's share implies
+    if (G <= 8 * num_sms && most * 100 <= 105L * G) return MMVQ_GROUP;
+    return MMVQ_STREAM;
+}
+
 void plan_split(PackedQ8& m, int num_sms, int force_mode) {
-    m.mode = force_mode >= 0 ? force_mode : (m.G <= 2 * num_sms ? MMVQ_GROUP : MMVQ_STREAM);
+    m.mode = force_mode >= 0 ? force_mode : choose_mode(m.G, num_sms);
     // stream: W warps, each a contiguous run of the T = G * KG stages; W never
     // exceeds T, so every warp owns at least one stage.
     const long T = (long)m.G * m.KG;

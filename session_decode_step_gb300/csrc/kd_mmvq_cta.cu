@@ -1,5 +1,5 @@
-// kd_mmvq_cta.cu -- Q8_0 mmvq, "group" schedule: for matrices with about as
-// many 32-row groups as SMs (qkv, o-proj, down).
+// kd_mmvq_cta.cu -- Q8_0 mmvq, "group" schedule: for matrices whose 32-row
+// groups spread evenly over the SMs (q|k|v, o-proj, gate|up, down).
 //
 // CTA c owns row groups c, c + grid, ...; within a group its 8 warps split the
 // K range into 8 contiguous k-group ranges (fixed by the shape), each streamed

@@ -1,5 +1,5 @@
 // kd_mmvq_stream.cu -- Q8_0 mmvq, "stream" schedule: for matrices with many
-// more 32-row groups than SMs (gate|up, lm_head).
+// more 32-row groups than SMs that do not spread evenly over them (lm_head).
 //
 // The matrix is a sequence of T = G * KG stages (one 128-column k-group of one
 // row group, contiguous in memory).  Warp w of W takes stages [w*T/W, (w+1)*T/W),

@@ -1,10 +1,10 @@
 // kd_rowops.cu -- the row-parallel operations of the decode step: embedding
-// gather (with the row's sum of squares for the first fused RMSNorm) and the
-// greedy argmax.  RMSNorm itself is fused into the projections' activation load.
+// gather with the first RMSNorm, the RMSNorm between a residual writer and the
+// next projection, and the greedy argmax.
 //
-// memra-engine decode_batch.rs: "Row-parallel ops (norm/rope/quantize/activation)
-// batch trivially -- they are the SAME kernels prefill already runs at T rows";
-// one CTA per row, so row b's bytes never depend on B.
+// memra-engine decode_batch.rs treats the row-parallel ops as the same kernels
+// run at B rows; here every row's arithmetic is its own, so row b's bytes never
+// depend on B.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
