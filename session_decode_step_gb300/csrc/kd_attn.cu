@@ -133,11 +133,12 @@ __device__ __forceinline__ bool wait_value(const volatile int* p, int v) {
 // refills that stage with item k + STAGES.  A consumer first waits until the
 // stage's item word says k (the copy of item k was issued, so the stage's
 // barrier is in item k's phase), then for the barrier.  The scores S = Q K^T
-// and the output O = P V are m16n8k16 tensor-core products: the A rows are the
-// group's heads, rows [0, GQ) with q (then p) rounded to fp16 and rows
-// [GQ, 2 GQ) with the remainder of that rounding (GQ = 8: rows g and g + 8), so
-// their sum is the fp32-accurate product; K tiles are the B operand of S as
-// stored, V tiles that of O through the transposing ldmatrix.
+// and the output O = P V are m16n8k16 tensor-core products taken transposed
+// (S^T = K Q^T, O^T = V^T P^T): the 16 MMA rows are keys, then head dims, with
+// no padding; the 8 columns are the GQA group's heads, each as q (then p)
+// rounded to fp16 and the remainder of that rounding, whose two products add
+// up to the fp32-accurate one.  K tiles are the A operand as stored, V tiles
+// through the transposing ldmatrix.
 template <int HD, int GQ>
 __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     attn_split_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -155,10 +156,6 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     volatile int* stage_item = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
     volatile int* cta_failed = stage_item + S;
-    // Rows of the A operand this lane supplies: head qh rounded (hi) or its remainder (lo).
-    const int qh = GQ == 8 ? g : (g < 2 * GQ ? g % GQ : -1);
-    const bool lo_row = GQ < 8 && g >= GQ;
-    constexpr int PARTNER = GQ < 8 ? 4 * GQ : 0;  // lane xor that holds the other half of a row pair
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -219,15 +216,27 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             if (lane == 0) issue(it, k);
         }
 
-    // q of the lane's head, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
-    float2 qv[KS][2];
+    // The MMAs' 8-wide N dimension: column 2h + part of N-tile j is head 4j + h,
+    // part 0 carrying q (then p) rounded to fp16 and part 1 the remainder of that
+    // rounding.  Lane (g, c) supplies column g (head 4j + g/2, part g & 1) of the
+    // B fragments and holds columns 2c, 2c + 1 (both parts of head 4j + c) of
+    // the results, so the two parts add up in the lane.
+    constexpr int NQ = GQ > 4 ? GQ / 4 : 1;  // N-tiles of heads
+    const int colh = g >> 1;
+    const bool col_lo = (g & 1) != 0;
+    // q of the lane's column head, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
+    float2 qv[NQ][KS][2];
     auto load_q = [&](const AttnItem& it) {
-        if (qh >= 0) {
-            const float* qp = a.q + ((size_t)it.b * a.nh + (size_t)it.kvh * GQ + qh) * HD + 2 * c;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                qv[ks][0] = *reinterpret_cast<const float2*>(qp + 16 * ks);
-                qv[ks][1] = *reinterpret_cast<const float2*>(qp + 16 * ks + 8);
+        for (int j = 0; j < NQ; ++j) {
+            const int h = 4 * j + colh;
+            if (h < GQ) {
+                const float* qp = a.q + ((size_t)it.b * a.nh + (size_t)it.kvh * GQ + h) * HD + 2 * c;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    qv[j][ks][0] = *reinterpret_cast<const float2*>(qp + 16 * ks);
+                    qv[j][ks][1] = *reinterpret_cast<const float2*>(qp + 16 * ks + 8);
+                }
             }
         }
     };
@@ -239,20 +248,15 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
         uint8_t* stg = smem + st * L::STAGE;
         const uint32_t kbase = smem_u32(stg), vbase = kbase + L::K_BYTES;
 
-        uint32_t qa[KS][4];
+        uint32_t qb[NQ][KS][2];  // B fragments of Q^T
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const float2 u = qv[ks][0], w = qv[ks][1];
-            if constexpr (GQ == 8) {
-                qa[ks][0] = f2_hi(u.x, u.y);
-                qa[ks][1] = f2_lo(u.x, u.y);
-                qa[ks][2] = f2_hi(w.x, w.y);
-                qa[ks][3] = f2_lo(w.x, w.y);
-            } else {
-                qa[ks][0] = qh < 0 ? 0u : (lo_row ? f2_lo(u.x, u.y) : f2_hi(u.x, u.y));
-                qa[ks][2] = qh < 0 ? 0u : (lo_row ? f2_lo(w.x, w.y) : f2_hi(w.x, w.y));
-                qa[ks][1] = 0u;
-                qa[ks][3] = 0u;
+        for (int j = 0; j < NQ; ++j) {
+            const bool on = 4 * j + colh < GQ;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const float2 u = qv[j][ks][0], w = qv[j][ks][1];
+                qb[j][ks][0] = !on ? 0u : (col_lo ? f2_lo(u.x, u.y) : f2_hi(u.x, u.y));
+                qb[j][ks][1] = !on ? 0u : (col_lo ? f2_lo(w.x, w.y) : f2_hi(w.x, w.y));
             }
         }
         if (k + AT_WARPS < nk) load_q(tab.item(a, lane, gitem(k + AT_WARPS)));  // lands during this item
@@ -279,116 +283,113 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             __syncwarp();
         }
 
-        // ---- S = Q K^T over the 8 key tiles.  k-steps outside, tiles inside: the
-        // MMAs issued back to back go to 8 different accumulators (each tile still
-        // adds its k-steps in order).
-        float sacc[8][4];
+        // ---- S^T = K Q^T: M = 16 keys (4 tiles), N = the head columns, K = 16 dims.
+        // k-steps outside, key tiles inside: MMAs issued back to back go to
+        // different accumulators; each tile adds its k-steps in order.
+        float sacc[4][NQ][4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sacc[t][i] = 0.0f;
+            for (int j = 0; j < NQ; ++j)
 #pragma unroll
-        for (int kp = 0; kp < KS / 2; ++kp) {
-            uint32_t kb[8][4];
+                for (int i = 0; i < 4; ++i) sacc[m][j][i] = 0.0f;
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-                ldsm_x4(kbase + L::off(8 * t + (lane & 7), 4 * kp + (lane >> 3)), kb[t][0], kb[t][1], kb[t][2],
-                        kb[t][3]);
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t ka[4][4];
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-                mma_16816_acc(sacc[t], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], kb[t][0], kb[t][1]);
+            for (int m = 0; m < 4; ++m)
+                ldsm_x4(kbase + L::off(16 * m + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * ks + (lane >> 4)), ka[m][0],
+                        ka[m][1], ka[m][2], ka[m][3]);
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-                mma_16816_acc(sacc[t], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3],
-                              kb[t][2], kb[t][3]);
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    mma_16816_acc(sacc[m][j], ka[m][0], ka[m][1], ka[m][2], ka[m][3], qb[j][ks][0], qb[j][ks][1]);
         }
-        // ---- row pair sum, scale, mask, softmax over the item's keys (4 lanes per row)
-        float sv[8][2];
-        float m = -INFINITY;
+        // ---- per head 4j + c: scores of keys 16m + g (e = 0) and 16m + g + 8 (e = 1);
+        // scale, mask, softmax over the item's keys (the 8 lanes g of a head)
+        float sv[NQ][4][2], mx[NQ], lsum[NQ];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+        for (int j = 0; j < NQ; ++j) {
+            mx[j] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float s;
-                if constexpr (GQ == 8) {
-                    s = __fadd_rn(sacc[t][e], sacc[t][2 + e]);
-                } else {
-                    const float o = __shfl_xor_sync(FULL_MASK, sacc[t][e], PARTNER);
-                    s = lo_row ? __fadd_rn(o, sacc[t][e]) : __fadd_rn(sacc[t][e], o);
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float sc = __fadd_rn(sacc[m][j][2 * e], sacc[m][j][2 * e + 1]);  // both parts
+                    const int key = 16 * m + g + 8 * e;
+                    sv[j][m][e] = key < n ? __fmul_rn(sc, a.scale) : -INFINITY;
+                    mx[j] = fmaxf(mx[j], sv[j][m][e]);
                 }
-                const int key = 8 * t + 2 * c + e;
-                sv[t][e] = key < n ? __fmul_rn(s, a.scale) : -INFINITY;
-                m = fmaxf(m, sv[t][e]);
-            }
-        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 2));
-        float l = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
+            for (int o = 4; o < 32; o <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL_MASK, mx[j], o));
+            lsum[j] = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = 8 * t + 2 * c + e;
-                sv[t][e] = key < n ? expf(__fsub_rn(sv[t][e], m)) : 0.0f;
-                l = __fadd_rn(l, sv[t][e]);
-            }
-        l = __fadd_rn(l, __shfl_xor_sync(FULL_MASK, l, 1));
-        l = __fadd_rn(l, __shfl_xor_sync(FULL_MASK, l, 2));
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = 16 * m + g + 8 * e;
+                    sv[j][m][e] = key < n ? expf(__fsub_rn(sv[j][m][e], mx[j])) : 0.0f;
+                    lsum[j] = __fadd_rn(lsum[j], sv[j][m][e]);
+                }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) lsum[j] = __fadd_rn(lsum[j], __shfl_xor_sync(FULL_MASK, lsum[j], o));
+        }
 
-        // ---- O = P V over the 16-key steps that hold keys
-        float oacc[NU][4];
+        // ---- O^T = V^T P^T: M = 16 dims (NU/2 tiles), N = the head columns, K = 16 keys,
+        // over the key steps that hold keys.  P^T's B fragment of lane (g, c) wants
+        // keys 2c, 2c + 1 (and + 8) of its column head: they sit in lanes
+        // (2c, g/2) and (2c + 1, g/2).
+        float oacc[NU / 2][NQ][4];
 #pragma unroll
-        for (int u = 0; u < NU; ++u)
+        for (int mt = 0; mt < NU / 2; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) oacc[u][i] = 0.0f;
+            for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) oacc[mt][j][i] = 0.0f;
         const int nsteps = (n + 15) >> 4;
+        const int src0 = (2 * c) * 4 + colh, src1 = src0 + 4;
 #pragma unroll
         for (int js = 0; js < 4; ++js) {
             if (js < nsteps) {
-                const float* p0 = sv[2 * js];
-                const float* p1 = sv[2 * js + 1];
-                uint32_t pa0, pa1, pa2, pa3;
-                if constexpr (GQ == 8) {
-                    pa0 = f2_hi(p0[0], p0[1]);
-                    pa1 = f2_lo(p0[0], p0[1]);
-                    pa2 = f2_hi(p1[0], p1[1]);
-                    pa3 = f2_lo(p1[0], p1[1]);
-                } else {
-                    pa0 = qh < 0 ? 0u : (lo_row ? f2_lo(p0[0], p0[1]) : f2_hi(p0[0], p0[1]));
-                    pa2 = qh < 0 ? 0u : (lo_row ? f2_lo(p1[0], p1[1]) : f2_hi(p1[0], p1[1]));
-                    pa1 = 0u;
-                    pa3 = 0u;
-                }
-                uint32_t vb[NU / 2][4];
+                uint32_t pb[NQ][2];
 #pragma unroll
-                for (int up = 0; up < NU / 2; ++up) {
-                    const int i = lane >> 3;
-                    ldsm_x4_trans(vbase + L::off(16 * js + 8 * (i & 1) + (lane & 7), 2 * up + (i >> 1)), vb[up][0],
-                                  vb[up][1], vb[up][2], vb[up][3]);
+                for (int j = 0; j < NQ; ++j) {
+                    const float v00 = __shfl_sync(FULL_MASK, sv[j][js][0], src0);
+                    const float v01 = __shfl_sync(FULL_MASK, sv[j][js][0], src1);
+                    const float v10 = __shfl_sync(FULL_MASK, sv[j][js][1], src0);
+                    const float v11 = __shfl_sync(FULL_MASK, sv[j][js][1], src1);
+                    const bool on = 4 * j + colh < GQ;
+                    pb[j][0] = !on ? 0u : (col_lo ? f2_lo(v00, v01) : f2_hi(v00, v01));
+                    pb[j][1] = !on ? 0u : (col_lo ? f2_lo(v10, v11) : f2_hi(v10, v11));
                 }
+                uint32_t va[NU / 2][4];
 #pragma unroll
-                for (int up = 0; up < NU / 2; ++up) {
-                    mma_16816_acc(oacc[2 * up], pa0, pa1, pa2, pa3, vb[up][0], vb[up][1]);
-                    mma_16816_acc(oacc[2 * up + 1], pa0, pa1, pa2, pa3, vb[up][2], vb[up][3]);
-                }
+                for (int mt = 0; mt < NU / 2; ++mt)
+                    ldsm_x4_trans(vbase + L::off(16 * js + (lane >> 4) * 8 + (lane & 7), 2 * mt + ((lane >> 3) & 1)),
+                                  va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+#pragma unroll
+                for (int j = 0; j < NQ; ++j)
+#pragma unroll
+                    for (int mt = 0; mt < NU / 2; ++mt)
+                        mma_16816_acc(oacc[mt][j], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pb[j][0], pb[j][1]);
             }
         }
-        // ---- row pair sum; lanes holding a head's rounded row write (o, m, l)
-        float* dst = a.part + (((size_t)it.b * a.nh + (size_t)it.kvh * GQ + (qh < 0 ? 0 : qh)) * a.max_splits + it.s) *
-                                  ATT_REC(HD);
-        const bool writer = qh >= 0 && !lo_row;
+        // ---- both parts of head 4j + c, dims 16 mt + g and 16 mt + g + 8: write (o, m, l)
 #pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            float o0, o1;
-            if constexpr (GQ == 8) {
-                o0 = __fadd_rn(oacc[u][0], oacc[u][2]);
-                o1 = __fadd_rn(oacc[u][1], oacc[u][3]);
-            } else {
-                o0 = __fadd_rn(oacc[u][0], __shfl_xor_sync(FULL_MASK, oacc[u][0], PARTNER));
-                o1 = __fadd_rn(oacc[u][1], __shfl_xor_sync(FULL_MASK, oacc[u][1], PARTNER));
+        for (int j = 0; j < NQ; ++j) {
+            const int h = 4 * j + c;
+            if (h < GQ) {
+                float* dst = a.part + (((size_t)it.b * a.nh + (size_t)it.kvh * GQ + h) * a.max_splits + it.s) *
+                                          ATT_REC(HD);
+#pragma unroll
+                for (int mt = 0; mt < NU / 2; ++mt) {
+                    dst[16 * mt + g] = __fadd_rn(oacc[mt][j][0], oacc[mt][j][1]);
+                    dst[16 * mt + g + 8] = __fadd_rn(oacc[mt][j][2], oacc[mt][j][3]);
+                }
+                if (g == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(mx[j], lsum[j]);
             }
-            if (writer) *reinterpret_cast<float2*>(dst + 8 * u + 2 * c) = make_float2(o0, o1);
         }
-        if (writer && c == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(m, l);
 
         __syncwarp();  // the stage is consumed: refill it
         if (k + S < nk) {
