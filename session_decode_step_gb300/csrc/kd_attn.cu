@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
 // order), the numerator a sum over the splits in order.  Both orders depend on
 // the split count only.
 constexpr int COMB_MAX_SPLITS = ATT_MAX_SPLITS;
-constexpr int COMB_BATCH = 16;
+constexpr int COMB_BATCH = 32;
 
 template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {

@@ -20,7 +20,7 @@ namespace kd {
 // activation tiles; then the barriers and the partial-sum buffer.
 template <int NT, bool PAIR>
 struct CtaSmem {
-    static constexpr int RD = PAIR ? 2 : (NT == 1 ? RING : RING - 1);  // stages in flight per warp
+    static constexpr int RD = PAIR ? 2 : 3;  // stages in flight per warp (measured best for the step)
     static constexpr int RS = NT == 1 ? 9 : 16;  // partial-row stride (floats), padded against bank conflicts
     static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * RD * NT * XTILE_BYTES;  // at a 1024-byte boundary
     static constexpr size_t W_OFF = X_BYTES;
