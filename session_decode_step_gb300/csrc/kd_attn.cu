@@ -208,8 +208,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             early |= 1u << i;
         }
     }
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS)
         if (!((early >> i) & 1u)) {
             const AttnItem it = tab.item(a, lane, gitem(k));
@@ -424,8 +424,8 @@ template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __shared__ float wts[COMB_MAX_SPLITS], ls[COMB_MAX_SPLITS];
     __shared__ float red_m[HD / 32], red_l[HD / 32];
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     if (b >= a.B) return;
     const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;

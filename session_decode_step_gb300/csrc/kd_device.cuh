@@ -117,6 +117,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 // A no-op when the kernel was launched without the PDL attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Let the next kernel in the stream start launching (its pre-wait prologue).
+// Issued before this kernel's own wait: the dependent grid is only scheduled
+// once every CTA of this grid is resident, and its griddepcontrol.wait still
+// waits for this grid to complete, so the order of work is unchanged while the
+// dependent's weight prefetch can start on SMs this grid leaves free.
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

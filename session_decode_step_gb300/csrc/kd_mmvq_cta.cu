@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     // stage's weights and activations; the activations follow after the wait.
     if (lane == 0)
         for (int i = 0; i < RD && i < total; ++i) issue_w(i);
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     if (lane == 0)
         for (int i = 0; i < RD && i < total; ++i)
             tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);

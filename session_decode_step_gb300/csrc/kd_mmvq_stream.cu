@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
             mbar_arrive_expect_tx(&bar[i], SB);
             bulk_g2s_hint(ring + i * STAGE_BYTES, wsrc + (size_t)i * STAGE_BYTES, STAGE_BYTES, &bar[i], policy);
         }
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
 
     int g = (int)(s_begin / a.KG), kg = (int)(s_begin - (long)g * a.KG);
     int xkg = kg;  // k-group of the next stage whose activations are requested (lane 0)

@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
                                                               const int* __restrict__ token, int H,
                                                               float* __restrict__ x, const float* __restrict__ w,
                                                               float eps, __half* __restrict__ xn) {
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     const int b = blockIdx.x, tid = threadIdx.x;
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
     float* xr = x + (size_t)b * H;
@@ -117,8 +117,8 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float
                                                                      const float* __restrict__ w, float eps,
                                                                      __half* __restrict__ xn) {
     __shared__ float rsh;
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     const int b = blockIdx.y, tid = threadIdx.x;
     const int i = blockIdx.x * NORM_COLS + tid * 4;
     const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __r
                                                                 int* __restrict__ out) {
     __shared__ unsigned long long wbest[ARGMAX_THREADS / 32];
     __shared__ bool last;
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
-    pdl_launch_dependents();
     const int b = blockIdx.y, tid = threadIdx.x;
     const float* row = logits + (size_t)b * V;
     const int i0 = blockIdx.x * ARGMAX_CHUNK + tid * 4;
