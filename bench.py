@@ -56,6 +56,7 @@ def step_bytes(s, positions):
 
 def kernels_per_step(s, with_argmax=True):
     # embed; per layer qkv, attention split, combine, o-proj, norm, gate|up, down, norm; lm_head; argmax
+    # (the most a step launches; bench.py reports the count the library's profile saw)
     return 1 + s.n_layers * 8 + 1 + (1 if with_argmax else 0)
 
 
@@ -273,6 +274,7 @@ def run_kd(args, rank, world):
                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(ach / peak, 4),
                     "traffic": traffic_for(dominant), "alg_bytes_per_launch": int(alg),
                     "avg_launch_us": round(avg_s * 1e6, 2)}
+    launches_per_step = sum(v[0] for v in prof.values()) / n_prof
     kernel_share = {k: {"launches": v[0], "ms": round(v[1], 3),
                         "share": round(v[1] / max(1e-9, sum(x[1] for x in prof.values())), 4)}
                     for k, v in prof.items()}
@@ -292,7 +294,8 @@ def run_kd(args, rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, w, B)
     return dict(value=tok_s, ms=ms, gbs=gbs, e2e=e2e, roofline=roofline, sweep=sweep, cpu=cpu,
-                clocks=clk.summary(), peak=peak, peak_kind=peak_kind, status=status, shares=kernel_share)
+                clocks=clk.summary(), peak=peak, peak_kind=peak_kind, status=status, shares=kernel_share,
+                launches_per_step=launches_per_step)
 
 
 def cpu_baseline(shape, w, B):
@@ -537,7 +540,7 @@ def main():
             "peak_hbm_gbs": r["peak"], "peak_source": r["peak_kind"],
             "e2e": r["e2e"], "roofline": r["roofline"], "batch_sweep": r["sweep"],
             "cpu_baseline": r["cpu"], "clocks": r["clocks"],
-            "gpu_launches": kernels_per_step(shape) * args.steps,
+            "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
             "kernel_time_share": r["shares"], "device_status": r["status"],
         }
         print(json.dumps(out), flush=True)
