@@ -21,7 +21,7 @@ constexpr int NORM_SLOTS = MAX_NORM_SLOTS;
 // One stage (one 128-column k-group of a 32-row group) into the accumulators.
 // x: this lane's activation fragments for the stage's 4 blocks (k permutation
 // of the packed layout); acc[mt][nt][i]: row mt*16 + gq (+8 for i >= 2),
-// session nt*8 + 2*cq + (i & 1).
+// MMA column nt*8 + 2*cq + (i & 1), i.e. session nt*8 + col_session(2*cq + (i & 1)).
 template <int NT>
 __device__ __forceinline__ void mma_stage(const uint8_t* st, int lane, int gq, const uint4 (&x)[4][NT],
                                           float (&acc)[MT][NT][4]) {
@@ -70,15 +70,23 @@ __device__ __forceinline__ void tma_x_tile(uint8_t* xt, const void* xmap, int kg
         for (int h = 0; h < 2; ++h) tma_load_2d(xt + (nt * 2 + h) * 1024, xmap, kg * KGROUP + 64 * h, 8 * nt, bar);
 }
 
-// Lane (gq, cq) multiplies session n = gq + 8*nt at columns 8cq .. 8cq+7 of each
-// 32-column block kb: the 16-byte chunk 4kb + cq of row gq.
+// MMA column c (0..7) of an 8-session tile carries session col_session(c):
+// the lanes of one shared-memory wavefront (gq = 2w, 2w + 1) then read tile
+// rows w and w + 4, whose swizzled chunks fall in different bank halves.
+// Which column holds a session changes nothing in its arithmetic.
+__device__ __forceinline__ int col_session(int c) { return (c >> 1) | ((c & 1) << 2); }
+__device__ __forceinline__ int session_col(int s) { return ((s & 3) << 1) | (s >> 2); }
+
+// Lane (gq, cq) multiplies session 8*nt + col_session(gq) at columns 8cq .. 8cq+7
+// of each 32-column block kb: the 16-byte chunk 4kb + cq of that session's row.
 template <int NT>
 __device__ __forceinline__ void lds_x_tile(const uint8_t* xt, int gq, int cq, uint4 (&xv)[4][NT]) {
+    const int row = col_session(gq);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb)
-            xv[kb][nt] = lds_v4(xt + (nt * 2 + (kb >> 1)) * 1024 + gq * 128 + ((((kb & 1) * 4 + cq) ^ gq) << 4));
+            xv[kb][nt] = lds_v4(xt + (nt * 2 + (kb >> 1)) * 1024 + row * 128 + ((((kb & 1) * 4 + cq) ^ row) << 4));
 }
 
 // ---- epilogues on single outputs ------------------------------------------

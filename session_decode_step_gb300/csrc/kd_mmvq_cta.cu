@@ -126,10 +126,11 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
                 rw[(r0 + 8) * L::RS + c0 + 1] = acc[mt][nt][3];
             }
         __syncthreads();
-        auto sum_rows = [&](int row, int n) {  // warps 0..7 in order
-            float v = red[row * L::RS + n];
+        auto sum_rows = [&](int row, int n) {  // session n's column, warps 0..7 in order
+            const int col = (n & ~7) | session_col(n & 7);
+            float v = red[row * L::RS + col];
 #pragma unroll
-            for (int w = 1; w < MMVQ_WARPS; ++w) v = __fadd_rn(v, red[((size_t)w * GROUP_ROWS + row) * L::RS + n]);
+            for (int w = 1; w < MMVQ_WARPS; ++w) v = __fadd_rn(v, red[((size_t)w * GROUP_ROWS + row) * L::RS + col]);
             return v;
         };
         if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {

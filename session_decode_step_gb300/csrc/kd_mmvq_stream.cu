@@ -28,7 +28,7 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int n = nt * 8 + 2 * cq + (i & 1);
+            const int n = nt * 8 + col_session(2 * cq + (i & 1));
             if (n >= a.B) continue;
             const int r = gq + ((i >> 1) << 3);  // row within a 16-row tile
             if constexpr (EPI == EPI_STORE) {
@@ -54,7 +54,7 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
                 s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 4));
                 s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 8));
                 s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 16));
-                const int n = nt * 8 + 2 * cq + j;
+                const int n = nt * 8 + col_session(2 * cq + j);
                 if (gq == 0 && n < a.B) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
             }
     }
