@@ -101,6 +101,15 @@ __device__ __forceinline__ float epi_resid(const MmvqArgs& a, int g, int r, int 
     *p = x;
     return x;
 }
+// The same with the old value loaded ahead of time (resid_load).
+__device__ __forceinline__ float resid_load(const MmvqArgs& a, int g, int r, int n) {
+    return a.y[(size_t)n * a.ld + (size_t)g * GROUP_ROWS + r];
+}
+__device__ __forceinline__ float epi_resid_apply(const MmvqArgs& a, int g, int r, int n, float old, float v) {
+    const float x = __fadd_rn(old, v);
+    a.y[(size_t)n * a.ld + (size_t)g * GROUP_ROWS + r] = x;
+    return x;
+}
 // Pair epilogues: tile 0 row r with tile 1 row r (r = 0..15).
 //   SwiGLU: act = fp16(silu(gate) * up)
 __device__ __forceinline__ void epi_swiglu(const MmvqArgs& a, int g, int r, int n, float gt, float up) {
@@ -109,14 +118,30 @@ __device__ __forceinline__ void epi_swiglu(const MmvqArgs& a, int g, int r, int 
 }
 //   QKV: dims (i, i + hd/2) of one head; RoPE at the row's position for q and k;
 //   q to fp32, k and v appended to the session's slot at its position as fp16.
-__device__ __forceinline__ void epi_qkv(const MmvqArgs& a, int g, int r, int n, float x0, float x1) {
+//   What it reads from global memory (the position, the slot, the cos/sin pair)
+//   can be loaded ahead of time (qkv_load).
+struct QkvIn {
+    int p, slot;
+    float2 cs;
+};
+__device__ __forceinline__ QkvIn qkv_load(const MmvqArgs& a, int g, int r, int n) {
+    const int per_head = a.hd / GROUP_ROWS;
+    const int head = g / per_head;
+    const int dim = (g - head * per_head) * TILE_ROWS + r;
+    QkvIn in;
+    in.p = a.pos[n];
+    in.slot = a.slot[n];
+    in.cs = head < a.nh + a.nkv ? a.rope[(size_t)in.p * (a.hd >> 1) + dim] : make_float2(0.0f, 0.0f);
+    return in;
+}
+__device__ __forceinline__ void epi_qkv_in(const MmvqArgs& a, int g, int r, int n, float x0, float x1, const QkvIn& in) {
     const int per_head = a.hd / GROUP_ROWS;
     const int head = g / per_head;
     const int dim = (g - head * per_head) * TILE_ROWS + r;
     const int half = a.hd >> 1;
-    const int p = a.pos[n];
+    const int p = in.p;
     if (head < a.nh + a.nkv) {
-        const float2 cs = a.rope[(size_t)p * half + dim];
+        const float2 cs = in.cs;
         const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
         const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
         if (head < a.nh) {
@@ -124,15 +149,18 @@ __device__ __forceinline__ void epi_qkv(const MmvqArgs& a, int g, int r, int n, 
             q[dim] = y0;
             q[dim + half] = y1;
         } else {
-            __half* k = a.kc + (((size_t)a.slot[n] * a.nkv + (head - a.nh)) * a.cap + p) * a.hd;
+            __half* k = a.kc + (((size_t)in.slot * a.nkv + (head - a.nh)) * a.cap + p) * a.hd;
             k[dim] = __float2half_rn(y0);
             k[dim + half] = __float2half_rn(y1);
         }
     } else {
-        __half* vv = a.vc + (((size_t)a.slot[n] * a.nkv + (head - a.nh - a.nkv)) * a.cap + p) * a.hd;
+        __half* vv = a.vc + (((size_t)in.slot * a.nkv + (head - a.nh - a.nkv)) * a.cap + p) * a.hd;
         vv[dim] = __float2half_rn(x0);
         vv[dim + half] = __float2half_rn(x1);
     }
+}
+__device__ __forceinline__ void epi_qkv(const MmvqArgs& a, int g, int r, int n, float x0, float x1) {
+    epi_qkv_in(a, g, r, n, x0, x1, qkv_load(a, g, r, n));
 }
 
 }  // namespace kd

@@ -85,6 +85,20 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     bool failed = false;
     for (int gi = 0; gi < ngrp; ++gi) {
         const int g = blockIdx.x + gi * gridDim.x;
+        // What the epilogue reads from global memory, loaded now so the group's end
+        // does not wait for it: the residual rows (thread (warp, lane) takes session
+        // warp + 8j, row lane) or the q|k|v epilogue's positions and cos/sin pairs.
+        float xold[NT];
+        QkvIn qin{};
+        if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int n = warp + MMVQ_WARPS * j;
+                xold[j] = n < a.B ? resid_load(a, g, lane, n) : 0.0f;
+            }
+        } else if constexpr (EPI == EPI_QKV) {
+            if (tid < a.B * TILE_ROWS) qin = qkv_load(a, g, tid & 15, tid >> 4);
+        }
         float acc[MT][NT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -139,7 +153,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
                 if constexpr (EPI == EPI_STORE) {
                     epi_store(a, g, lane, n, v);
                 } else {
-                    const float x = epi_resid(a, g, lane, n, v);
+                    const float x = epi_resid_apply(a, g, lane, n, n >= MMVQ_WARPS ? xold[NT - 1] : xold[0], v);
                     float s = __fmul_rn(x, x);
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
@@ -153,7 +167,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
                 if constexpr (EPI == EPI_SWIGLU)
                     epi_swiglu(a, g, rr, n, v0, v1);
                 else
-                    epi_qkv(a, g, rr, n, v0, v1);
+                    epi_qkv_in(a, g, rr, n, v0, v1, e == tid ? qin : qkv_load(a, g, rr, n));
             }
         }
         __syncthreads();  // the partial buffer is reused by the next group
