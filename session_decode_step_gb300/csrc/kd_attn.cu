@@ -27,7 +27,8 @@ namespace kd {
 
 constexpr int AT_C = ATT_CHUNK;  // keys per work item (split)
 constexpr int AT_WARPS = 8;      // consumer warps per CTA (two per SM sub-partition)
-static_assert(AT_C == 64, "a work item is 8 key tiles of 8 and 4 key steps of 16");
+constexpr int AT_KT = AT_C / 16;  // 16-key tiles (and 16-key steps) of a work item
+static_assert(AT_C % 16 == 0 && AT_C <= 64, "a work item is whole 16-key tiles, at most 4");
 
 // Shared memory of one CTA: a ring of STAGES stages shared by its warps.  A
 // stage holds one work item: its K tile, then its V tile, each as 64-dim halves
@@ -38,7 +39,7 @@ static_assert(AT_C == 64, "a work item is 8 key tiles of 8 and 4 key steps of 16
 template <int HD>
 struct AttnSmem {
     static constexpr int NREG = HD / 64;                    // 64-dim halves of a row
-    static constexpr int HALF_BYTES = AT_C * 128;           // one half of a 64-key tile
+    static constexpr int HALF_BYTES = AT_C * 128;           // one half of a work item's tile
     static constexpr int K_BYTES = NREG * HALF_BYTES;
     static constexpr int STAGE = 2 * K_BYTES;               // K tile, V tile
     static constexpr int STAGES = 192 * 1024 / STAGE;       // 6 at hd 128, 12 at hd 64
@@ -283,37 +284,37 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             __syncwarp();
         }
 
-        // ---- S^T = K Q^T: M = 16 keys (4 tiles), N = the head columns, K = 16 dims.
+        // ---- S^T = K Q^T: M = 16 keys (AT_KT tiles), N = the head columns, K = 16 dims.
         // k-steps outside, key tiles inside: MMAs issued back to back go to
         // different accumulators; each tile adds its k-steps in order.
-        float sacc[4][NQ][4];
+        float sacc[AT_KT][NQ][4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < AT_KT; ++m)
 #pragma unroll
             for (int j = 0; j < NQ; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sacc[m][j][i] = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            uint32_t ka[4][4];
+            uint32_t ka[AT_KT][4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < AT_KT; ++m)
                 ldsm_x4(kbase + L::off(16 * m + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * ks + (lane >> 4)), ka[m][0],
                         ka[m][1], ka[m][2], ka[m][3]);
 #pragma unroll
             for (int j = 0; j < NQ; ++j)
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
+                for (int m = 0; m < AT_KT; ++m)
                     mma_16816_acc(sacc[m][j], ka[m][0], ka[m][1], ka[m][2], ka[m][3], qb[j][ks][0], qb[j][ks][1]);
         }
         // ---- per head 4j + c: scores of keys 16m + g (e = 0) and 16m + g + 8 (e = 1);
         // scale, mask, softmax over the item's keys (the 8 lanes g of a head)
-        float sv[NQ][4][2], mx[NQ], lsum[NQ];
+        float sv[NQ][AT_KT][2], mx[NQ], lsum[NQ];
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
             mx[j] = -INFINITY;
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < AT_KT; ++m)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const float sc = __fadd_rn(sacc[m][j][2 * e], sacc[m][j][2 * e + 1]);  // both parts
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             for (int o = 4; o < 32; o <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(FULL_MASK, mx[j], o));
             lsum[j] = 0.0f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < AT_KT; ++m)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = 16 * m + g + 8 * e;
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
         const int nsteps = (n + 15) >> 4;
         const int src0 = (2 * c) * 4 + colh, src1 = src0 + 4;
 #pragma unroll
-        for (int js = 0; js < 4; ++js) {
+        for (int js = 0; js < AT_KT; ++js) {
             if (js < nsteps) {
                 uint32_t pb[NQ][2];
 #pragma unroll
