@@ -429,14 +429,18 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     pdl_wait();
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     if (b >= a.B) return;
-    const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
+    // The first records' loads do not wait for the split count: they are bounded
+    // by the buffer's split capacity and go out together with the position's load.
     float o[COMB_BATCH];
 #pragma unroll
-    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < ns ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
+    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < a.max_splits ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
+    const float2 ml0 = d < a.max_splits ? __ldcg(reinterpret_cast<const float2*>(p + (size_t)d * ATT_REC(HD) + HD))
+                                        : make_float2(0.0f, 0.0f);
+    const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
     float mloc = -INFINITY;
     for (int s = d; s < ns; s += HD) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
+        const float2 ml = s == d ? ml0 : __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
         wts[s] = ml.x;
         ls[s] = ml.y;
         mloc = fmaxf(mloc, ml.x);
