@@ -257,7 +257,6 @@ def run_kd(args, rank, world):
     per_launch_bytes = {
         "gate_up": 2 * F * H * wb + B * H * 2 + B * F * 2,
         "down": H * F * wb + B * F * 2 + 2 * B * H * 4,
-        "ffn": 2 * F * H * wb + B * H * 2 + 2 * B * F * 2 + H * F * wb + 2 * B * H * 4,
         "qkv": (shape.q_dim + 2 * shape.kv_dim) * H * wb + B * H * 2 + B * shape.q_dim * 4 + 2 * B * shape.kv_dim * 2,
         "wo": H * shape.q_dim * wb + B * shape.q_dim * 2 + 2 * B * H * 4,
         "lm_head": shape.vocab * H * wb + B * H * 2 + B * shape.vocab * 4,

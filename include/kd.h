@@ -75,9 +75,6 @@ typedef struct {
  * two schedules).  Default: chosen per matrix from its shape and the SM count. */
 #define KD_FLAG_SCHEDULE_STREAM 2
 #define KD_FLAG_SCHEDULE_GROUP 4
-/* Run the FFN (gate|up, then down) as one launch per layer where both matrices
- * are on the group schedule, instead of two launches (same results). */
-#define KD_FLAG_FUSED_FFN 8
 
 /* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
  * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the
@@ -174,14 +171,11 @@ kd_status kd_device_status(kd_model* m, int32_t* flags_out);
  * step's stream.  kd_profile_read waits for the model's work, then returns per
  * kernel class (KD_K_*) the number of launches and their summed device time in
  * milliseconds since the previous read, and resets the sums. */
-/* (No class for RMSNorm: the embedding forms the first normed input, and each
- * later norm is split between the residual writer before it and the projection
- * after it.) */
-/* (KD_K_FFN: gate|up and down as one launch, KD_FLAG_FUSED_FFN; otherwise
- * KD_K_GATE_UP and KD_K_DOWN count them.) */
+/* (KD_K_RMSNORM: the elementwise norm between a residual writer and the next
+ * projection; its row reductions are fused into the residual writer.) */
 enum {
-    KD_K_EMBED = 0, KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO,
-    KD_K_GATE_UP, KD_K_DOWN, KD_K_FFN, KD_K_LM_HEAD, KD_K_ARGMAX, KD_K_COUNT
+    KD_K_EMBED = 0, KD_K_RMSNORM, KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO,
+    KD_K_GATE_UP, KD_K_DOWN, KD_K_LM_HEAD, KD_K_ARGMAX, KD_K_COUNT
 };
 kd_status kd_profile_enable(kd_model* m, int32_t on);
 kd_status kd_profile_read(kd_model* m, int32_t* launches /* [KD_K_COUNT] */,

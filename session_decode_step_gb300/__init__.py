@@ -19,9 +19,6 @@ LIB_PATH = _PKG / "libkd.so"
 KD_MAX_BATCH = 16
 KD_ATTN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 KD_FLAG_NO_GRAPH = 1
-KD_FLAG_SCHEDULE_STREAM = 2
-KD_FLAG_SCHEDULE_GROUP = 4
-KD_FLAG_FUSED_FFN = 8
 STATUS = {0: "KD_OK", -1: "KD_ERR_INVALID_ARG", -2: "KD_ERR_OOM", -3: "KD_ERR_CUDA",
           -4: "KD_ERR_NO_FREE_SLOT", -5: "KD_ERR_BAD_SESSION", -6: "KD_ERR_POSITION",
           -7: "KD_ERR_BATCH", -8: "KD_ERR_UNSUPPORTED", -9: "KD_ERR_DEVICE"}
@@ -234,7 +231,7 @@ def kd_device_status(m) -> int:
     return out.value
 
 
-KERNEL_CLASSES = ("embed", "qkv", "attn_split", "attn_combine", "wo", "gate_up", "down", "ffn",
+KERNEL_CLASSES = ("embed", "rmsnorm", "qkv", "attn_split", "attn_combine", "wo", "gate_up", "down",
                   "lm_head", "argmax")
 
 

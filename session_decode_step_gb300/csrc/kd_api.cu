@@ -7,9 +7,7 @@
 //   RMSNorm -> QKV mmvq (+RoPE at each row's position, +KV append) ->
 //   split-K flash-decode -> combine -> O mmvq (+residual) -> RMSNorm ->
 //   gate|up mmvq (+SwiGLU) -> down mmvq (+residual),
-// then the final RMSNorm, the lm_head mmvq and the device argmax.  The norms
-// after the first have no launch: each is split between the residual writer
-// before it and the projection after it (NormLink in kd_kernels.h).  The launch
+// then the final RMSNorm, the lm_head mmvq and the device argmax.  The launch
 // train is captured once per (B, output buffers) as a CUDA graph and replayed;
 // consecutive kernels overlap through programmatic dependent launch (each
 // kernel's weight prefetch runs before it waits for its predecessor).
@@ -63,7 +61,6 @@ cudaError_t init_device_attributes(int dev) {
         cudaError_t e = kd::mmvq_init_attributes();
         if (e == cudaSuccess) e = kd::attn_init_attributes();
         if (e == cudaSuccess) e = kd::rowops_init_attributes();
-        if (e == cudaSuccess) e = kd::ffn_init_attributes();
         g_attr_err[dev] = e;
     });
     return g_attr_err[dev];
@@ -143,11 +140,8 @@ struct kd_model {
     kd::AttnMaps kmaps{};     // tensor maps over the K and V arenas
     CUtensorMap map_xn{}, map_attn{}, map_act{};  // activation maps the projections read through
     float* x = nullptr;       // [16][H] residual stream
-    __half* xn = nullptr;     // [16][H] the next projection's input (NormLink xs; the embedding's normed rows)
-    float* ssq_a = nullptr;   // [16][H/32] per-group sums of squares after the attention residual add
-    float* ssq_f = nullptr;   // [16][H/32] the same after the FFN residual add (or the embedding)
-    bool ffn_fused = false;   // gate|up and down as one launch per layer (KD_FLAG_FUSED_FFN, both on the group schedule)
-    int* ffn_ready = nullptr; // [L] arrival counters of the fused FFN (zeroed by each step's embedding)
+    __half* xn = nullptr;     // [16][H] normed activations (written by the fused RMSNorm)
+    float* ssq = nullptr;     // [H/32][16] per-group sums of squares of the residual rows
     float* q = nullptr;       // [16][nh][hd]
     __half* attn = nullptr;   // [16][nh*hd]
     __half* act = nullptr;    // [16][F]
@@ -258,8 +252,6 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
             st = upload_packed({{w->w_down[l], H}}, F, tiles_natural(H), staging, d_tiles, m->num_sms, m->down[l], fm);
     }
     if (st == KD_OK) st = upload_packed({{w->output, V}}, H, tiles_natural(V), staging, d_tiles, m->num_sms, m->head, fm);
-    m->ffn_fused = (c.flags & KD_FLAG_FUSED_FFN) && L > 0 && m->gu[0].mode == kd::MMVQ_GROUP &&
-                   m->down[0].mode == kd::MMVQ_GROUP;
     cudaFree(staging);
     cudaFree(d_tiles);
     if (st != KD_OK) return st;
@@ -299,10 +291,7 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     const int MB = KD_MAX_BATCH;
     KD_CK(m->alloc(&m->x, (size_t)MB * H * sizeof(float)));
     KD_CK(m->alloc(&m->xn, (size_t)MB * H * sizeof(__half)));
-    KD_CK(m->alloc(&m->ssq_a, (size_t)(H / kd::GROUP_ROWS) * kd::MAX_NORM_SLOTS * sizeof(float)));
-    KD_CK(m->alloc(&m->ssq_f, (size_t)(H / kd::GROUP_ROWS) * kd::MAX_NORM_SLOTS * sizeof(float)));
-    KD_CK(m->alloc(&m->ffn_ready, (size_t)L * sizeof(int)));
-    KD_CK(cudaMemset(m->ffn_ready, 0, (size_t)L * sizeof(int)));
+    KD_CK(m->alloc(&m->ssq, (size_t)(H / kd::GROUP_ROWS) * kd::MAX_NORM_SLOTS * sizeof(float)));
 
     KD_CK(m->alloc(&m->q, (size_t)MB * nh * hd * sizeof(float)));
     KD_CK(m->alloc(&m->attn, (size_t)MB * nh * hd * sizeof(__half)));
@@ -342,9 +331,8 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
 }
 
 // The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
-// With only_layer >= 0: that layer alone, on residual rows already in m->x with
-// their normed rows in m->xn and their sums of squares in both tables (as the
-// embedding leaves them); no embedding, no head.
+// With only_layer >= 0: that layer alone, on residual rows already in m->x whose
+// full-row sums of squares are in m->ssq (one group); no embedding, no head.
 static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1) {
     const kd_config& c = m->cfg;
     const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
@@ -394,24 +382,19 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.x = x; a.B = B; a.part = m->part; a.cnt = m->cnt; a.err = m->err;
         return a;
     };
-    // RMSNorm has no launch of its own (NormLink): the embedding writes the first
-    // normed input; each residual writer (o-proj, down) leaves its rows' per-group
-    // sums of squares in its table and the next projection's input m->xn scaled by
-    // the factor of the other table; the projection reading m->xn rescales its sums
-    // by the ratio of the two factors.
-    auto resid = [&](kd::MmvqArgs& a, float* ssq_out, const float* ssq_pre, const float* next_norm) {
-        a.y = m->x; a.ld = H; a.ssq_out = ssq_out;
-        a.nl.rs_pre = ssq_pre; a.nl.ng = H / kd::GROUP_ROWS; a.nl.eps = c.rms_eps;
-        a.nl.nw = next_norm; a.nl.xs = m->xn;
+    // RMSNorm: the embedding writes the first normed input itself; the residual
+    // writers (o-proj, down) leave per-group sums of squares, and an elementwise
+    // kernel forms the next projection's normed fp16 input m->xn from them.
+    auto resid = [&](kd::MmvqArgs& a) {
+        a.y = m->x; a.ld = H; a.ssq_out = m->ssq;
     };
-    auto normed = [&](kd::MmvqArgs& a, const float* ssq_cur, const float* ssq_pre) {
-        a.nl.rs_pre = ssq_pre; a.nl.rs_cur = ssq_cur; a.nl.ng = H / kd::GROUP_ROWS; a.nl.eps = c.rms_eps;
+    auto norm = [&](const float* w) {
+        return kd::launch_norm_from_ssq(m->x, m->ssq, B, H, w, c.rms_eps, m->xn, pdl, s);
     };
     const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
     const bool whole = only_layer < 0;
     if (whole)
-        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, m->ssq_a,
-                                            m->ssq_f, m->ffn_ready, L, pdl, s));
+        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, pdl, s));
     if (whole && m->hidden_dbg &&
         (e = cudaMemcpyAsync(m->hidden_dbg, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
@@ -419,7 +402,6 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         __half* kc = m->kc + (size_t)l * m->layer_kv;
         __half* vc = m->vc + (size_t)l * m->layer_kv;
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
-        normed(a, m->ssq_f, m->ssq_a);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
         KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->map_xn, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
@@ -431,20 +413,17 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->kmaps, m->attn_grid, pdl, s));
         KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
         a = mm(m->wo[l], m->attn);
-        resid(a, m->ssq_a, m->ssq_f, m->norms + (size_t)(2 * l + 1) * H);  // then the FFN norm
+        resid(a);
         KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * l + 1) * H));  // the FFN norm
         a = mm(m->gu[l], m->xn);
-        normed(a, m->ssq_a, m->ssq_f);
         a.act = m->act; a.ld = F;
-        kd::MmvqArgs d = mm(m->down[l], m->act);
-        // then the next layer's attention norm, or the output norm
-        resid(d, m->ssq_f, m->ssq_a, m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H);
-        if (m->ffn_fused) {
-            KD_RUN(KD_K_FFN, kd::launch_ffn(a, d, m->ffn_ready + l, m->map_xn, m->map_act, m->num_sms, pdl, s));
-        } else {
-            KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
-            KD_RUN(KD_K_DOWN, kd::launch_mmvq(d, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
-        }
+        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
+        a = mm(m->down[l], m->act);
+        resid(a);
+        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        if (whole || l + 1 < l1)  // next layer's attention norm, or the output norm
+            KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H));
         if (whole && m->hidden_dbg &&
             (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)(l + 1) * B * H, m->x, (size_t)B * H * 4,
                                  cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
@@ -452,7 +431,6 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     }
     if (!whole) return cudaSuccess;
     kd::MmvqArgs a = mm(m->head, m->xn);
-    normed(a, m->ssq_f, m->ssq_a);
     a.y = lg; a.ld = V;
     KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->map_xn, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
     if (am)
@@ -673,8 +651,7 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const i
     const size_t bytes = (size_t)B * m->cfg.hidden * sizeof(float);
     KD_CK(cudaMemcpyAsync(m->x, x_in, bytes, cudaMemcpyDefault, s));
     KD_CK(kd::launch_row_norm(m->x, B, m->cfg.hidden, m->norms + (size_t)(2 * layer) * m->cfg.hidden,
-                              m->cfg.rms_eps, m->xn, m->ssq_a, m->ssq_f, s));
-    KD_CK(cudaMemsetAsync(m->ffn_ready + layer, 0, sizeof(int), s));
+                              m->cfg.rms_eps, m->xn, s));
     const bool prof = m->prof;
     m->prof = false;
     cudaError_t e = enqueue_step(m, B, nullptr, nullptr, s, layer);

@@ -80,35 +80,14 @@ inline cudaError_t make_x_map(const __half* x, int K, int rows, CUtensorMap* out
     return encode_fp16_2d(out, x, K, rows, 64, 8);
 }
 
-// RMSNorm is split between the kernels on either side of it, so it needs no
-// launch of its own.  For residual rows x (H = 32 * ng columns) let S[n][g] be
-// the sum of squares of row n's 32 columns of group g, and
-// r(S)[n] = 1 / sqrt(sum_g S[n][g] / H + eps).  A residual writer (EPI_RESID)
-// leaves S of the rows it wrote in ssq_out and, when xs is set, the next
-// projection's input xs[n][i] = fp16(x_new[n][i] * nw[i] * r(rs_pre)[n]), scaled
-// by the factor of the previous residual rows (known before the writer starts,
-// and close to the new one, so the fp16 values stay near unit scale).  A
-// projection that reads such an input (rs_pre set) multiplies every sum by
-// r(rs_cur)[n] / r(rs_pre)[n], which makes it the product with the normed input
-// x_new * r(rs_cur) * nw.  Both tables are session-major: [16][ng].
-struct NormLink {
-    const float* rs_pre = nullptr;  // S of the rows whose factor scaled xs (null: no norm on either side)
-    const float* rs_cur = nullptr;  // projection: S of the rows xs was formed from
-    int ng = 0;                     // groups per row (H / 32)
-    float eps = 0.0f;
-    const float* nw = nullptr;      // writer: the next norm's weight [H]
-    __half* xs = nullptr;           // writer: the next projection's input [B][H]
-};
-
 struct MmvqArgs {
     const uint8_t* w;
     int G, KG, W, maxc, K;
     const __half* x;     // [B][K] fp16 activations (the kernels read them through the launch's map of x)
     int B;
-    NormLink nl;
     // EPI_RESID: each group's writer also leaves sum(x_new^2) of its 32 rows per
-    // session in ssq_out[n][g] (session-major, G entries per session).
-    float* ssq_out;      // [16][G]
+    // session in ssq_out[g][n], so the next RMSNorm needs no row reduction.
+    float* ssq_out;      // [G][16]
     float* part;         // split-K partials
     int* cnt;            // [G] arrival counters, zero between launches
                          // (part: [G][maxc][32 rows][16 columns] fp32)
@@ -131,17 +110,6 @@ cudaError_t launch_mmvq(const MmvqArgs& a, const CUtensorMap& xmap, int mode, in
                         cudaStream_t s);
 // Smallest dynamic shared memory any mmvq launch needs (for occupancy checks).
 cudaError_t mmvq_init_attributes();
-
-// The feed-forward block as one launch (kd_ffn.cu): gu is the gate|up product
-// (EPI_SWIGLU into gu.act), dn the down product (EPI_RESID, reading gu.act
-// through xm_dn).  Both matrices on the group schedule; *ready is an arrival
-// counter (zero before the launch).  The grid is min(gu.G,
-// num_sms) CTAs of one per SM, whose down stages wait for other CTAs' gate|up
-// results: it needs every CTA resident at once (one per SM of a GPU running
-// nothing else alongside), else those waits run out and the fault word is set.
-cudaError_t launch_ffn(const MmvqArgs& gu, const MmvqArgs& dn, int* ready, const CUtensorMap& xm_gu,
-                       const CUtensorMap& xm_dn, int num_sms, bool pdl, cudaStream_t s);
-cudaError_t ffn_init_attributes();
 
 // ---- attention -------------------------------------------------------------
 constexpr int ATT_CHUNK = 64;        // keys per split; fixed, so a session's splits depend on its length only
@@ -184,16 +152,15 @@ cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half*
 
 // ---- row ops -----------------------------------------------------------------
 // x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and the first
-// layer's normed input xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w);
-// the per-group sums of squares of x (NormLink) go to both ssq0 and ssq1
-// ([16][H/32] each), so a projection reading xn scales by exactly 1.
-// It also zeroes zero[0 .. n_zero) (the step's arrival counters).
+// layer's normed input xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w)
 cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, float* ssq0, float* ssq1, int* zero, int n_zero, bool pdl,
-                         cudaStream_t s);
-// The norm and the two tables as in launch_embed, for rows supplied from outside.
-cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, float* ssq0,
-                            float* ssq1, cudaStream_t s);
+                         float eps, __half* xn, bool pdl, cudaStream_t s);
+// xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w) for rows supplied from outside
+cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, cudaStream_t s);
+// The same norm from the per-group sums of squares ssq[g][b] (g < H/32) a
+// residual writer left: elementwise, spread over many CTAs.
+cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
+                                 __half* xn, bool pdl, cudaStream_t s);
 cudaError_t rowops_init_attributes();
 // out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none).
 // keys [>= B] and done: device scratch that is zero before the first launch;

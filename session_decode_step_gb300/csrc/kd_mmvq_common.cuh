@@ -89,73 +89,6 @@ __device__ __forceinline__ void lds_x_tile(const uint8_t* xt, int gq, int cq, ui
             xv[kb][nt] = lds_v4(xt + (nt * 2 + (kb >> 1)) * 1024 + row * 128 + ((((kb & 1) * 4 + cq) ^ row) << 4));
 }
 
-// ---- RMSNorm split across the launches (NormLink) -----------------------------
-// Whether a launch's epilogue uses NormLink factors at all.
-template <int EPI>
-__device__ __forceinline__ bool norm_on(const MmvqArgs& a) {
-    return a.nl.rs_pre != nullptr && (EPI != EPI_RESID || a.nl.xs != nullptr);
-}
-// sc[n] for the launch's sessions, one warp per session (the caller
-// synchronises the CTA before reading sc):
-//   residual writer: r(rs_pre)[n], the scale of the xs it writes;
-//   any other epilogue: r(rs_cur)[n] / r(rs_pre)[n]
-//     = sqrt((sum rs_pre[n] / H + eps) / (sum rs_cur[n] / H + eps));
-//   1 without a NormLink (then nothing is rescaled).
-// A session's table total: lane l adds groups l, l + 32, ... in order, then a
-// fixed shuffle tree -- the same for any B.  Every load of a warp's sessions and
-// tables is issued before the first add, so this costs one memory round trip.
-template <int EPI>
-__device__ __forceinline__ void norm_scales(const MmvqArgs& a, float* sc, int warp, int lane) {
-    constexpr int NJ = MAX_NORM_SLOTS / MMVQ_WARPS;  // sessions per warp
-    constexpr int NTAB = EPI == EPI_RESID ? 1 : 2;   // tables read: rs_pre (and rs_cur)
-    if (!norm_on<EPI>(a)) {
-        for (int n = warp; n < a.B; n += MMVQ_WARPS)
-            if (lane == 0) sc[n] = 1.0f;
-        return;
-    }
-    const int ng = a.nl.ng;
-    const float* tab[2] = {a.nl.rs_pre, a.nl.rs_cur};
-    float s[NJ][NTAB];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j)
-#pragma unroll
-        for (int t = 0; t < NTAB; ++t) s[j][t] = 0.0f;
-    for (int g0 = 0; g0 < ng; g0 += 4 * 32) {
-        float p[NJ][NTAB][4];
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-#pragma unroll
-            for (int t = 0; t < NTAB; ++t)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int n = warp + MMVQ_WARPS * j, gi = g0 + lane + 32 * k;
-                    p[j][t][k] = n < a.B && gi < ng ? __ldcg(tab[t] + (size_t)n * ng + gi) : 0.0f;
-                }
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-#pragma unroll
-            for (int t = 0; t < NTAB; ++t)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) s[j][t] = __fadd_rn(s[j][t], p[j][t][k]);
-    }
-    const float h = (float)(ng * GROUP_ROWS);
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-#pragma unroll
-        for (int t = 0; t < NTAB; ++t)
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s[j][t] = __fadd_rn(s[j][t], __shfl_xor_sync(FULL_MASK, s[j][t], o));
-        const int n = warp + MMVQ_WARPS * j;
-        if (lane == 0 && n < a.B) {
-            const float dp = __fadd_rn(__fdiv_rn(s[j][0], h), a.nl.eps);
-            if constexpr (EPI == EPI_RESID)
-                sc[n] = __fdiv_rn(1.0f, __fsqrt_rn(dp));
-            else
-                sc[n] = __fsqrt_rn(__fdiv_rn(dp, __fadd_rn(__fdiv_rn(s[j][NTAB - 1], h), a.nl.eps)));
-        }
-    }
-}
-
 // ---- epilogues on single outputs ------------------------------------------
 // Row r (0..31) of row group g, session n, value v.
 __device__ __forceinline__ void epi_store(const MmvqArgs& a, int g, int r, int n, float v) {
@@ -176,11 +109,6 @@ __device__ __forceinline__ float epi_resid_apply(const MmvqArgs& a, int g, int r
     const float x = __fadd_rn(old, v);
     a.y[(size_t)n * a.ld + (size_t)g * GROUP_ROWS + r] = x;
     return x;
-}
-// The next projection's input from a new residual value (NormLink): nwr is the
-// next norm's weight at this row, scn the session's r(rs_pre).
-__device__ __forceinline__ void epi_xs(const MmvqArgs& a, int g, int r, int n, float x, float nwr, float scn) {
-    a.nl.xs[(size_t)n * a.ld + (size_t)g * GROUP_ROWS + r] = __float2half_rn(__fmul_rn(__fmul_rn(x, nwr), scn));
 }
 // Pair epilogues: tile 0 row r with tile 1 row r (r = 0..15).
 //   SwiGLU: act = fp16(silu(gate) * up)

@@ -17,8 +17,7 @@ namespace kd {
 // shallower ring and the partial buffer laid over it let two CTAs share an SM,
 // so no CTA waits for a second group while others idle.
 // Shared memory: per warp a ring of RD stages, each the stage's weights and its
-// activation tiles; then the barriers, the partial-sum buffer and the sessions'
-// norm factors (NormLink).
+// activation tiles; then the barriers and the partial-sum buffer.
 template <int NT, bool PAIR>
 struct CtaSmem {
     static constexpr int RD = PAIR ? 2 : 3;  // stages in flight per warp (measured best for the step)
@@ -29,8 +28,8 @@ struct CtaSmem {
     static constexpr size_t BAR_OFF = W_OFF + RING_BYTES;
     static constexpr size_t RED_BYTES = (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
     static constexpr size_t RED_OFF = PAIR ? W_OFF : BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
-    static constexpr size_t SC_OFF = PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES;
-    static constexpr size_t TOTAL = SC_OFF + MAX_NORM_SLOTS * sizeof(float) + 1024;  // + alignment slack
+    static constexpr size_t TOTAL =
+        (PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES) + 1024;  // + alignment slack
     static_assert(!PAIR || RED_BYTES <= RING_BYTES, "the partial buffer lies over the ring");
 };
 
@@ -49,7 +48,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     uint8_t* ring = smem + L::W_OFF + (size_t)warp * RD * STAGE_BYTES;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
     float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [warp][32 rows][RS]
-    float* sc = reinterpret_cast<float*>(smem + L::SC_OFF);    // [session]
 
     const int kg0 = warp * a.KG / MMVQ_WARPS, nk = (warp + 1) * a.KG / MMVQ_WARPS - kg0;
     const int ngrp = (int)blockIdx.x < a.G ? (a.G - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -81,9 +79,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     if (lane == 0)
         for (int i = 0; i < RD && i < total; ++i)
             tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);
-    // The sessions' norm factors, while the first activation tiles are in flight.
-    norm_scales<EPI>(a, sc, warp, lane);
-    __syncthreads();
 
     int sidx = 0, slot = 0;
     uint32_t phase = 0;
@@ -94,7 +89,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
         // does not wait for it: the residual rows (thread (warp, lane) takes session
         // warp + 8j, row lane) or the q|k|v epilogue's positions and cos/sin pairs.
         float xold[NT];
-        float nwr = 0.0f;  // the next norm's weight at row lane (when the writer forms xs)
         QkvIn qin{};
         if constexpr (EPI == EPI_RESID) {
 #pragma unroll
@@ -102,7 +96,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
                 const int n = warp + MMVQ_WARPS * j;
                 xold[j] = n < a.B ? resid_load(a, g, lane, n) : 0.0f;
             }
-            if (a.nl.xs != nullptr) nwr = a.nl.nw[(size_t)g * GROUP_ROWS + lane];
         } else if constexpr (EPI == EPI_QKV) {
             if (tid < a.B * TILE_ROWS) qin = qkv_load(a, g, tid & 15, tid >> 4);
         }
@@ -158,21 +151,19 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
             for (int n = warp; n < a.B; n += MMVQ_WARPS) {  // a warp per session, a lane per row
                 const float v = sum_rows(lane, n);
                 if constexpr (EPI == EPI_STORE) {
-                    epi_store(a, g, lane, n, __fmul_rn(v, sc[n]));
+                    epi_store(a, g, lane, n, v);
                 } else {
                     const float x = epi_resid_apply(a, g, lane, n, n >= MMVQ_WARPS ? xold[NT - 1] : xold[0], v);
-                    if (a.nl.xs != nullptr) epi_xs(a, g, lane, n, x, nwr, sc[n]);
                     float s = __fmul_rn(x, x);
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
-                    if (lane == 0) a.ssq_out[(size_t)n * a.G + g] = s;
+                    if (lane == 0) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
                 }
             }
         } else {
             for (int e = tid; e < a.B * TILE_ROWS; e += MMVQ_WARPS * 32) {  // (row pair, session)
                 const int n = e >> 4, rr = e & 15;
-                const float f = sc[n];
-                const float v0 = __fmul_rn(sum_rows(rr, n), f), v1 = __fmul_rn(sum_rows(rr + TILE_ROWS, n), f);
+                const float v0 = sum_rows(rr, n), v1 = sum_rows(rr + TILE_ROWS, n);
                 if constexpr (EPI == EPI_SWIGLU)
                     epi_swiglu(a, g, rr, n, v0, v1);
                 else

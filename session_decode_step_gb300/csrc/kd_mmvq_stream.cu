@@ -18,11 +18,9 @@ namespace kd {
 
 __device__ __forceinline__ int stage_owner(long t, long T, long W) { return (int)(((t + 1) * W - 1) / T); }
 
-// Epilogue over this lane's fragment of a finished row group; sc: the sessions'
-// norm factors (norm_scales).
+// Epilogue over this lane's fragment of a finished row group.
 template <int NT, int EPI>
-__device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, int cq, float (&v)[MT][NT][4],
-                                              const float* sc) {
+__device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, int cq, float (&v)[MT][NT][4]) {
     float ss[NT][2];  // RESID: this lane's share of sum(x_new^2) per column
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) ss[nt][0] = ss[nt][1] = 0.0f;
@@ -33,22 +31,17 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
             const int n = nt * 8 + col_session(2 * cq + (i & 1));
             if (n >= a.B) continue;
             const int r = gq + ((i >> 1) << 3);  // row within a 16-row tile
-            const float f = sc[n];
             if constexpr (EPI == EPI_STORE) {
-                epi_store(a, g, r, n, __fmul_rn(v[0][nt][i], f));
-                epi_store(a, g, r + TILE_ROWS, n, __fmul_rn(v[1][nt][i], f));
+                epi_store(a, g, r, n, v[0][nt][i]);
+                epi_store(a, g, r + TILE_ROWS, n, v[1][nt][i]);
             } else if constexpr (EPI == EPI_RESID) {
                 const float x0 = epi_resid(a, g, r, n, v[0][nt][i]);
                 const float x1 = epi_resid(a, g, r + TILE_ROWS, n, v[1][nt][i]);
-                if (a.nl.xs != nullptr) {
-                    epi_xs(a, g, r, n, x0, a.nl.nw[(size_t)g * GROUP_ROWS + r], f);
-                    epi_xs(a, g, r + TILE_ROWS, n, x1, a.nl.nw[(size_t)g * GROUP_ROWS + r + TILE_ROWS], f);
-                }
                 ss[nt][i & 1] = __fmaf_rn(x1, x1, __fmaf_rn(x0, x0, ss[nt][i & 1]));
             } else if constexpr (EPI == EPI_SWIGLU) {
-                epi_swiglu(a, g, r, n, __fmul_rn(v[0][nt][i], f), __fmul_rn(v[1][nt][i], f));
+                epi_swiglu(a, g, r, n, v[0][nt][i], v[1][nt][i]);
             } else {
-                epi_qkv(a, g, r, n, __fmul_rn(v[0][nt][i], f), __fmul_rn(v[1][nt][i], f));
+                epi_qkv(a, g, r, n, v[0][nt][i], v[1][nt][i]);
             }
         }
     if constexpr (EPI == EPI_RESID) {
@@ -62,21 +55,20 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
                 s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 8));
                 s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, 16));
                 const int n = nt * 8 + col_session(2 * cq + j);
-                if (gq == 0 && n < a.B) a.ssq_out[(size_t)n * a.G + g] = s;
+                if (gq == 0 && n < a.B) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
             }
     }
 }
 
 // Shared memory: per warp a ring of RD stages, each the stage's weights and its
-// activation tiles; then the barriers and the sessions' norm factors.
+// activation tiles.
 template <int NT>
 struct StreamSmem {
     static constexpr int RD = NT == 1 ? RING : RING - 1;  // stages in flight per warp
     static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * RD * NT * XTILE_BYTES;  // at a 1024-byte boundary
     static constexpr size_t W_OFF = X_BYTES;
     static constexpr size_t BAR_OFF = W_OFF + (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
-    static constexpr size_t SC_OFF = BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
-    static constexpr size_t TOTAL = SC_OFF + MAX_NORM_SLOTS * sizeof(float) + 1024;  // + alignment slack
+    static constexpr size_t TOTAL = BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) + 1024;  // + alignment slack
 };
 
 template <int NT, int EPI>
@@ -92,7 +84,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     uint8_t* xring = smem + (size_t)warp * RD * NT * XTILE_BYTES;
     uint8_t* ring = smem + L::W_OFF + (size_t)warp * RD * STAGE_BYTES;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
-    float* sc = reinterpret_cast<float*>(smem + L::SC_OFF);
 
     const long T = (long)a.G * a.KG;
     const int w = blockIdx.x * MMVQ_WARPS + warp;
@@ -126,9 +117,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
             tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, xkg, &bar[i]);
             if (++xkg == a.KG) xkg = 0;
         }
-    // The sessions' norm factors, while the first activation tiles are in flight.
-    norm_scales<EPI>(a, sc, warp, lane);
-    __syncthreads();
 
     float acc[MT][NT][4];
 #pragma unroll
@@ -171,7 +159,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
         const long gfirst = (long)g * a.KG;
         const int w0 = stage_owner(gfirst, T, a.W), w1 = stage_owner(gfirst + a.KG - 1, T, a.W);
         if (w0 == w1) {
-            frag_epilogue<NT, EPI>(a, g, gq, cq, acc, sc);  // the whole group was this warp's
+            frag_epilogue<NT, EPI>(a, g, gq, cq, acc);  // the whole group was this warp's
         } else {
             const int ncontrib = w1 - w0 + 1;
             float* pt = a.part + ((size_t)g * a.maxc + (w - w0)) * (GROUP_ROWS * 16);
@@ -231,7 +219,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
                             }
                     }
                 }
-                frag_epilogue<NT, EPI>(a, g, gq, cq, v, sc);
+                frag_epilogue<NT, EPI>(a, g, gq, cq, v);
                 if (lane == 0) a.cnt[g] = 0;  // ready for the next launch
             }
         }

@@ -1,8 +1,6 @@
 // kd_rowops.cu -- the row-parallel operations of the decode step: embedding
-// gather with the first RMSNorm, the same norm for rows supplied from outside,
-// and the greedy argmax.  (The norms inside the layer stack have no kernel of
-// their own: NormLink splits them between the residual writer and the next
-// projection.)
+// gather with the first RMSNorm, the RMSNorm between a residual writer and the
+// next projection, and the greedy argmax.
 //
 // memra-engine decode_batch.rs treats the row-parallel ops as the same kernels
 // run at B rows; here every row's arithmetic is its own, so row b's bytes never
@@ -54,32 +52,15 @@ __device__ __forceinline__ void norm_row(const float* x, int H, const float* w, 
     }
 }
 
-// Sum of squares of one 32-column group held one value per lane of a warp:
-// a fixed shuffle tree; lane 0 writes it to both NormLink tables ([16][H/32]).
-__device__ __forceinline__ void group_ssq(float v, int b, int gi, int ng, float* ssq0, float* ssq1) {
-    float s = __fmul_rn(v, v);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
-    if ((threadIdx.x & 31) == 0 && gi < ng) {
-        ssq0[(size_t)b * ng + gi] = s;
-        ssq1[(size_t)b * ng + gi] = s;
-    }
-}
-
 // x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), then the
-// first layer's normed input xn[b] = fp16(rmsnorm(x[b]) * w) and the per-group
-// sums of squares of x[b] in both tables.  Element i = i0 + tid + 256u: for a
-// fixed u each warp holds one whole 32-column group.
+// first layer's normed input xn[b] = fp16(rmsnorm(x[b]) * w).
 __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __restrict__ emb,
                                                               const int* __restrict__ token, int H,
                                                               float* __restrict__ x, const float* __restrict__ w,
-                                                              float eps, __half* __restrict__ xn,
-                                                              float* __restrict__ ssq0, float* __restrict__ ssq1,
-                                                              int* __restrict__ zero, int n_zero) {
+                                                              float eps, __half* __restrict__ xn) {
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     const int b = blockIdx.x, tid = threadIdx.x;
-    for (int i = b * EMBED_THREADS + tid; i < n_zero; i += gridDim.x * EMBED_THREADS) zero[i] = 0;
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
     float* xr = x + (size_t)b * H;
     constexpr int U = 16;  // elements per thread whose loads are issued together
@@ -97,40 +78,91 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = i0 + tid + EMBED_THREADS * u;
-            float v = 0.0f;
             if (i < H) {
                 const __half_raw hr{dbits[u]};
-                v = __fmul_rn((float)q[u], __half2float(__half(hr)));
+                const float v = __fmul_rn((float)q[u], __half2float(__half(hr)));
                 xr[i] = v;
                 s = __fmaf_rn(v, v, s);
             }
-            group_ssq(v, b, (i0 + EMBED_THREADS * u) / 32 + (tid >> 5), H / 32, ssq0, ssq1);
         }
     }
     norm_row(xr, H, w, eps, xn + (size_t)b * H, s);  // each thread re-reads only what it wrote
 }
 
-// The same norm and tables for residual rows supplied from outside.
+// The same norm for residual rows supplied from outside.
 __global__ void __launch_bounds__(EMBED_THREADS) row_norm_kernel(const float* __restrict__ x, int H,
                                                                  const float* __restrict__ w, float eps,
-                                                                 __half* __restrict__ xn, float* __restrict__ ssq0,
-                                                                 float* __restrict__ ssq1) {
+                                                                 __half* __restrict__ xn) {
     const int b = blockIdx.x, tid = threadIdx.x;
     const float* xr = x + (size_t)b * H;
     float s = 0.0f;
-    for (int i0 = 0; i0 < H; i0 += EMBED_THREADS) {  // H is a multiple of 32: warps stay converged
-        const int i = i0 + tid;
-        const float v = i < H ? xr[i] : 0.0f;
-        s = __fmaf_rn(v, v, s);
-        group_ssq(v, b, i0 / 32 + (tid >> 5), H / 32, ssq0, ssq1);
-    }
+    for (int i = tid; i < H; i += EMBED_THREADS) s = __fmaf_rn(xr[i], xr[i], s);
     norm_row(xr, H, w, eps, xn + (size_t)b * H, s);
 }
 
-cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, float* ssq0,
-                            float* ssq1, cudaStream_t s) {
-    row_norm_kernel<<<B, EMBED_THREADS, 0, s>>>(x, H, w, eps, xn, ssq0, ssq1);
+cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, cudaStream_t s) {
+    row_norm_kernel<<<B, EMBED_THREADS, 0, s>>>(x, H, w, eps, xn);
     return cudaGetLastError();
+}
+
+// RMSNorm of residual rows whose per-group sums of squares were left by the
+// kernel that wrote them: r_b = 1 / sqrt(sum_g ssq[g][b] / H + eps) (groups in
+// order: lane-strided, then a fixed shuffle tree), then elementwise
+// xn = fp16(x * r_b * w).  Block (c, b) covers columns [1024c, 1024c + 1024) of row b.
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_COLS = NORM_THREADS * 4;
+
+__global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float* __restrict__ x,
+                                                                     const float* __restrict__ ssq, int H,
+                                                                     const float* __restrict__ w, float eps,
+                                                                     __half* __restrict__ xn) {
+    __shared__ float rsh;
+    pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
+    pdl_wait();
+    const int b = blockIdx.y, tid = threadIdx.x;
+    const int i = blockIdx.x * NORM_COLS + tid * 4;
+    const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
+    const float4 g = i < H ? *reinterpret_cast<const float4*>(w + i) : make_float4(0, 0, 0, 0);
+    if (tid < 32) {
+        // lane l adds groups l, l + 32, l + 64, ... in order; the loads of 8 of
+        // them are issued together
+        const int ng = H / 32;
+        float s = 0.0f;
+        for (int g0 = 0; g0 < ng; g0 += 8 * 32) {
+            float part[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gi = g0 + tid + 32 * j;
+                part[j] = gi < ng ? ssq[(size_t)gi * MAX_NORM_SLOTS + b] : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (g0 + tid + 32 * j < ng) s = __fadd_rn(s, part[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+        if (tid == 0) rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
+    }
+    __syncthreads();
+    if (i >= H) return;
+    const float r = rsh;
+    __half2* o = reinterpret_cast<__half2*>(xn + (size_t)b * H + i);
+    o[0] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.x, r), g.x), __fmul_rn(__fmul_rn(v.y, r), g.y));
+    o[1] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
+}
+
+cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
+                                 __half* xn, bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.gridDim = dim3((H + NORM_COLS - 1) / NORM_COLS, B);
+    cfg.blockDim = dim3(NORM_THREADS);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, norm_from_ssq_kernel, x, ssq, H, w, eps, xn);
 }
 
 // Greedy argmax over many CTAs.  Each (value, index) maps to a 64-bit key whose
@@ -197,7 +229,8 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __r
 cudaError_t rowops_init_attributes() {
     // One shared-memory carveout for every kernel of the step, so consecutive
     // kernels never wait for an SM to reconfigure its L1/shared split.
-    for (const void* f : {(const void*)embed_kernel, (const void*)row_norm_kernel, (const void*)argmax_kernel}) {
+    for (const void* f : {(const void*)embed_kernel, (const void*)row_norm_kernel, (const void*)norm_from_ssq_kernel,
+                          (const void*)argmax_kernel}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -213,15 +246,14 @@ static void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pd
 }
 
 cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, float* ssq0, float* ssq1, int* zero, int n_zero, bool pdl,
-                         cudaStream_t s) {
+                         float eps, __half* xn, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
     cfg.gridDim = dim3(B);
     cfg.blockDim = dim3(EMBED_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn, ssq0, ssq1, zero, n_zero);
+    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn);
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,

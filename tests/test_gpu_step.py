@@ -51,9 +51,8 @@ def tiny():
 
 
 # 0: schedules chosen per matrix; 2 / 4: every projection forced onto the
-# stream / group schedule (the tiny model alone would only exercise one of them);
-# 12 (group + KD_FLAG_FUSED_FFN) runs the FFN as one launch.
-@pytest.mark.parametrize("flags", [0, 2, 4, 12])
+# stream / group schedule (the tiny model alone would only exercise one of them).
+@pytest.mark.parametrize("flags", [0, 2, 4])
 def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags):
     kd = kdlib
     shape, w = tiny
@@ -99,7 +98,7 @@ def greedy_stream(kd, m, ids, lens, tok0, steps, V):
 
 
 # graph replay (auto schedules), kernel-by-kernel launches, and each schedule forced
-@pytest.mark.parametrize("flags", [0, 1, 2, 4, 12])
+@pytest.mark.parametrize("flags", [0, 1, 2, 4])
 def test_tiny_batch_invariance(kdlib, tiny, flags):
     kd = kdlib
     shape, w = tiny
@@ -142,27 +141,6 @@ def test_tiny_graph_equals_direct_and_rewind(kdlib, tiny):
         finally:
             kd.kd_model_free(m)
     assert np.array_equal(out[0].view(np.uint32), out[1].view(np.uint32))
-
-
-def test_tiny_fused_ffn_equals_two_launches(kdlib, tiny):
-    """The FFN as one launch (KD_FLAG_FUSED_FFN, group schedule) against gate|up
-    and down launched one after the other: the same arithmetic and split of K,
-    so the same bits, over several steps that feed back their own tokens."""
-    kd = kdlib
-    shape, w = tiny
-    cap, steps, lens = 64, 4, [17, 40, 3]
-    tok0 = synth.tokens(0, "tiny-ffn", len(lens), shape.vocab)
-    out = []
-    for flags in (4, 12):
-        m = load(kd, shape, w, 4, cap, flags)
-        try:
-            ids = bind_prefilled(kd, m, shape, lens)
-            out.append(greedy_stream(kd, m, ids, lens, tok0, steps, shape.vocab))
-            assert kd.kd_device_status(m) == 0
-        finally:
-            kd.kd_model_free(m)
-    assert np.array_equal(out[0][0], out[1][0])
-    assert np.array_equal(out[0][1].view(np.uint32), out[1][1].view(np.uint32))
 
 
 def test_tiny_errors_change_no_state(kdlib, tiny):
