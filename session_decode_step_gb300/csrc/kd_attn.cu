@@ -43,9 +43,9 @@ struct AttnSmem {
     static constexpr int K_BYTES = NREG * HALF_BYTES;
     static constexpr int STAGE = 2 * K_BYTES;               // K tile, V tile
     static constexpr int STAGES = 192 * 1024 / STAGE;       // 6 at hd 128, 12 at hd 64
-    static constexpr int BAR_OFF = STAGES * STAGE;
-    static constexpr int ITEM_OFF = BAR_OFF + STAGES * 8;
-    static constexpr int TOTAL = ITEM_OFF + STAGES * 4 + 16 + 1024;  // + flag, alignment slack
+    static constexpr int BAR_OFF = STAGES * STAGE;           // per stage a K barrier, then per stage a V barrier
+    static constexpr int ITEM_OFF = BAR_OFF + 2 * STAGES * 8;  // the same for the item words
+    static constexpr int TOTAL = ITEM_OFF + 2 * STAGES * 4 + 16 + 1024;  // + flag, alignment slack
     static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
     // byte offset of (row, 16-byte chunk along the head dim) inside a tile
     static __device__ __forceinline__ uint32_t off(int row, int chunk) {
@@ -154,12 +154,14 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     uint8_t* smem = align1024(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
+    // Stage st's K tile lands on bar[st] and its V tile on bar[S + st]; item
+    // words likewise (the last item whose K, resp. V, copy was issued there).
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     volatile int* stage_item = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
-    volatile int* cta_failed = stage_item + S;
+    volatile int* cta_failed = stage_item + 2 * S;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
+        for (int i = 0; i < 2 * S; ++i) {
             mbar_init(&bar[i], 1);
             stage_item[i] = -1;
         }
@@ -173,27 +175,28 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     const int n_items = tab.n_items;
     const int nk = (int)blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto gitem = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
-    // Issue the copies of the CTA's item k into stage k % S (lane 0).
-    auto issue = [&](const AttnItem& it, int k) {
+    // Issue the copies of the CTA's item k into stage k % S (lane 0): its K tile
+    // (parts & 1) and/or its V tile (parts & 2), each on its own barrier.
+    auto issue = [&](const AttnItem& it, int k, int parts) {
         const int st = k % S;
         uint8_t* stg = smem + st * L::STAGE;
         const int row = (int)(a.row0 + ((long)it.slot * a.nkv + it.kvh) * a.cap + (long)it.s * AT_C);
         const bool full = it.n == AT_C;
         const int krows = full ? AT_C : (it.n + 7) / 8 * 8;
-        uint64_t* b = &bar[st];
-        stage_item[st] = k;
-        mbar_arrive_expect_tx(b, (uint32_t)(2 * L::NREG * krows * 128));
-        for (int r = 0; r < L::NREG; ++r) {
-            uint8_t* kdst = stg + r * L::HALF_BYTES;
-            uint8_t* vdst = kdst + L::K_BYTES;
-            if (full) {
-                tma_load_2d(kdst, &tmk, r * 64, row, b);
-                tma_load_2d(vdst, &tmv, r * 64, row, b);
-            } else {
-                for (int k8 = 0; k8 < krows; k8 += 8) {
-                    tma_load_2d(kdst + k8 * 128, &tmk8, r * 64, row + k8, b);
-                    tma_load_2d(vdst + k8 * 128, &tmv8, r * 64, row + k8, b);
-                }
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            if (!((parts >> part) & 1)) continue;
+            uint64_t* b = &bar[part * S + st];
+            const CUtensorMap* tm = part ? &tmv : &tmk;
+            const CUtensorMap* tm8 = part ? &tmv8 : &tmk8;
+            stage_item[part * S + st] = k;
+            mbar_arrive_expect_tx(b, (uint32_t)(L::NREG * krows * 128));
+            for (int r = 0; r < L::NREG; ++r) {
+                uint8_t* dst = stg + part * L::K_BYTES + r * L::HALF_BYTES;
+                if (full)
+                    tma_load_2d(dst, tm, r * 64, row, b);
+                else
+                    for (int k8 = 0; k8 < krows; k8 += 8) tma_load_2d(dst + k8 * 128, tm8, r * 64, row + k8, b);
             }
         }
     };
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS) {
         const AttnItem it = tab.item(a, lane, gitem(k));
         if (it.s != it.ns - 1) {
-            if (lane == 0) issue(it, k);
+            if (lane == 0) issue(it, k, 3);
             early |= 1u << i;
         }
     }
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS)
         if (!((early >> i) & 1u)) {
             const AttnItem it = tab.item(a, lane, gitem(k));
-            if (lane == 0) issue(it, k);
+            if (lane == 0) issue(it, k, 3);
         }
 
     // The MMAs' 8-wide N dimension: column 2h + part of N-tile j is head 4j + h,
@@ -262,8 +265,9 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
         }
         if (k + AT_WARPS < nk) load_q(tab.item(a, lane, gitem(k + AT_WARPS)));  // lands during this item
 
+        const uint32_t par = (uint32_t)(k / S) & 1u;
         bool ok = wait_value(stage_item + st, k);
-        ok = ok && mbar_wait_bounded(&bar[st], (uint32_t)(k / S) & 1u);
+        ok = ok && mbar_wait_bounded(&bar[st], par);  // the K tile
         if (__any_sync(FULL_MASK, !ok)) {
             if (lane == 0) {
                 atomicOr(a.err, ERR_WAIT_TIMEOUT);
@@ -272,17 +276,9 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             break;
         }
         const int n = it.n;
-        if (n < AT_C) {
-            // V rows [n, 16-key step end) enter the last P V step with p = 0: make
-            // them zero (they hold other positions or stale data, possibly NaN).
-            const int z = ((n + 15) & ~15) - n;
-            for (int e = lane; e < z * L::NREG * 8; e += 32) {
-                const int r = n + e / (L::NREG * 8), rem = e % (L::NREG * 8);
-                *reinterpret_cast<uint4*>(stg + L::K_BYTES + (rem >> 3) * L::HALF_BYTES + r * 128 + (rem & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-        }
+        const bool refill = k + S < nk;
+        AttnItem nx{};
+        if (refill) nx = tab.item(a, lane, gitem(k + S));
 
         // ---- S^T = K Q^T: M = 16 keys (AT_KT tiles), N = the head columns, K = 16 dims.
         // k-steps outside, key tiles inside: MMAs issued back to back go to
@@ -306,6 +302,12 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
 #pragma unroll
                 for (int m = 0; m < AT_KT; ++m)
                     mma_16816_acc(sacc[m][j], ka[m][0], ka[m][1], ka[m][2], ka[m][3], qb[j][ks][0], qb[j][ks][1]);
+        }
+        // The K tile is read: refill it with item k + S's, half an item before its V.
+        __syncwarp();
+        if (refill && lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(nx, k + S, 1);
         }
         // ---- per head 4j + c: scores of keys 16m + g (e = 0) and 16m + g + 8 (e = 1);
         // scale, mask, softmax over the item's keys (the 8 lanes g of a head)
@@ -335,6 +337,28 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
                 }
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) lsum[j] = __fadd_rn(lsum[j], __shfl_xor_sync(FULL_MASK, lsum[j], o));
+        }
+
+        // The V tile.
+        ok = wait_value(stage_item + S + st, k);
+        ok = ok && mbar_wait_bounded(&bar[S + st], par);
+        if (__any_sync(FULL_MASK, !ok)) {
+            if (lane == 0) {
+                atomicOr(a.err, ERR_WAIT_TIMEOUT);
+                *cta_failed = 1;
+            }
+            break;
+        }
+        if (n < AT_C) {
+            // V rows [n, 16-key step end) enter the last P V step with p = 0: make
+            // them zero (they hold other positions or stale data, possibly NaN).
+            const int z = ((n + 15) & ~15) - n;
+            for (int e = lane; e < z * L::NREG * 8; e += 32) {
+                const int r = n + e / (L::NREG * 8), rem = e % (L::NREG * 8);
+                *reinterpret_cast<uint4*>(stg + L::K_BYTES + (rem >> 3) * L::HALF_BYTES + r * 128 + (rem & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
         }
 
         // ---- O^T = V^T P^T: M = 16 dims (NU/2 tiles), N = the head columns, K = 16 keys,
@@ -392,22 +416,20 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             }
         }
 
-        __syncwarp();  // the stage is consumed: refill it
-        if (k + S < nk) {
-            const AttnItem nx = tab.item(a, lane, gitem(k + S));
-            if (lane == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(nx, k + S);
-            }
+        __syncwarp();  // the V tile is read: refill it
+        if (refill && lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(nx, k + S, 2);
         }
     }
     // After a wait gave up, copies may still be in flight: before the CTA's shared
-    // memory is released, wait (bounded) for the last item issued into each stage.
+    // memory is released, wait (bounded) for the last item issued into each K and
+    // each V tile.
     __syncthreads();
     if (threadIdx.x == 0 && *cta_failed)
-        for (int st = 0; st < S; ++st) {
-            const int k = stage_item[st];
-            if (k >= 0) (void)mbar_wait_bounded(&bar[st], (uint32_t)(k / S) & 1u);
+        for (int i = 0; i < 2 * S; ++i) {
+            const int k = stage_item[i];
+            if (k >= 0) (void)mbar_wait_bounded(&bar[i], (uint32_t)(k / S) & 1u);
         }
 }
 
