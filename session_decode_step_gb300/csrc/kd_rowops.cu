@@ -15,11 +15,9 @@ namespace kd {
 
 constexpr int EMBED_THREADS = 256;
 
-// out[i] = fp16(x[i] / sqrt(mean(x^2) + eps) * w[i]) for the row x[0..H) already
-// in global memory (written by this CTA); the sum of squares in a fixed order:
-// per-thread strided, a fixed shuffle tree, then warps in order.
-__device__ __forceinline__ void norm_row(const float* x, int H, const float* w, float eps, __half* out,
-                                         float ss_thread) {
+// 1 / sqrt(mean(x^2) + eps) of a row from each thread's share of its sum of
+// squares, added in a fixed order: a fixed shuffle tree, then warps in order.
+__device__ __forceinline__ float block_rms_factor(float ss_thread, int H, float eps) {
     __shared__ float wsum[EMBED_THREADS / 32];
     __shared__ float rsh;
     const int tid = threadIdx.x;
@@ -34,7 +32,16 @@ __device__ __forceinline__ void norm_row(const float* x, int H, const float* w, 
         rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), eps)));
     }
     __syncthreads();
-    const float r = rsh;
+    return rsh;
+}
+
+// out[i] = fp16(x[i] / sqrt(mean(x^2) + eps) * w[i]) for the row x[0..H) already
+// in global memory (written by this CTA); ss_thread: this thread's share of the
+// sum of squares (its elements tid, tid + 256, ... in order).
+__device__ __forceinline__ void norm_row(const float* x, int H, const float* w, float eps, __half* out,
+                                         float ss_thread) {
+    const int tid = threadIdx.x;
+    const float r = block_rms_factor(ss_thread, H, eps);
     constexpr int U = 16;  // loads issued together
     for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
         float xv[U], wv[U];
@@ -61,9 +68,48 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     const int b = blockIdx.x, tid = threadIdx.x;
-    const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
     float* xr = x + (size_t)b * H;
     constexpr int U = 16;  // elements per thread whose loads are issued together
+    if (H <= EMBED_THREADS * U) {
+        // The whole row in registers: the norm's weights load with the token's
+        // row, and the norm reads x from registers (the same arithmetic as below).
+        float wv[U], xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            wv[u] = i < H ? w[i] : 0.0f;
+        }
+        const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
+        int8_t q[U];
+        unsigned short dbits[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            const uint8_t* blk = row + (i >> 5) * 34;
+            q[u] = i < H ? (int8_t)blk[2 + (i & 31)] : (int8_t)0;
+            dbits[u] = i < H ? (unsigned short)(blk[0] | (blk[1] << 8)) : (unsigned short)0;
+        }
+        float s = 0.0f;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            const __half_raw hr{dbits[u]};
+            xv[u] = __fmul_rn((float)q[u], __half2float(__half(hr)));
+            if (i < H) {
+                xr[i] = xv[u];
+                s = __fmaf_rn(xv[u], xv[u], s);
+            }
+        }
+        const float r = block_rms_factor(s, H, eps);
+        __half* out = xn + (size_t)b * H;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            if (i < H) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(xv[u], r), wv[u]));
+        }
+        return;
+    }
+    const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
     float s = 0.0f;
     for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
         int8_t q[U];
