@@ -60,6 +60,21 @@ def kernels_per_step(s, with_argmax=True):
     return 1 + s.n_layers * 8 + 1 + (1 if with_argmax else 0)
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of the ranks' values, returned on every rank (the value itself for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tok_s(batch: int, steps: int, world: int, seconds: float) -> float:
+    """Tokens of all ranks (each rank decodes `batch` sessions for `steps` steps) over the slowest rank's time."""
+    return batch * steps * world / seconds
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -200,11 +215,7 @@ def run_kd(args, rank, world):
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         return ms, byts
 
     gpu_index = local
@@ -217,7 +228,7 @@ def run_kd(args, rank, world):
     with ClockSampler(gpu_index) as clk:
         ms, byts = timed(B, args.steps, args.warmup)
     status = kd.kd_device_status(m)
-    tok_s = B * args.steps * world / (ms / 1e3)
+    tok_s = whole_job_tok_s(B, args.steps, world, ms / 1e3)
     gbs = byts / (ms / 1e3) / 1e9
 
     # ---- end to end through the public API: host tokens in, host argmax out, every step
@@ -235,12 +246,8 @@ def run_kd(args, rank, world):
         host_out.copy_(am[:B], non_blocking=True)
         stream.synchronize()
         host_tok.copy_(host_out)  # greedy feedback through the host
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": round(B * e2e_steps * world / e2e_s, 2), "unit": "tok/s",
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": round(whole_job_tok_s(B, e2e_steps, world, e2e_s), 2), "unit": "tok/s",
            "h2d_bytes_per_step": 3 * 16 * 4, "d2h_bytes_per_step": B * 4, "steps": e2e_steps}
 
     # ---- per-kernel device times (events around every launch) for the roofline
@@ -285,7 +292,7 @@ def run_kd(args, rank, world):
         for b in (1, 2, 4, 8, 16):
             sm, sb = timed(b, max(16, min(args.steps, 128)), args.warmup)
             n = max(16, min(args.steps, 128))
-            sweep[str(b)] = {"tok_s": round(b * n * world / (sm / 1e3), 1),
+            sweep[str(b)] = {"tok_s": round(whole_job_tok_s(b, n, world, sm / 1e3), 1),
                              "hbm_gbs": round(sb / (sm / 1e3) / 1e9, 1),
                              "frac_of_peak": round(sb / (sm / 1e3) / 1e9 / peak, 4)}
     kd.kd_model_free(m)
