@@ -86,6 +86,47 @@ def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags):
         kd.kd_model_free(m)
 
 
+def test_tiny_first_position_and_last_slot_position(kdlib, tiny):
+    """The degenerate ends of a slot in one ragged batch, teacher-forced against
+    the oracle: a fresh session decoding from position 0 (one key, a single
+    split, the KV append at the slot's first row) beside a session that decodes
+    up to the slot's last position (cap - 1), where the next position is refused."""
+    kd = kdlib
+    shape, w = tiny
+    cap, steps = 64, 4
+    lens = [0, cap - steps]
+    m = load(kd, shape, w, 4, cap)
+    try:
+        fresh = kd.kd_session_bind(m)
+        (full,) = bind_prefilled(kd, m, shape, [lens[1]], first_session=1)
+        ids = [fresh, full]
+        om = oracle.OracleModel(shape, w)
+        caches = [om.new_cache(cap), om.new_cache(cap, *synth.kv_prefill(shape, 0, 1, lens[1]))]
+        B, L, H = 2, shape.n_layers, shape.hidden
+        hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+        kd.kd_debug_capture_hidden(m, hid)
+        tok = synth.tokens(0, "tiny-ends", B, shape.vocab)
+        for step in range(steps):
+            pos = [n + step for n in lens]
+            lg, _ = gpu_step(kd, m, ids, tok, pos, shape.vocab)
+            ref, ref_am, ref_h = om.step(tok, pos, caches, cap, want_hidden=True)
+            assert np.abs(lg - ref).max() <= LOGIT_TOL, (step, float(np.abs(lg - ref).max()))
+            gh = hid.cpu().numpy()
+            for b in range(B):
+                for l in range(L + 1):
+                    rel = np.linalg.norm(gh[l, b] - ref_h[b, l]) / np.linalg.norm(ref_h[b, l])
+                    assert rel <= HIDDEN_REL_L2, (step, b, l, rel)
+            tok = ref_am
+        assert kd.kd_session_length(m, full) == cap
+        kd.kd_debug_capture_hidden(m, None)
+        with pytest.raises(kd.KdError) as e:  # the slot is full
+            kd.kd_decode_step(m, [full], tok[1:], np.array([cap], np.int32), None, None)
+        assert e.value.name == "KD_ERR_POSITION"
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
 def greedy_stream(kd, m, ids, lens, tok0, steps, V):
     tok = np.array(tok0, np.int32)
     toks, logits = [], []
