@@ -452,14 +452,14 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     if (b >= a.B) return;
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
-    // The first records' loads do not wait for the split count: they are bounded
-    // by the buffer's split capacity and go out together with the position's load.
+    // Only the session's own split records are read: records past its split count
+    // may be cold (never written), and the first round waits for its slowest load.
+    const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
     float o[COMB_BATCH];
 #pragma unroll
-    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < a.max_splits ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
-    const float2 ml0 = d < a.max_splits ? __ldcg(reinterpret_cast<const float2*>(p + (size_t)d * ATT_REC(HD) + HD))
-                                        : make_float2(0.0f, 0.0f);
-    const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
+    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < ns ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
+    const float2 ml0 = d < ns ? __ldcg(reinterpret_cast<const float2*>(p + (size_t)d * ATT_REC(HD) + HD))
+                              : make_float2(0.0f, 0.0f);
     float mloc = -INFINITY;
     for (int s = d; s < ns; s += HD) {
         const float2 ml = s == d ? ml0 : __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
