@@ -204,6 +204,12 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     // The first S items fill the ring.  History rows (keys < pos) were written by
     // earlier steps: items that do not hold this step's new row are fetched before
     // waiting on the QKV kernel.
+    if (threadIdx.x == 0) {  // the ragged-tail maps are often first used after the wait
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        prefetch_tmap(&tmk8);
+        prefetch_tmap(&tmv8);
+    }
     unsigned early = 0;
     for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS) {
         const AttnItem it = tab.item(a, lane, gitem(k));

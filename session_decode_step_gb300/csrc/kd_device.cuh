@@ -90,6 +90,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// Fetch a tensor map's descriptor ahead of its first copy (the map itself never
+// depends on an earlier kernel, so this can run before the dependency wait).
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // The first 1024-byte boundary at or after p (tiles written with the 128-byte
 // swizzle need it; dynamic shared memory is only guaranteed 16-byte alignment).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

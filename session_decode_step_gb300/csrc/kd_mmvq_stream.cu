@@ -102,11 +102,13 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     // The weights do not depend on earlier kernels: start streaming them before
     // waiting for the producer of the activations.  Each barrier expects the
     // stage's weights and activations; the activations follow after the wait.
-    if (lane == 0)
+    if (lane == 0) {
         for (int i = 0; i < RD && i < n; ++i) {
             mbar_arrive_expect_tx(&bar[i], SB);
             bulk_g2s_hint(ring + i * STAGE_BYTES, wsrc + (size_t)i * STAGE_BYTES, STAGE_BYTES, &bar[i], policy);
         }
+        prefetch_tmap(&xm);
+    }
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
 
