@@ -454,13 +454,16 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __shared__ float wts[COMB_MAX_SPLITS], ls[COMB_MAX_SPLITS];
     __shared__ float red_m[HD / 32], red_l[HD / 32];
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
-    pdl_wait();
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    // The step's positions were staged before its first kernel: read while the
+    // split kernel finishes.
+    const int pos_b = b < a.B ? a.pos[b] : 0;
+    pdl_wait();
     if (b >= a.B) return;
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
     // Only the session's own split records are read: records past its split count
     // may be cold (never written), and the first round waits for its slowest load.
-    const int ns = (a.pos[b] + ATT_CHUNK) / ATT_CHUNK;
+    const int ns = (pos_b + ATT_CHUNK) / ATT_CHUNK;
     float o[COMB_BATCH];
 #pragma unroll
     for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < ns ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
