@@ -10,9 +10,9 @@
 // the session's own length only -- the result does not depend on what else is
 // in the batch.  A persistent CTA per SM walks its items through a ring of
 // shared-memory stages, filled by tensor-map copies of the split's K and V rows
-// with the 128-byte swizzle; each item is computed by one warp.  Per item: the GQA group's scores and
-// the weighted V sum as tensor-core products, a local softmax (max m, sum l) in
-// between, written as (o, m, l).  A second kernel merges a session-head's
+// with the 128-byte swizzle; each item is computed by one warp.  Per item: the
+// GQA group's scores and the weighted V sum as tensor-core products, a local
+// softmax (max m, sum l) in between, written as (o, m, l).  A second kernel merges a session-head's
 // splits in split order (online-softmax combine).
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -131,9 +131,10 @@ __device__ __forceinline__ bool wait_value(const volatile int* p, int v) {
 
 // A CTA takes the items blockIdx.x + k * gridDim.x, k = 0, 1, ...: item k goes
 // through stage k % STAGES and is computed by warp k % AT_WARPS, which then
-// refills that stage with item k + STAGES.  A consumer first waits until the
-// stage's item word says k (the copy of item k was issued, so the stage's
-// barrier is in item k's phase), then for the barrier.  The scores S = Q K^T
+// refills that stage with item k + STAGES: the K tile right after its scores,
+// the V tile after its output.  For each tile a consumer first waits until the
+// tile's item word says k (the copy of item k was issued, so the tile's barrier
+// is in item k's phase), then for the barrier.  The scores S = Q K^T
 // and the output O = P V are m16n8k16 tensor-core products taken transposed
 // (S^T = K Q^T, O^T = V^T P^T): the 16 MMA rows are keys, then head dims, with
 // no padding; the 8 columns are the GQA group's heads, each as q (then p)
