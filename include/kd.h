@@ -207,6 +207,20 @@ kd_status kd_q8_matrix_free(kd_q8_matrix* w);
 kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
                   kd_stream stream);
 
+/* The schedule the library picks for a Q8_0 matrix of rows x cols on a GPU with
+ * num_sms SMs (host only: no CUDA call, usable without a GPU).  It depends on the
+ * shape and the SM count only, never on the batch, so a row's arithmetic is the
+ * same at every m.  *mode_out: 1 = group (a CTA owns whole 32-row groups and its
+ * 8 warps split K), chosen when the groups number at most twice the SMs, or at
+ * most 8 times the SMs with the busiest SM's share at most 5% above the average;
+ * 0 = stream (warps stream equal contiguous shares of the matrix's 128-column
+ * stages).  *warps_out: the streaming warps (min(8 * num_sms, stages)); *share_out:
+ * the most stream warps meeting in one row group (1 on the group schedule).
+ * rows a multiple of 32, cols of 128, num_sms >= 1: else KD_ERR_UNSUPPORTED /
+ * KD_ERR_INVALID_ARG. */
+kd_status kd_mmvq_schedule(int32_t rows, int32_t cols, int32_t num_sms, int32_t* mode_out,
+                           int32_t* warps_out, int32_t* share_out);
+
 /* Greedy pick over logit rows, as the step's argmax (memra decode_batch.rs
  * `decode_batch_epilogue`, a device argmax equal to the host one):
  *   out[b] = the index of the largest logits[b][v]; equal values go to the

@@ -79,6 +79,7 @@ def lib():
             "kd_q8_matrix_free": [_vp],
             "kd_mmvq": [_vp, _vp, i32, _vp, _vp],
             "kd_argmax": [_vp, i32, i32, _vp, _vp, _vp],
+            "kd_mmvq_schedule": [i32, i32, i32, i32p, i32p, i32p],
             "kd_attn_append_decode": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                       i32, _vp, _vp, C.c_size_t, _vp],
             "kd_attn_append_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
@@ -266,6 +267,14 @@ def kd_mmvq(w, x, m: int, y, stream=None):
 
 
 KD_ARGMAX_WORKSPACE_BYTES = 256
+
+
+def kd_mmvq_schedule(rows: int, cols: int, num_sms: int):
+    """(mode, warps, share) the library picks for a rows x cols Q8_0 matrix on num_sms SMs
+    (host only): mode 1 = group, 0 = stream."""
+    mode, warps, share = C.c_int32(), C.c_int32(), C.c_int32()
+    _check(lib().kd_mmvq_schedule(int(rows), int(cols), int(num_sms), C.byref(mode), C.byref(warps), C.byref(share)))
+    return mode.value, warps.value, share.value
 
 
 def kd_argmax(logits, B: int, V: int, out, workspace, stream=None):

@@ -785,6 +785,25 @@ kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
     return KD_OK;
 }
 
+kd_status kd_mmvq_schedule(int32_t rows, int32_t cols, int32_t num_sms, int32_t* mode_out, int32_t* warps_out,
+                           int32_t* share_out) {
+    if (!mode_out || !warps_out || !share_out) return fail(KD_ERR_INVALID_ARG, "kd_mmvq_schedule: null argument");
+    if (num_sms < 1) return fail(KD_ERR_INVALID_ARG, "kd_mmvq_schedule: num_sms=%d", num_sms);
+    if (rows < kd::GROUP_ROWS || rows % kd::GROUP_ROWS || cols < kd::KGROUP || cols % kd::KGROUP)
+        return fail(KD_ERR_UNSUPPORTED, "kd_mmvq_schedule: need rows %% 32 == 0 and cols %% 128 == 0 (got %d x %d)",
+                    rows, cols);
+    PackedQ8 p;
+    p.rows = rows;
+    p.K = cols;
+    p.G = rows / kd::GROUP_ROWS;
+    p.KG = cols / kd::KGROUP;
+    kd::plan_split(p, num_sms);
+    *mode_out = p.mode;
+    *warps_out = p.W;
+    *share_out = p.mode == kd::MMVQ_STREAM ? p.maxc : 1;
+    return KD_OK;
+}
+
 kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, void* workspace, kd_stream stream) {
     if (!logits || !out || !workspace) return fail(KD_ERR_INVALID_ARG, "kd_argmax: null argument");
     if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_argmax: B=%d outside [1, %d]", B, KD_MAX_BATCH);
