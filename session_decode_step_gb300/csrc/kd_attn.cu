@@ -177,7 +177,10 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     const int nk = (int)blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto gitem = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
     // Issue the copies of the CTA's item k into stage k % S (lane 0): its K tile
-    // (parts & 1) and/or its V tile (parts & 2), each on its own barrier.
+    // (parts & 1) and/or its V tile (parts & 2), each on its own barrier.  Cached
+    // keys and values are read once per step: their lines go first when L2 needs
+    // room, ahead of the step's small, often re-read activation buffers.
+    const uint64_t kv_policy = l2_policy_evict_first();
     auto issue = [&](const AttnItem& it, int k, int parts) {
         const int st = k % S;
         uint8_t* stg = smem + st * L::STAGE;
@@ -195,9 +198,10 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             for (int r = 0; r < L::NREG; ++r) {
                 uint8_t* dst = stg + part * L::K_BYTES + r * L::HALF_BYTES;
                 if (full)
-                    tma_load_2d(dst, tm, r * 64, row, b);
+                    tma_load_2d_hint(dst, tm, r * 64, row, b, kv_policy);
                 else
-                    for (int k8 = 0; k8 < krows; k8 += 8) tma_load_2d(dst + k8 * 128, tm8, r * 64, row + k8, b);
+                    for (int k8 = 0; k8 < krows; k8 += 8)
+                        tma_load_2d_hint(dst + k8 * 128, tm8, r * 64, row + k8, b, kv_policy);
             }
         }
     };
