@@ -331,8 +331,8 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
 }
 
 // The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
-// With only_layer >= 0: that layer alone, on residual rows already in m->x whose
-// full-row sums of squares are in m->ssq (one group); no embedding, no head.
+// With only_layer >= 0: that layer alone, on residual rows already in m->x and
+// their normed rows in m->xn; no embedding, no head.
 static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1) {
     const kd_config& c = m->cfg;
     const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
