@@ -70,6 +70,16 @@ KDO_EXPORT uint16_t kdo_double_to_half(double x) {
 }
 
 static double round_half(double x) { return kdo_half_to_double(kdo_double_to_half(x)); }
+
+/* The same decoding as a table over all 65536 bit patterns, filled from
+ * kdo_half_to_double when the library loads: identical values, one load per
+ * cached K/V element instead of a call (the attention reads tens of millions
+ * of them per long-context step). */
+static double g_half_table[65536];
+__attribute__((constructor)) static void fill_half_table(void) {
+    for (uint32_t h = 0; h < 65536; ++h) g_half_table[h] = kdo_half_to_double((uint16_t)h);
+}
+static inline double half_value(uint16_t h) { return g_half_table[h]; }
 static double round_float(double x) { return (double)(float)x; }
 
 /* ---------------------------------------------------------------------------
@@ -148,17 +158,19 @@ KDO_EXPORT void kdo_attention_head(const double* q, const uint16_t* K, const uin
     double m = -INFINITY;
     for (int t = 0; t < t_kv; ++t) {
         double dot = 0.0;
-        for (int i = 0; i < hd; ++i) dot += q[i] * kdo_half_to_double(K[(size_t)t * stride + i]);
+        for (int i = 0; i < hd; ++i) dot += q[i] * half_value(K[(size_t)t * stride + i]);
         s[t] = dot * scale;
         if (s[t] > m) m = s[t];
     }
     double l = 0.0;
     for (int t = 0; t < t_kv; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
-    for (int i = 0; i < hd; ++i) {
-        double acc = 0.0;
-        for (int t = 0; t < t_kv; ++t) acc += s[t] * kdo_half_to_double(V[(size_t)t * stride + i]);
-        out[i] = acc / l;
-    }
+    /* a_i = sum over t in order of s_t V_t,i (row by row through V; each
+     * dimension's sum still runs over t = 0, 1, ... in order) */
+    double* acc = (double*)calloc((size_t)hd, sizeof(double));
+    for (int t = 0; t < t_kv; ++t)
+        for (int i = 0; i < hd; ++i) acc[i] += s[t] * half_value(V[(size_t)t * stride + i]);
+    for (int i = 0; i < hd; ++i) out[i] = acc[i] / l;
+    free(acc);
     free(s);
 }
 
