@@ -297,10 +297,13 @@ def run_kd(args, rank, world):
                              "frac_of_peak": round(sb / (sm / 1e3) / 1e9 / peak, 4)}
     kd.kd_model_free(m)
 
+    workloads = None
+    if rank == 0 and args.workloads:
+        workloads = other_workloads(args.steps, args.warmup, w if synth.LONG_CTX_8B_CASE["seed"] == 0 else None)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, w, B)
-    return dict(value=tok_s, ms=ms, gbs=gbs, e2e=e2e, roofline=roofline, sweep=sweep, cpu=cpu,
+    return dict(value=tok_s, ms=ms, gbs=gbs, e2e=e2e, roofline=roofline, sweep=sweep, cpu=cpu, workloads=workloads,
                 clocks=clk.summary(), peak=peak, peak_kind=peak_kind, status=status, shares=kernel_share,
                 launches_per_step=launches_per_step)
 
@@ -322,19 +325,15 @@ def cpu_baseline(shape, w, B):
 
 
 # --------------------------------------------------------------- op-level modes
-def run_op_mmvq(args):
-    """Isolated Q8_0 mmvq (rows x cols weights, m fp16 activation rows ~N(0,1)).
+def time_mmvq(R, K, m, steps, warmup):
+    """Isolated Q8_0 mmvq (R x K weights, m fp16 activation rows ~N(0,1)).
     Distinct weight copies totalling more than 4x L2 are rotated, so every launch
     streams its weights from HBM."""
     import torch
 
     import session_decode_step_gb300 as kd
-    from session_decode_step_gb300 import build as kbuild
-    kbuild.build()
-    torch.cuda.set_device(0)
-    R, K, m = args.rows, args.cols, args.m
     wbytes = R * K * 34 // 32
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     copies = max(2, -(-4 * l2 // wbytes))
     base = synth.q8_0_matrix(0, f"op-{R}x{K}", R, K)
     hs = []
@@ -345,77 +344,95 @@ def run_op_mmvq(args):
     x = torch.from_numpy(synth.activations_fp16(0, "op-x", m, K).view(np.int16)).cuda()
     y = torch.empty(m, R, device="cuda", dtype=torch.float32)
     st = torch.cuda.current_stream()
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, warmup)):
         kd.kd_mmvq(hs[i % copies], x, m, y, st)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    for i in range(args.steps):
+    for i in range(steps):
         kd.kd_mmvq(hs[i % copies], x, m, y, st)
     e1.record(st)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    us = e0.elapsed_time(e1) * 1e3 / steps
     alg = wbytes + m * K * 2 + m * R * 4
     peak, kind = read_peaks()
+    status = max(kd.kd_q8_matrix_status(h) for h in hs)
     for h in hs:
         kd.kd_q8_matrix_free(h)
-    return {"op": "mmvq", "rows": R, "cols": K, "m": m, "copies": copies, "launches": args.steps,
+    return {"rows": R, "cols": K, "m": m, "copies": copies, "launches": steps,
             "avg_us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1), "peak": peak,
-            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4)}
+            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4), "device_status": status}
 
 
-def run_op_attn(args):
+def run_op_mmvq(args):
+    import torch
+
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    return dict(op="mmvq", **time_mmvq(args.rows, args.cols, args.m, args.steps, args.warmup))
+
+
+def time_attn(B, cap, steps, warmup):
     """Isolated KV append + ragged split-K flash-decode: 32/8 heads of 128, B sessions with
     attended lengths uniform in [1, cap] (seeded), fp16 KV ~N(0,1)."""
     import torch
 
     import session_decode_step_gb300 as kd
-    from session_decode_step_gb300 import build as kbuild
-    kbuild.build()
-    torch.cuda.set_device(0)
     c = synth.RAGGED_ATTN_CASE
-    nh, nkv, hd, cap, B = c["n_heads"], c["n_kv_heads"], c["head_dim"], args.cap, args.m
+    nh, nkv, hd = c["n_heads"], c["n_kv_heads"], c["head_dim"]
     lens = synth.ragged_lengths(0, "attn-config", B, 1, cap)
-    kc = torch.randn(B, nkv, cap, hd, device="cuda", dtype=torch.float32).to(torch.float16)
-    vc = torch.randn(B, nkv, cap, hd, device="cuda", dtype=torch.float32).to(torch.float16)
-    q = torch.randn(B, nh, hd, device="cuda")
-    kn = torch.randn(B, nkv, hd, device="cuda")
-    vn = torch.randn(B, nkv, hd, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    kc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
+    vc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
+    q = torch.randn(B, nh, hd, device="cuda", generator=g)
+    kn = torch.randn(B, nkv, hd, device="cuda", generator=g)
+    vn = torch.randn(B, nkv, hd, device="cuda", generator=g)
     out = torch.empty(B, nh * hd, dtype=torch.float16, device="cuda")
     ws = torch.empty(kd.kd_attn_workspace_bytes(B, nh, hd, cap), dtype=torch.uint8, device="cuda")
     slots = np.arange(B, dtype=np.int32)
     pos = (lens - 1).astype(np.int32)
     st = torch.cuda.current_stream()
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    for _ in range(args.steps):
+    for _ in range(steps):
         kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
     e1.record(st)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    us = e0.elapsed_time(e1) * 1e3 / steps
     alg = int(lens.sum()) * nkv * hd * 2 * 2 + B * nkv * hd * 2 * 2
     peak, kind = read_peaks()
-    return {"op": "attn_append_decode", "B": B, "cap": cap, "sum_t_kv": int(lens.sum()), "launches": args.steps,
+    status = kd.kd_attn_device_status(ws, st)
+    return {"B": B, "cap": cap, "sum_t_kv": int(lens.sum()), "launches": steps,
             "avg_us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1), "peak": peak,
-            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4)}
+            "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4), "device_status": status,
+            "note": "per call: host-staged descriptor copy, append, split kernel, combine"}
 
 
-def run_op_long(args):
+def run_op_attn(args):
+    import torch
+
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    return dict(op="attn_append_decode", **time_attn(args.m, args.cap, args.steps, args.warmup))
+
+
+def time_long(steps, warmup, w=None):
     """The long-context multi-tenant workload: 8 sessions in 32768-position slots, pre-filled to
     25704 + 1000 i (i = 0..7) fp16 positions, each step at its own position (64 positions cycling)."""
     import torch
 
     import session_decode_step_gb300 as kd
-    from session_decode_step_gb300 import build as kbuild
-    kbuild.build()
-    torch.cuda.set_device(0)
     c = synth.LONG_CTX_8B_CASE
     shape, S, cap, win = c["shape"], c["sessions"], c["capacity"], c["steps"]
     lens = [c["prefill_base"] + c["prefill_stagger"] * i for i in range(S)]
-    w = synth.model_weights(shape, seed=c["seed"])
+    if w is None:
+        w = synth.model_weights(shape, seed=c["seed"])
     m = kd.kd_model_load(kd.make_config(shape, max_sessions=S, max_ctx=cap), w)
     ids = []
     for i, n in enumerate(lens):
@@ -432,27 +449,47 @@ def run_op_long(args):
     def pos(i):
         return np.array([n + (i % win) for n in lens], np.int32)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, warmup)):
         kd.kd_decode_step(m, ids, tok, pos(i), None, am, st)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     byts = 0
     e0.record(st)
-    for i in range(args.steps):
+    for i in range(steps):
         p = pos(i)
         kd.kd_decode_step(m, ids, tok, p, None, am, st)
         byts += step_bytes(shape, p)
     e1.record(st)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     peak, kind = read_peaks()
     status = kd.kd_device_status(m)
     kd.kd_model_free(m)
-    return {"op": "long_context_step", "B": S, "capacity": cap, "positions": f"{lens[0]}..{lens[-1] + win - 1}",
-            "steps": args.steps, "ms_per_step": round(ms, 4), "tok_s": round(S / (ms / 1e3), 1),
-            "alg_bytes_per_step": int(byts / args.steps), "gbs": round(byts / args.steps / (ms / 1e3) / 1e9, 1),
-            "peak": peak, "peak_source": kind, "frac": round(byts / args.steps / (ms / 1e3) / 1e9 / peak, 4),
+    return {"B": S, "capacity": cap, "positions": f"{lens[0]}..{lens[-1] + win - 1}",
+            "steps": steps, "ms_per_step": round(ms, 4), "tok_s": round(S / (ms / 1e3), 1),
+            "alg_bytes_per_step": int(byts / steps), "gbs": round(byts / steps / (ms / 1e3) / 1e9, 1),
+            "peak": peak, "peak_source": kind, "frac": round(byts / steps / (ms / 1e3) / 1e9 / peak, 4),
             "device_status": status}
+
+
+def run_op_long(args):
+    import torch
+
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    return dict(op="long_context_step", **time_long(args.steps, args.warmup))
+
+
+def other_workloads(steps, warmup, w):
+    """The workloads other than the headline one, measured in the same run: the
+    long-context step, the isolated mmvq at every m, the isolated ragged attention."""
+    c2, c3 = synth.MMVQ_CASE, synth.RAGGED_ATTN_CASE
+    out = {"long_context": time_long(max(16, min(steps, synth.LONG_CTX_8B_CASE["steps"])), warmup, w)}
+    out["isolated_mmvq"] = [time_mmvq(R, K, m, max(50, min(steps, 200)), warmup)
+                            for R, K in c2["matrices"] for m in c2["rows_m"]]
+    out["isolated_attention"] = time_attn(c3["sessions"], c3["max_ctx"], max(50, min(steps, 200)), warmup)
+    return out
 
 
 # ------------------------------------------------------------------ reference arm
@@ -505,6 +542,8 @@ def main():
     ap.add_argument("--impl", default="kd", choices=["kd", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the long-context, isolated-mmvq and isolated-attention measurements")
     ap.add_argument("--op", choices=["mmvq", "attn", "long"],
                     help="time one kernel family in isolation, or the long-context step")
     ap.add_argument("--rows", type=int, default=4096)
@@ -549,6 +588,7 @@ def main():
             "cpu_baseline": r["cpu"], "clocks": r["clocks"],
             "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
             "kernel_time_share": r["shares"], "device_status": r["status"],
+            "workloads": r["workloads"],
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -101,10 +101,23 @@ typedef struct {
 
 /* Copy and repack the weights into device memory and allocate the KV arena
  * (2 * n_layers * max_sessions * n_kv_heads * max_ctx * head_dim fp16) and the
- * step workspaces.  Synchronous.  On success *out owns all of it. */
+ * step workspaces.  Synchronous.  On success *out owns all of it.
+ * The model is the state every step shares: memra decode_batch.rs
+ * `decode_step_batch(&self, e, tokens, caches)` reads one set of weights for
+ * all B rows (module header: the weights are streamed once per step), while
+ * each session's KV lives apart from them.  The arena is a fixed number of
+ * slots of a fixed capacity each, as in hf2q ADR-040 section 0.0 ("Full-context
+ * slot correction": `--max-slots` slots, each with the whole configured
+ * context; weights and compute scratch kept apart from the slots' KV).
+ * Errors: KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED for a bad or unsupported
+ * shape (checked before any CUDA call), KD_ERR_OOM if device or pinned memory
+ * runs out, KD_ERR_CUDA otherwise; nothing is left allocated on failure. */
 kd_status kd_model_load(const kd_config* cfg, const kd_weights* w, kd_model** out);
 
-/* Wait for the model's outstanding work, then free everything it owns. */
+/* Wait for the model's outstanding work, then free everything it owns: the
+ * teardown matching kd_model_load (the pages' engines release the weights and
+ * the slots with the engine; hf2q ADR-040 section 0.0, weights and slot KV are
+ * separate budgets owned by the worker).  The handle is invalid afterwards. */
 kd_status kd_model_free(kd_model* m);
 
 /* Claim a free slot (lowest free id) for a new session of length 0.
@@ -113,17 +126,33 @@ kd_status kd_model_free(kd_model* m);
 kd_status kd_session_bind(kd_model* m, int32_t* session_id_out);
 
 /* Release a session's slot.  Waits on the host for the last step that used the
- * model, so a freed slot is never rebound while a step may still write it. */
+ * model, so a freed slot is never rebound while a step may still write it.
+ * hf2q ADR-040 section 0.0 ("Agent-slot lifetime"): a slot is a retained
+ * cache; a new conversation reuses an idle slot and invalidates its old state
+ * first -- here a freed slot is bound again at length 0.
+ * Errors: KD_ERR_BAD_SESSION if the id is not bound. */
 kd_status kd_session_free(kd_model* m, int32_t session_id);
 
 /* Fill a bound session's cache with `len` positions (its prompt history):
  * k_fp16 and v_fp16 are [n_layers][n_kv_heads][len][head_dim] fp16, host or
  * device memory (any address CUDA can copy from).  Sets the length to len.
- * Enqueued on `stream`; the source must stay valid until the stream reaches it. */
+ * Enqueued on `stream`; the source must stay valid until the stream reaches it.
+ * A session's state is its own position and KV: in memra decode_batch.rs
+ * `decode_step_batch`, row b carries a cache of its own holding its position
+ * and its quantized KV;
+ * Kakeya PR-A3c binds each batch row to a session with its own KV-cache row,
+ * filled with its ~1238-token context before batched decode.  Loading a slot
+ * also restores a retained history (hf2q ADR-040 section 0.0, "Agent-slot
+ * lifetime": a continuation reuses its slot's KV instead of re-prefilling).
+ * Errors: KD_ERR_BAD_SESSION (not bound), KD_ERR_POSITION (len outside
+ * [0, max_ctx]), KD_ERR_INVALID_ARG (null cache with len > 0). */
 kd_status kd_session_load_kv(kd_model* m, int32_t session_id, const void* k_fp16,
                              const void* v_fp16, int32_t len, kd_stream stream);
 
-/* The number of positions a bound session holds. */
+/* The number of positions a bound session holds: memra's `cache.pos`, which a
+ * batched step moves forward by one for every row, as a single-sequence step
+ * would (decode_batch.rs `decode_step_batch`); here it becomes the step's
+ * position + 1.  Host only, no CUDA call.  Errors: KD_ERR_BAD_SESSION. */
 kd_status kd_session_length(const kd_model* m, int32_t session_id, int32_t* len_out);
 
 /* One batched decode step (memra decode_batch.rs `decode_step_batch`: row b is
@@ -146,7 +175,13 @@ kd_status kd_decode_step(kd_model* m, const int32_t* session_ids, const int32_t*
 
 /* Debug: when dev_buf is not NULL, later steps also write the residual stream
  * after the embedding and after every layer to dev_buf, device fp32
- * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off. */
+ * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off.
+ * The residual stream is the fp32 `x` of memra decode_batch.rs
+ * `decode_batch_layers` (a `CudaSlice<f32>` carried from layer to layer); the
+ * capture exposes it per layer so that a batched step can be compared layer by
+ * layer with a reference, the way hf2q ADR-040 narrowed its N = 8 divergence
+ * down to one operation (section 0.13, post-audit finding).  The buffer is
+ * caller-owned and must hold B rows of the steps that run while it is set. */
 kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf);
 
 /* Debug: run decoder layer `layer` alone on the residual rows x_in (device or
@@ -162,8 +197,21 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* session_ids,
 
 /* Wait for the model's work, then read and clear its device fault word.
  * *flags_out = 0 when no kernel gave up a bounded wait; KD_ERR_DEVICE is
- * returned when one did. */
+ * returned when one did (the outputs of that step are not valid; the model's
+ * internal arrival counters are cleared as well, so the next step is correct).
+ * memra returns an error for the request rather than stopping the process
+ * (decode_batch.rs: every step returns a `Result`). */
 kd_status kd_device_status(kd_model* m, int32_t* flags_out);
+
+/* Debug fault hook, for testing kd_device_status: the next kd_decode_step
+ * launches kernel by kernel, and the first launch of kernel class
+ * `kernel_class` (one with bounded waits: KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_WO,
+ * KD_K_GATE_UP, KD_K_DOWN or KD_K_LM_HEAD) has one barrier expect a few bytes
+ * more than its copies deliver.  Every copy still lands; the wait on that
+ * barrier runs out after its time limit (about half a second), the kernel sets
+ * the fault word and returns, and the step's outputs are invalid.  Nothing
+ * faults or hangs.  One-shot.  Errors: KD_ERR_INVALID_ARG for another class. */
+kd_status kd_debug_inject_wait_timeout(kd_model* m, int32_t kernel_class);
 
 /* Measurement (the event-based counterpart of memra's per-phase breakdown,
  * decode_batch.rs BATCH_PHASE, without its host syncs).  While enabled, steps
@@ -181,7 +229,26 @@ kd_status kd_profile_enable(kd_model* m, int32_t on);
 kd_status kd_profile_read(kd_model* m, int32_t* launches /* [KD_K_COUNT] */,
                           double* ms /* [KD_K_COUNT] */);
 
-/* The message of the last failure on the calling thread ("" if none). */
+/* Measurement: a per-CTA timeline of later steps, in the pipelined step as it
+ * runs (CUDA graph and programmatic dependent launch kept; one graph per
+ * buffer).  While dev_buf is set, launch i of a step (i < max_launches) stamps
+ * in dev_buf[i][cta][0..3] (device uint64 [max_launches][KD_TIMELINE_CTAS][4],
+ * cta = blockIdx.y * gridDim.x + blockIdx.x < KD_TIMELINE_CTAS) the GPU global
+ * timer in ns when the CTA started, when its dependency wait returned and when
+ * its last warp ended, and its SM id.  Records a launch does not use are not
+ * written: zero the buffer first.  Each step overwrites the records.  When
+ * classes_out (host int32 [max_launches]) is not NULL it receives the kernel
+ * class (KD_K_*) of each launch index of a full step (-1 past its end).  NULL
+ * dev_buf turns it off.  The counterpart of memra's per-phase breakdown
+ * (decode_batch.rs BATCH_PHASE) without its stream syncs. */
+#define KD_TIMELINE_CTAS 1024
+kd_status kd_profile_timeline(kd_model* m, uint64_t* dev_buf, int32_t max_launches, int32_t* classes_out);
+
+/* The message of the last failure on the calling thread ("" if none).  The C
+ * counterpart of the error value memra's batched calls return with their
+ * `Result<_, Box<dyn Error>>` (decode_batch.rs `decode_step_batch`): a status
+ * code says which kind of failure, this string says what failed.  Owned by the
+ * library; valid until the thread's next failing call. */
 const char* kd_last_error(void);
 
 /* ------------------------------------------------------------------------
@@ -206,6 +273,11 @@ kd_status kd_q8_matrix_free(kd_q8_matrix* w);
  * (they share its workspace). */
 kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
                   kd_stream stream);
+
+/* Wait for the whole device, then read and clear the fault word of the
+ * matrix's kd_mmvq calls (0: no bounded wait ran out; else KD_ERR_DEVICE, and
+ * the results of those calls are not valid). */
+kd_status kd_q8_matrix_status(kd_q8_matrix* w, int32_t* flags_out);
 
 /* The schedule the library picks for a Q8_0 matrix of rows x cols on a GPU with
  * num_sms SMs (host only: no CUDA call, usable without a GPU).  It depends on the
@@ -254,6 +326,13 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
                                 int32_t cap, uint16_t* out, void* workspace,
                                 size_t workspace_bytes, kd_stream stream);
 
+/* Wait for `stream`, then read the fault word of the last attention call:
+ * `workspace` = the workspace that call was given, or NULL for the last
+ * kd_attn_append_decode_noalloc call on the current device.  *flags_out = 0
+ * when no bounded wait ran out; otherwise KD_ERR_DEVICE (that call's output is
+ * not valid).  Each call clears its word when it starts. */
+kd_status kd_attn_device_status(const void* workspace, int32_t* flags_out, kd_stream stream);
+
 /* ------------------------------------------------------------------------
  * Allocation-free variant (no counterpart on the batched-decode pages: it
  * exists for callers, not for the method).
@@ -278,8 +357,11 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
  * overlap on the GPU -- on different streams without ordering, or from
  * different threads -- race on it and must not be issued.
  * The first call on each device looks up the array's device address (once,
- * with that device current); make that first call before any stream capture.
- * Arguments, layouts and errors as for kd_attn_append_decode. */
+ * with that device current); make that first call before any stream capture
+ * (a first call made during a capture is refused with KD_ERR_INVALID_ARG, and
+ * a failed lookup is retried by the next call).
+ * Arguments, layouts and errors as for kd_attn_append_decode; a device-side
+ * fault (a bounded wait that ran out) is read with kd_attn_device_status(NULL). */
 #define KD_ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 kd_status kd_attn_append_decode_noalloc(const float* q, const float* k_new, const float* v_new,
                                         uint16_t* k_cache, uint16_t* v_cache,

@@ -73,8 +73,12 @@ def lib():
             "kd_debug_capture_hidden": [_vp, _vp],
             "kd_debug_layer": [_vp, i32, i32p, i32p, i32, _vp, _vp, _vp],
             "kd_device_status": [_vp, i32p],
+            "kd_debug_inject_wait_timeout": [_vp, i32],
+            "kd_q8_matrix_status": [_vp, i32p],
+            "kd_attn_device_status": [_vp, i32p, _vp],
             "kd_profile_enable": [_vp, i32],
             "kd_profile_read": [_vp, i32p, C.POINTER(C.c_double)],
+            "kd_profile_timeline": [_vp, _vp, i32, i32p],
             "kd_q8_matrix_create": [_vp, i32, i32, C.POINTER(_vp)],
             "kd_q8_matrix_free": [_vp],
             "kd_mmvq": [_vp, _vp, i32, _vp, _vp],
@@ -236,8 +240,26 @@ KERNEL_CLASSES = ("embed", "rmsnorm", "qkv", "attn_split", "attn_combine", "wo",
                   "lm_head", "argmax")
 
 
+def kd_debug_inject_wait_timeout(m, kernel_class: str):
+    """Make one bounded wait of the next step's first `kernel_class` launch run out
+    (a test of the device fault path; nothing faults or hangs)."""
+    _check(lib().kd_debug_inject_wait_timeout(m, KERNEL_CLASSES.index(kernel_class)))
+
+
 def kd_profile_enable(m, on: bool = True):
     _check(lib().kd_profile_enable(m, 1 if on else 0))
+
+
+KD_TIMELINE_CTAS = 1024
+
+
+def kd_profile_timeline(m, buf, max_launches: int = 0):
+    """Turn the per-CTA timeline on (buf: device uint64 [max_launches][KD_TIMELINE_CTAS][4],
+    zeroed) or off (buf None).  Returns the kernel class name of each launch index."""
+    n = int(max_launches) if buf is not None else 0
+    cls = (C.c_int32 * max(n, 1))()
+    _check(lib().kd_profile_timeline(m, _ptr(buf), n, cls if n else None))
+    return [KERNEL_CLASSES[c] if c >= 0 else None for c in cls[:n]]
 
 
 def kd_profile_read(m) -> dict:
@@ -264,6 +286,12 @@ def kd_q8_matrix_free(w):
 
 def kd_mmvq(w, x, m: int, y, stream=None):
     _check(lib().kd_mmvq(w, _ptr(x), int(m), _ptr(y), _stream(stream)))
+
+
+def kd_q8_matrix_status(w) -> int:
+    out = C.c_int32()
+    _check(lib().kd_q8_matrix_status(w, C.byref(out)))
+    return out.value
 
 
 KD_ARGMAX_WORKSPACE_BYTES = 256
@@ -297,6 +325,14 @@ def kd_attn_append_decode(q, k_new, v_new, k_cache, v_cache, slots, positions, n
                                        sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p), B, n_heads,
                                        n_kv_heads, head_dim, n_slots, cap, _ptr(out), _ptr(workspace),
                                        nbytes, _stream(stream)))
+
+
+def kd_attn_device_status(workspace=None, stream=None) -> int:
+    """Fault word of the last attention call given `workspace` (None: the last
+    allocation-free call on the current device)."""
+    out = C.c_int32()
+    _check(lib().kd_attn_device_status(_ptr(workspace), C.byref(out), _stream(stream)))
+    return out.value
 
 
 def kd_attn_append_decode_noalloc(q, k_new, v_new, k_cache, v_cache, slots, positions, n_heads, n_kv_heads,

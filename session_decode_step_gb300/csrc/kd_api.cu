@@ -29,6 +29,7 @@
 #include "kd_kernels.h"
 
 using kd::PackedQ8;
+static_assert(KD_TIMELINE_CTAS == kd::TL_CTAS, "timeline record layout");
 
 namespace {
 
@@ -147,6 +148,7 @@ struct kd_model {
     __half* act = nullptr;    // [16][F]
     float* part = nullptr;    // mmvq split-K partials
     int* cnt = nullptr;       // mmvq arrival counters
+    int cnt_n = 0;            // entries of cnt
     float* apart = nullptr;   // attention split partials
     int max_splits = 0;
     float* logits_ws = nullptr;
@@ -160,8 +162,11 @@ struct kd_model {
     cudaStream_t cap_stream = nullptr;
     std::vector<uint8_t> bound;
     std::vector<int32_t> len;
-    std::map<std::tuple<int, float*, int*>, cudaGraphExec_t> graphs;
+    std::map<std::tuple<int, float*, int*, unsigned long long*>, cudaGraphExec_t> graphs;
     float* hidden_dbg = nullptr;
+    int inject_cls = -1;      // debug fault hook: kernel class whose next launch's bounded wait runs out
+    unsigned long long* tl = nullptr;  // timeline records (kd_profile_timeline), or nullptr
+    int tl_launches = 0;      // launches the timeline buffer holds
     std::vector<void*> allocs;
     // measurement: (kernel class, start, end) of every bracketed launch since the last read
     bool prof = false;
@@ -309,6 +314,7 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(m->alloc(&m->part, part * sizeof(float)));
     KD_CK(m->alloc(&m->cnt, (size_t)max_g * sizeof(int)));
     KD_CK(cudaMemset(m->cnt, 0, (size_t)max_g * sizeof(int)));
+    m->cnt_n = max_g;
     m->max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
     if (m->max_splits > kd::ATT_MAX_SPLITS)
         return fail(KD_ERR_UNSUPPORTED, "max_ctx %d exceeds %d positions", cap, kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
@@ -342,6 +348,12 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     const int* pos = m->desc + 2 * KD_MAX_BATCH;
     const bool pdl = m->pdl && !m->prof;
     cudaError_t e;
+    // Timeline records of the step's i-th launch (kd_profile_timeline), or nullptr.
+    int launch_i = 0;
+    auto tl_next = [&]() -> unsigned long long* {
+        const int i = launch_i++;
+        return m->tl && i < m->tl_launches ? m->tl + (size_t)i * kd::TL_CTAS * kd::TL_WORDS : nullptr;
+    };
     // With measurement on, every launch is bracketed by two events (no host wait).
     cudaEvent_t ev0 = nullptr;
     auto mark0 = [&]() -> cudaError_t {
@@ -382,6 +394,13 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.x = x; a.B = B; a.part = m->part; a.cnt = m->cnt; a.err = m->err;
         return a;
     };
+    // The debug fault hook: the first launch of the chosen class expects a few
+    // bytes its copies never deliver, so one of its bounded waits runs out.
+    auto inject = [&](int cls) {
+        if (m->inject_cls != cls) return 0;
+        m->inject_cls = -1;
+        return 16;
+    };
     // RMSNorm: the embedding writes the first normed input itself; the residual
     // writers (o-proj, down) leave per-group sums of squares, and an elementwise
     // kernel forms the next projection's normed fp16 input m->xn from them.
@@ -389,12 +408,12 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.y = m->x; a.ld = H; a.ssq_out = m->ssq;
     };
     auto norm = [&](const float* w) {
-        return kd::launch_norm_from_ssq(m->x, m->ssq, B, H, w, c.rms_eps, m->xn, pdl, s);
+        return kd::launch_norm_from_ssq(m->x, m->ssq, B, H, w, c.rms_eps, m->xn, pdl, s, tl_next());
     };
     const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
     const bool whole = only_layer < 0;
     if (whole)
-        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, pdl, s));
+        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, pdl, s, tl_next()));
     if (whole && m->hidden_dbg &&
         (e = cudaMemcpyAsync(m->hidden_dbg, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
@@ -404,23 +423,34 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
+        a.inject_tx = inject(KD_K_QKV);
+        a.tl = tl_next();
         KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->map_xn, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
         kd::AttnArgs t{};
         t.q = m->q; t.kc = kc; t.vc = vc; t.row0 = (long)l * c.max_sessions * nkv * c.max_ctx;
         t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
         t.hd = hd; t.cap = c.max_ctx; t.scale = 1.0f / std::sqrt((float)hd); t.part = m->apart;
         t.max_splits = m->max_splits; t.out = m->attn; t.err = m->err;
+        t.inject_tx = inject(KD_K_ATTN_SPLIT);
+        t.tl = tl_next();
         KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->kmaps, m->attn_grid, pdl, s));
+        t.tl = tl_next();
         KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
         a = mm(m->wo[l], m->attn);
         resid(a);
+        a.inject_tx = inject(KD_K_WO);
+        a.tl = tl_next();
         KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
         KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * l + 1) * H));  // the FFN norm
         a = mm(m->gu[l], m->xn);
         a.act = m->act; a.ld = F;
+        a.inject_tx = inject(KD_K_GATE_UP);
+        a.tl = tl_next();
         KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
         a = mm(m->down[l], m->act);
         resid(a);
+        a.inject_tx = inject(KD_K_DOWN);
+        a.tl = tl_next();
         KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
         if (whole || l + 1 < l1)  // next layer's attention norm, or the output norm
             KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H));
@@ -432,16 +462,19 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     if (!whole) return cudaSuccess;
     kd::MmvqArgs a = mm(m->head, m->xn);
     a.y = lg; a.ld = V;
+    a.inject_tx = inject(KD_K_LM_HEAD);
+    a.tl = tl_next();
     KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->map_xn, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
     if (am)
         KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, m->amax_keys,
-                                              reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s));
+                                              reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s,
+                                              tl_next()));
 #undef KD_RUN
     return cudaSuccess;
 }
 
 static kd_status get_graph(kd_model* m, int B, float* lg, int* am, cudaGraphExec_t* out) {
-    auto key = std::make_tuple(B, lg, am);
+    auto key = std::make_tuple(B, lg, am, m->tl);
     auto it = m->graphs.find(key);
     if (it != m->graphs.end()) {
         *out = it->second;
@@ -624,7 +657,7 @@ kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens,
     if (st0 != KD_OK) return st0;
 
     float* lg = logits_out ? logits_out : m->logits_ws;
-    if (m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH)) {
+    if (m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH) || m->inject_cls >= 0) {
         KD_CK(enqueue_step(m, B, lg, argmax_out, s));
     } else {
         cudaGraphExec_t g = nullptr;
@@ -650,8 +683,11 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const i
     if (st != KD_OK) return st;
     const size_t bytes = (size_t)B * m->cfg.hidden * sizeof(float);
     KD_CK(cudaMemcpyAsync(m->x, x_in, bytes, cudaMemcpyDefault, s));
-    KD_CK(kd::launch_row_norm(m->x, B, m->cfg.hidden, m->norms + (size_t)(2 * layer) * m->cfg.hidden,
-                              m->cfg.rms_eps, m->xn, s));
+    // The layer's attention norm through the step's own norm kernel: sums of
+    // squares per 32-row group (as a residual writer leaves them), then xn.
+    KD_CK(kd::launch_ssq_rows(m->x, B, m->cfg.hidden, m->ssq, s));
+    KD_CK(kd::launch_norm_from_ssq(m->x, m->ssq, B, m->cfg.hidden, m->norms + (size_t)(2 * layer) * m->cfg.hidden,
+                                   m->cfg.rms_eps, m->xn, false, s));
     const bool prof = m->prof;
     m->prof = false;
     cudaError_t e = enqueue_step(m, B, nullptr, nullptr, s, layer);
@@ -671,6 +707,26 @@ kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf) {
 kd_status kd_profile_enable(kd_model* m, int32_t on) {
     if (!m) return fail(KD_ERR_INVALID_ARG, "kd_profile_enable: null model");
     m->prof = on != 0;
+    return KD_OK;
+}
+
+kd_status kd_profile_timeline(kd_model* m, uint64_t* dev_buf, int32_t max_launches, int32_t* classes_out) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_profile_timeline: null model");
+    if (dev_buf && max_launches < 1) return fail(KD_ERR_INVALID_ARG, "kd_profile_timeline: max_launches < 1");
+    m->tl = reinterpret_cast<unsigned long long*>(dev_buf);
+    m->tl_launches = dev_buf ? max_launches : 0;
+    if (classes_out) {  // the launch train of a whole step, in order
+        const int L = m->cfg.n_layers;
+        std::vector<int32_t> cls;
+        cls.push_back(KD_K_EMBED);
+        for (int l = 0; l < L; ++l)
+            for (int k : {KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO, KD_K_RMSNORM, KD_K_GATE_UP,
+                          KD_K_DOWN, KD_K_RMSNORM})
+                cls.push_back(k);
+        cls.push_back(KD_K_LM_HEAD);
+        cls.push_back(KD_K_ARGMAX);
+        for (int i = 0; i < max_launches; ++i) classes_out[i] = i < (int)cls.size() ? cls[i] : -1;
+    }
     return KD_OK;
 }
 
@@ -705,8 +761,26 @@ kd_status kd_device_status(kd_model* m, int32_t* flags_out) {
     KD_CK(cudaMemcpy(&v, m->err, sizeof(int), cudaMemcpyDeviceToHost));
     KD_CK(cudaMemset(m->err, 0, sizeof(int)));
     *flags_out = v;
-    if (v) return fail(KD_ERR_DEVICE, "a kernel gave up a bounded wait (flags 0x%x)", v);
+    if (v) {
+        // The kernels keep their arrival counters consistent when they give up;
+        // clear them anyway, so nothing a faulted step left can reach the next one.
+        KD_CK(cudaMemset(m->cnt, 0, (size_t)m->cnt_n * sizeof(int)));
+        KD_CK(cudaDeviceSynchronize());
+        return fail(KD_ERR_DEVICE, "a kernel gave up a bounded wait (flags 0x%x)", v);
+    }
     return KD_OK;
+}
+
+kd_status kd_debug_inject_wait_timeout(kd_model* m, int32_t kernel_class) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_debug_inject_wait_timeout: null model");
+    switch (kernel_class) {
+        case KD_K_QKV: case KD_K_ATTN_SPLIT: case KD_K_WO: case KD_K_GATE_UP: case KD_K_DOWN: case KD_K_LM_HEAD:
+            m->inject_cls = kernel_class;
+            return KD_OK;
+        default:
+            return fail(KD_ERR_INVALID_ARG, "kd_debug_inject_wait_timeout: kernel class %d has no bounded wait",
+                        kernel_class);
+    }
 }
 
 // ------------------------------------------------------------- op level ----
@@ -785,6 +859,22 @@ kd_status kd_mmvq(const kd_q8_matrix* w, const uint16_t* x, int32_t m, float* y,
     return KD_OK;
 }
 
+kd_status kd_q8_matrix_status(kd_q8_matrix* w, int32_t* flags_out) {
+    if (!w || !flags_out) return fail(KD_ERR_INVALID_ARG, "kd_q8_matrix_status: null argument");
+    KD_CK(cudaSetDevice(w->dev));
+    KD_CK(cudaDeviceSynchronize());
+    int v = 0;
+    KD_CK(cudaMemcpy(&v, w->err, sizeof(int), cudaMemcpyDeviceToHost));
+    *flags_out = v;
+    if (v) {
+        KD_CK(cudaMemset(w->err, 0, sizeof(int)));
+        KD_CK(cudaMemset(w->cnt, 0, (size_t)w->p.G * sizeof(int)));
+        KD_CK(cudaDeviceSynchronize());
+        return fail(KD_ERR_DEVICE, "kd_mmvq: a kernel gave up a bounded wait (flags 0x%x)", v);
+    }
+    return KD_OK;
+}
+
 kd_status kd_mmvq_schedule(int32_t rows, int32_t cols, int32_t num_sms, int32_t* mode_out, int32_t* warps_out,
                            int32_t* share_out) {
     if (!mode_out || !warps_out || !share_out) return fail(KD_ERR_INVALID_ARG, "kd_mmvq_schedule: null argument");
@@ -825,6 +915,29 @@ size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int
     if (B < 1 || n_heads < 1 || head_dim < 1 || cap < 1) return 0;
     const size_t splits = (size_t)(cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
     return 256 + (size_t)B * n_heads * splits * kd::ATT_REC(head_dim) * sizeof(float);
+}
+
+kd_status kd_attn_device_status(const void* workspace, int32_t* flags_out, kd_stream stream) {
+    if (!flags_out) return fail(KD_ERR_INVALID_ARG, "kd_attn_device_status: null argument");
+    cudaStream_t s = (cudaStream_t)stream;
+    KD_CK(cudaStreamSynchronize(s));
+    int* word = nullptr;
+    if (workspace) {
+        word = (int*)workspace + 2 * KD_MAX_BATCH;
+    } else {
+        int dev = 0;
+        KD_CK(cudaGetDevice(&dev));
+        KD_CK(kd::noalloc_fault_word(dev, &word));
+        if (!word) {  // the allocation-free call never ran on this device: nothing to report
+            *flags_out = 0;
+            return KD_OK;
+        }
+    }
+    int v = 0;
+    KD_CK(cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost));
+    *flags_out = v;
+    if (v) return fail(KD_ERR_DEVICE, "attention: a kernel gave up a bounded wait (flags 0x%x)", v);
+    return KD_OK;
 }
 
 kd_status kd_attn_append_decode(const float* q, const float* k_new, const float* v_new, uint16_t* k_cache,

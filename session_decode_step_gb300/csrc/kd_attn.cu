@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     constexpr int NU = HD / 8;   // 8-dim output tiles of P V
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "GQA group");
     extern __shared__ uint8_t smem_raw[];
+    tl_entry(a.tl);
     uint8_t* smem = align1024(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
         }
         *cta_failed = 0;
         mbar_init_fence();
+        if (a.inject_tx && blockIdx.x == 0) mbar_expect_tx(&bar[0], (uint32_t)a.inject_tx);  // debug fault hook
     }
     __syncthreads();
 
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     }
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(a.tl);
     for (int i = 0, k = warp; k < S && k < nk; ++i, k += AT_WARPS)
         if (!((early >> i) & 1u)) {
             const AttnItem it = tab.item(a, lane, gitem(k));
@@ -442,6 +445,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
             const int k = stage_item[i];
             if (k >= 0) (void)mbar_wait_bounded(&bar[i], (uint32_t)(k / S) & 1u);
         }
+    tl_exit(a.tl);
 }
 
 // Merge a (session, head)'s splits in split order:
@@ -458,13 +462,18 @@ template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __shared__ float wts[COMB_MAX_SPLITS], ls[COMB_MAX_SPLITS];
     __shared__ float red_m[HD / 32], red_l[HD / 32];
+    tl_entry(a.tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     // The step's positions were staged before its first kernel: read while the
     // split kernel finishes.
     const int pos_b = b < a.B ? a.pos[b] : 0;
     pdl_wait();
-    if (b >= a.B) return;
+    tl_waited(a.tl);
+    if (b >= a.B) {
+        tl_exit(a.tl);
+        return;
+    }
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
     // Only the session's own split records are read: records past its split count
     // may be cold (never written), and the first round waits for its slowest load.
@@ -514,6 +523,7 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
             if (s0 + s < ns) num = __fmaf_rn(wts[s0 + s], o[s], num);
     }
     a.out[(size_t)b * a.nh * HD + (size_t)h * HD + d] = __float2half_rn(__fdiv_rn(num, L));
+    tl_exit(a.tl);
 }
 
 // Standalone append (the op-level entry point; the step appends in the QKV epilogue).

@@ -29,9 +29,11 @@ namespace {
 constexpr size_t DESC_BYTES = 256;
 constexpr int MAX_DEVICES = 64;
 
-std::once_flag g_setup_once[MAX_DEVICES];
+// Per device, the scratch array's device address: stored only once the lookup
+// has succeeded, so a failed lookup (a transient error, or a first call made
+// during a stream capture) is retried by the next call.
+std::mutex g_setup_mu;
 void* g_scratch_ptr[MAX_DEVICES];
-cudaError_t g_setup_err[MAX_DEVICES];
 
 // Slots and positions arrive by value; the fault word must start at zero.
 struct DescArgs {
@@ -53,7 +55,36 @@ kd_status fail(kd_status st, const std::string& msg) {
     return st;
 }
 
+// The array's device address on device `dev` (current), looked up on first use.
+kd_status scratch_address(int dev, cudaStream_t s, void** out) {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_scratch_ptr[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+            return fail(KD_ERR_INVALID_ARG,
+                        "kd_attn_append_decode_noalloc: the first call on a device looks up the scratch "
+                        "array's address and must not be made during a stream capture");
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return fail(KD_ERR_CUDA, std::string("kd_attn_append_decode_noalloc: cudaGetSymbolAddress: ") +
+                                         cudaGetErrorString(e));
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return KD_OK;
+}
+
 }  // namespace
+
+cudaError_t kd::noalloc_fault_word(int dev, int** out) {
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    *out = g_scratch_ptr[dev] ? reinterpret_cast<int*>(g_scratch_ptr[dev]) + 2 * KD_MAX_BATCH : nullptr;
+    return cudaSuccess;
+}
 
 extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* k_new, const float* v_new,
                                                    uint16_t* k_cache, uint16_t* v_cache, const int32_t* slots,
@@ -91,14 +122,12 @@ extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
         return fail(KD_ERR_CUDA, "kd_attn_append_decode_noalloc: no current CUDA device");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Once per device, with it current: the scratch array's device address.  In
     // host code the array's name only stands in for it.
-    std::call_once(g_setup_once[dev], [dev] {
-        g_setup_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_attn_scratch);
-    });
-    if (g_setup_err[dev] != cudaSuccess)
-        return fail(KD_ERR_CUDA, std::string("kd_attn_append_decode_noalloc: cudaGetSymbolAddress: ") +
-                                     cudaGetErrorString(g_setup_err[dev]));
+    void* scratch = nullptr;
+    const kd_status st = scratch_address(dev, s, &scratch);
+    if (st != KD_OK) return st;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         kd::ensure_device_attributes(dev) != cudaSuccess)
@@ -107,8 +136,7 @@ extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* 
     if (kd::make_attn_maps(reinterpret_cast<const __half*>(k_cache), reinterpret_cast<const __half*>(v_cache),
                            (long)n_slots * n_kv_heads * cap, head_dim, &maps) != cudaSuccess)
         return fail(KD_ERR_CUDA, "kd_attn_append_decode_noalloc: tensor map encoding failed");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int* desc = reinterpret_cast<int*>(g_scratch_ptr[dev]);
+    int* desc = reinterpret_cast<int*>(scratch);
     cudaError_t e;
     set_descriptor_kernel<<<1, 32, 0, s>>>(d, B, desc);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(KD_ERR_CUDA, cudaGetErrorString(e));
@@ -128,7 +156,7 @@ extern "C" kd_status kd_attn_append_decode_noalloc(const float* q, const float* 
     t.hd = head_dim;
     t.cap = cap;
     t.scale = 1.0f / sqrtf((float)head_dim);
-    t.part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(g_scratch_ptr[dev]) + DESC_BYTES);
+    t.part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(scratch) + DESC_BYTES);
     t.max_splits = (int)splits;
     t.out = reinterpret_cast<__half*>(out);
     t.err = desc + 2 * KD_MAX_BATCH;

@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "kd_kernels.h"
+
 namespace kd {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
@@ -27,6 +29,40 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---- timeline (kd_profile_timeline): optional per-CTA stamps ------------------
+// A launch's records are [TL_CTAS][TL_WORDS] u64: the global timer (ns) at the
+// CTA's entry, when its dependency wait returned, the latest end over its
+// warps, and its SM id.  tl == nullptr (the normal case) costs one test.
+
+__device__ __forceinline__ unsigned long long* tl_rec(unsigned long long* tl) {
+    const unsigned cta = blockIdx.y * gridDim.x + blockIdx.x;
+    return cta < (unsigned)TL_CTAS ? tl + (size_t)cta * TL_WORDS : nullptr;
+}
+__device__ __forceinline__ void tl_entry(unsigned long long* tl) {
+    if (tl && threadIdx.x == 0) {
+        unsigned long long* r = tl_rec(tl);
+        if (r) {
+            unsigned sm;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+            r[0] = global_timer_ns();
+            r[3] = sm;
+        }
+    }
+}
+__device__ __forceinline__ void tl_waited(unsigned long long* tl) {
+    if (tl && threadIdx.x == 0) {
+        unsigned long long* r = tl_rec(tl);
+        if (r) r[1] = global_timer_ns();
+    }
+}
+// Called by every warp as it finishes (lane 0 stamps; the record keeps the latest).
+__device__ __forceinline__ void tl_exit(unsigned long long* tl) {
+    if (tl && (threadIdx.x & 31) == 0) {
+        unsigned long long* r = tl_rec(tl);
+        if (r) atomicMax(r + 2, (unsigned long long)global_timer_ns());
+    }
+}
+
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -42,6 +78,14 @@ __device__ __forceinline__ void mbar_init_fence() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
+                 : "memory");
+}
+
+// Raise the byte count the barrier's current phase waits for, without an
+// arrival (the debug fault hook: a phase that expects more bytes than its
+// copies deliver never completes, so the bounded wait on it runs out).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
 

@@ -40,6 +40,10 @@ enum Epilogue : int {
     EPI_QKV = 3,     // RoPE q and k at each row's position, q to fp32, k/v appended as fp16
 };
 
+// Timeline records (kd_profile_timeline): per launch [TL_CTAS][TL_WORDS] u64.
+constexpr int TL_CTAS = 1024;
+constexpr int TL_WORDS = 4;
+
 constexpr int MAX_NORM_SLOTS = 16;  // sum-of-squares tables hold one entry per session slot 0..15
 
 enum MmvqMode : int {
@@ -92,6 +96,10 @@ struct MmvqArgs {
     int* cnt;            // [G] arrival counters, zero between launches
                          // (part: [G][maxc][32 rows][16 columns] fp32)
     int* err;            // device fault word
+    // Debug fault hook (0 in normal use): extra bytes the first stage of CTA 0,
+    // warp 0 waits for, so that its bounded wait runs out (no copy is touched).
+    int inject_tx;
+    unsigned long long* tl;  // timeline records of this launch, or nullptr
     int ld;              // row stride (elements) of the epilogue output
     float* y;            // EPI_STORE / EPI_RESID target
     __half* act;         // EPI_SWIGLU target
@@ -131,6 +139,8 @@ struct AttnArgs {
     int max_splits;
     __half* out;          // [B][nh*hd]
     int* err;
+    int inject_tx;        // debug fault hook (0 in normal use): extra bytes item 0's K tile waits for
+    unsigned long long* tl;  // timeline records of this launch (split or combine), or nullptr
 };
 
 // Tensor maps over the K and V arenas, each viewed as [rows][hd] fp16: 64-row
@@ -154,19 +164,24 @@ cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half*
 // x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and the first
 // layer's normed input xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w)
 cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, bool pdl, cudaStream_t s);
-// xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w) for rows supplied from outside
-cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, cudaStream_t s);
+                         float eps, __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl = nullptr);
+// ssq[g][b] = sum of x[b][32g .. 32g+31]^2 for rows supplied from outside, in
+// the residual writers' group layout and summation order
+cudaError_t launch_ssq_rows(const float* x, int B, int H, float* ssq, cudaStream_t s);
 // The same norm from the per-group sums of squares ssq[g][b] (g < H/32) a
 // residual writer left: elementwise, spread over many CTAs.
 cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
-                                 __half* xn, bool pdl, cudaStream_t s);
+                                 __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl = nullptr);
 cudaError_t rowops_init_attributes();
 // out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none).
 // keys [>= B] and done: device scratch that is zero before the first launch;
 // every launch leaves it zero again.  V must be a multiple of 4.
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
-                          bool pdl, cudaStream_t s);
+                          bool pdl, cudaStream_t s, unsigned long long* tl = nullptr);
+
+// Device address of the allocation-free attention call's fault word on device
+// dev, or nullptr if that call has not run on the device yet.
+cudaError_t noalloc_fault_word(int dev, int** out);
 
 // Set the calling thread's last-error message (what kd_last_error() returns).
 void set_last_error(const char* msg);

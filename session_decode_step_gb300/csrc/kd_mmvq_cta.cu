@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     constexpr uint32_t SB = STAGE_BYTES + NT * XTILE_BYTES;  // bytes a stage's barrier waits for
     static_assert(!PAIR || NT == 1, "two CTAs per SM need the one-tile register budget");
     extern __shared__ uint8_t smem_raw[];
+    tl_entry(a.tl);
     uint8_t* smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
@@ -73,11 +74,17 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     // waiting for the producer of the activations.  Each barrier expects the
     // stage's weights and activations; the activations follow after the wait.
     if (lane == 0) {
+        if (a.inject_tx && blockIdx.x == 0 && total > 0) {  // debug fault hook: CTA 0's first warp with stages
+            int fw = 0;
+            while ((fw + 1) * a.KG / MMVQ_WARPS == fw * a.KG / MMVQ_WARPS) ++fw;
+            if (warp == fw) mbar_expect_tx(&bar[0], (uint32_t)a.inject_tx);
+        }
         for (int i = 0; i < RD && i < total; ++i) issue_w(i);
         prefetch_tmap(&xm);
     }
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(a.tl);
     if (lane == 0)
         for (int i = 0; i < RD && i < total; ++i)
             tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);
@@ -174,6 +181,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
         }
         __syncthreads();  // the partial buffer is reused by the next group
     }
+    tl_exit(a.tl);
 }
 
 template <int NT, int EPI, bool PAIR>

@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     constexpr int RD = L::RD;
     constexpr uint32_t SB = STAGE_BYTES + NT * XTILE_BYTES;  // bytes a stage's barrier waits for
     extern __shared__ uint8_t smem_raw[];
+    tl_entry(a.tl);
     uint8_t* smem = align1024(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     // waiting for the producer of the activations.  Each barrier expects the
     // stage's weights and activations; the activations follow after the wait.
     if (lane == 0) {
+        if (a.inject_tx && blockIdx.x == 0 && warp == 0 && n > 0) mbar_expect_tx(&bar[0], (uint32_t)a.inject_tx);
         for (int i = 0; i < RD && i < n; ++i) {
             mbar_arrive_expect_tx(&bar[i], SB);
             bulk_g2s_hint(ring + i * STAGE_BYTES, wsrc + (size_t)i * STAGE_BYTES, STAGE_BYTES, &bar[i], policy);
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     }
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(a.tl);
 
     int g = (int)(s_begin / a.KG), kg = (int)(s_begin - (long)g * a.KG);
     int xkg = kg;  // k-group of the next stage whose activations are requested (lane 0)
@@ -137,6 +140,18 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
             if (lane == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
             for (int t = i; t < n && t < i + RD; ++t)
                 (void)mbar_wait_bounded(&bar[t % RD], (uint32_t)(t / RD) & 1u);
+            // Keep the arrival counters consistent for the next launch: arrive on
+            // every shared row group this warp still owns (the current one has not
+            // been arrived on yet), and reset a counter when arriving last.  The
+            // groups' outputs are not valid after a fault (the fault word says so).
+            if (lane == 0) {
+                const int g_last = (int)((s_end - 1) / a.KG);
+                for (int gg = g; gg <= g_last; ++gg) {
+                    const long first = (long)gg * a.KG;
+                    const int w0 = stage_owner(first, T, a.W), w1 = stage_owner(first + a.KG - 1, T, a.W);
+                    if (w0 != w1 && atomicAdd(&a.cnt[gg], 1) == w1 - w0) a.cnt[gg] = 0;
+                }
+            }
             break;
         }
         uint4 xv[4][NT];
@@ -234,6 +249,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
         ++g;
         kg = 0;
     }
+    tl_exit(a.tl);
 }
 
 template <int NT, int EPI>

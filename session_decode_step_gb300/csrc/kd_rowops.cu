@@ -64,9 +64,12 @@ __device__ __forceinline__ void norm_row(const float* x, int H, const float* w, 
 __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __restrict__ emb,
                                                               const int* __restrict__ token, int H,
                                                               float* __restrict__ x, const float* __restrict__ w,
-                                                              float eps, __half* __restrict__ xn) {
+                                                              float eps, __half* __restrict__ xn,
+                                                              unsigned long long* tl) {
+    tl_entry(tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(tl);
     const int b = blockIdx.x, tid = threadIdx.x;
     float* xr = x + (size_t)b * H;
     constexpr int U = 16;  // elements per thread whose loads are issued together
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
             const int i = tid + EMBED_THREADS * u;
             if (i < H) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(xv[u], r), wv[u]));
         }
+        tl_exit(tl);
         return;
     }
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
@@ -133,21 +137,30 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
         }
     }
     norm_row(xr, H, w, eps, xn + (size_t)b * H, s);  // each thread re-reads only what it wrote
+    tl_exit(tl);
 }
 
-// The same norm for residual rows supplied from outside.
-__global__ void __launch_bounds__(EMBED_THREADS) row_norm_kernel(const float* __restrict__ x, int H,
-                                                                 const float* __restrict__ w, float eps,
-                                                                 __half* __restrict__ xn) {
-    const int b = blockIdx.x, tid = threadIdx.x;
-    const float* xr = x + (size_t)b * H;
-    float s = 0.0f;
-    for (int i = tid; i < H; i += EMBED_THREADS) s = __fmaf_rn(xr[i], xr[i], s);
-    norm_row(xr, H, w, eps, xn + (size_t)b * H, s);
+// Per-group sums of squares of residual rows supplied from outside, in the
+// layout and order the residual writers' epilogues leave them: one warp per
+// (32-row group g, row b), lane r holding x[b][32g + r]^2, added by a fixed
+// shuffle tree.  The step's own RMSNorm kernel then forms the normed input
+// from them (so a layer run alone goes through the same norm as in a step).
+constexpr int SSQ_WARPS = 8;
+
+__global__ void __launch_bounds__(SSQ_WARPS * 32) ssq_rows_kernel(const float* __restrict__ x, int H,
+                                                                  float* __restrict__ ssq) {
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x * SSQ_WARPS + (threadIdx.x >> 5), b = blockIdx.y;
+    if (g >= H / 32) return;
+    const float v = x[(size_t)b * H + (size_t)g * 32 + lane];
+    float s = __fmul_rn(v, v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+    if (lane == 0) ssq[(size_t)g * MAX_NORM_SLOTS + b] = s;
 }
 
-cudaError_t launch_row_norm(const float* x, int B, int H, const float* w, float eps, __half* xn, cudaStream_t s) {
-    row_norm_kernel<<<B, EMBED_THREADS, 0, s>>>(x, H, w, eps, xn);
+cudaError_t launch_ssq_rows(const float* x, int B, int H, float* ssq, cudaStream_t s) {
+    ssq_rows_kernel<<<dim3((H / 32 + SSQ_WARPS - 1) / SSQ_WARPS, B), SSQ_WARPS * 32, 0, s>>>(x, H, ssq);
     return cudaGetLastError();
 }
 
@@ -161,10 +174,13 @@ constexpr int NORM_COLS = NORM_THREADS * 4;
 __global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float* __restrict__ x,
                                                                      const float* __restrict__ ssq, int H,
                                                                      const float* __restrict__ w, float eps,
-                                                                     __half* __restrict__ xn) {
+                                                                     __half* __restrict__ xn,
+                                                                     unsigned long long* tl) {
     __shared__ float rsh;
+    tl_entry(tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(tl);
     const int b = blockIdx.y, tid = threadIdx.x;
     const int i = blockIdx.x * NORM_COLS + tid * 4;
     const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
@@ -190,15 +206,17 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float
         if (tid == 0) rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
     }
     __syncthreads();
-    if (i >= H) return;
-    const float r = rsh;
-    __half2* o = reinterpret_cast<__half2*>(xn + (size_t)b * H + i);
-    o[0] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.x, r), g.x), __fmul_rn(__fmul_rn(v.y, r), g.y));
-    o[1] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
+    if (i < H) {
+        const float r = rsh;
+        __half2* o = reinterpret_cast<__half2*>(xn + (size_t)b * H + i);
+        o[0] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.x, r), g.x), __fmul_rn(__fmul_rn(v.y, r), g.y));
+        o[1] = __floats2half2_rn(__fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
+    }
+    tl_exit(tl);
 }
 
 cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H, const float* w, float eps,
-                                 __half* xn, bool pdl, cudaStream_t s) {
+                                 __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -208,7 +226,7 @@ cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H,
     cfg.gridDim = dim3((H + NORM_COLS - 1) / NORM_COLS, B);
     cfg.blockDim = dim3(NORM_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, norm_from_ssq_kernel, x, ssq, H, w, eps, xn);
+    return cudaLaunchKernelEx(&cfg, norm_from_ssq_kernel, x, ssq, H, w, eps, xn, tl);
 }
 
 // Greedy argmax over many CTAs.  Each (value, index) maps to a 64-bit key whose
@@ -230,11 +248,13 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
 
 __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __restrict__ logits, int V,
                                                                 unsigned long long* keys, unsigned* done,
-                                                                int* __restrict__ out) {
+                                                                int* __restrict__ out, unsigned long long* tl) {
     __shared__ unsigned long long wbest[ARGMAX_THREADS / 32];
     __shared__ bool last;
+    tl_entry(tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
+    tl_waited(tl);
     const int b = blockIdx.y, tid = threadIdx.x;
     const float* row = logits + (size_t)b * V;
     const int i0 = blockIdx.x * ARGMAX_CHUNK + tid * 4;
@@ -270,12 +290,13 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __r
         out[tid] = k ? (int)(~(unsigned)(k & 0xffffffffull)) : -1;
         if (tid == 0) *done = 0u;
     }
+    tl_exit(tl);
 }
 
 cudaError_t rowops_init_attributes() {
     // One shared-memory carveout for every kernel of the step, so consecutive
     // kernels never wait for an SM to reconfigure its L1/shared split.
-    for (const void* f : {(const void*)embed_kernel, (const void*)row_norm_kernel, (const void*)norm_from_ssq_kernel,
+    for (const void* f : {(const void*)embed_kernel, (const void*)ssq_rows_kernel, (const void*)norm_from_ssq_kernel,
                           (const void*)argmax_kernel}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
@@ -292,18 +313,18 @@ static void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pd
 }
 
 cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, bool pdl, cudaStream_t s) {
+                         float eps, __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
     cfg.gridDim = dim3(B);
     cfg.blockDim = dim3(EMBED_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn);
+    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn, tl);
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
-                          bool pdl, cudaStream_t s) {
+                          bool pdl, cudaStream_t s, unsigned long long* tl) {
     if (V % 4) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -311,7 +332,7 @@ cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned 
     cfg.gridDim = dim3((V + ARGMAX_CHUNK - 1) / ARGMAX_CHUNK, B);
     cfg.blockDim = dim3(ARGMAX_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, keys, done, out);
+    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, keys, done, out, tl);
 }
 
 }  // namespace kd

@@ -12,8 +12,10 @@ of 128, SwiGLU FFN 14336, vocabulary 128256).  All weights are Q8_0: blocks of
 32 consecutive input-dimension values of one output row, stored as a
 little-endian fp16 scale ``d`` followed by 32 int8 quants (34 bytes), so that
 ``value = q * d``.  Quants are uniform over the integers in [-127, 127]; scales
-are ``fp16(|z| / 127)`` with ``z ~ N(0, 0.02^2)``.  Norm weights are fp32 ones.
-Pre-filled KV rows are fp16 draws of N(0, 1).
+are ``fp16(|z| / 127)`` with ``z ~ N(0, 0.02^2)``.  Norm weights are fp32 ones
+(the workloads' own weights); ``norm_weights`` draws non-unit ones, different
+for every layer, for extra parity cases.  Pre-filled KV rows are fp16 draws of
+N(0, 1).
 
 Every tensor has its own substream, keyed by ``(seed, name)``, so any piece can
 be regenerated on its own (the oracle regenerates only the sessions it checks).
@@ -132,6 +134,25 @@ def model_weights(shape: ModelShape, seed: int = 0, threads: int | None = None) 
     for l in range(shape.n_layers):
         w[f"blk.{l}.attn_norm"] = np.ones(shape.hidden, dtype=np.float32)
         w[f"blk.{l}.ffn_norm"] = np.ones(shape.hidden, dtype=np.float32)
+    return w
+
+
+def norm_weights(shape: ModelShape, seed: int = 0, spread: float = 0.1) -> dict:
+    """Non-unit fp32 norm weights, ``1 + spread * N(0, 1)``, one seeded vector per
+    (layer, norm) and one for the output norm, all different.
+
+    Keys as in ``model_weights``; ``dict(model_weights(...), **norm_weights(...))``
+    gives the same matrices with these norms (a parity case beside the
+    workloads' unit norms, so that a kernel dropping the weight, or reading the
+    wrong layer's, cannot pass)."""
+    def draw(name):
+        z = substream(seed, "norm", name).standard_normal(shape.hidden)
+        return (1.0 + spread * z).astype(np.float32)
+
+    w = {"output_norm": draw("output_norm")}
+    for l in range(shape.n_layers):
+        w[f"blk.{l}.attn_norm"] = draw(f"blk.{l}.attn_norm")
+        w[f"blk.{l}.ffn_norm"] = draw(f"blk.{l}.ffn_norm")
     return w
 
 

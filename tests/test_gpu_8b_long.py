@@ -9,6 +9,10 @@ Gates:
 - at the first step, the logits of the shortest and the longest session within
   5e-2 of the fp64 oracle (which runs each alone at its own length), and layers
   0, 16 and 31 of both within 1e-3 relative L2 when fed the oracle's input;
+- the longest session teacher-forced through all 64 steps: at the last one it
+  writes and attends the slot's last position (32767, a full last split), where
+  its logits must be within 5e-2 of the oracle's and its hidden states within
+  the end-to-end bound;
 - every session's 64-step greedy stream (tokens, and the logit bits of sampled
   steps) in the B = 8 batch equal to its run alone (B = 1) from the same start.
 """
@@ -77,6 +81,47 @@ def test_8b_long_context_against_oracle(long_model):
             want = ref_h[i][l + 1]
             rel = float(np.linalg.norm(out[j] - want) / np.linalg.norm(want))
             assert rel <= HIDDEN_REL_L2, (l, i, rel)
+    assert kd.kd_device_status(m) == 0
+
+
+HIDDEN_REL_L2_END_TO_END = 1e-2  # as in test_gpu_8b.py (see the sensitivity test)
+
+
+def test_8b_long_context_last_position_against_oracle(long_model):
+    kd, m, w, ids, keep = long_model
+    V, H, L = SHAPE.vocab, SHAPE.hidden, SHAPE.n_layers
+    i = S - 1
+    assert LENS[i] + STEPS == CAP  # the last step decodes position CAP - 1
+    tok0 = synth.tokens(CASE["seed"], "8b-long-tf", S, V)
+    om = oracle.OracleModel(SHAPE, w)
+    cache = om.new_cache(CAP, *keep[i])
+    tok = tok0[i:i + 1].copy()
+    toks = []
+    for s in range(STEPS):  # the oracle alone, from its own greedy tokens
+        lg, am, h = om.step(tok, [LENS[i] + s], [cache], CAP, want_hidden=s == STEPS - 1)
+        toks.append(int(tok[0]))
+        tok = am.copy()
+    ref_lg, ref_h = lg[0], h[0]
+    del cache
+    hid = torch.empty(L + 1, S, H, device="cuda", dtype=torch.float32)
+    lgd = torch.empty(S, V, device="cuda", dtype=torch.float32)
+    amd = torch.empty(S, device="cuda", dtype=torch.int32)
+    tok = tok0.copy()
+    try:
+        for s in range(STEPS):
+            tok[i] = toks[s]
+            kd.kd_debug_capture_hidden(m, hid if s == STEPS - 1 else None)
+            kd.kd_decode_step(m, ids, tok, [n + s for n in LENS], lgd, amd)
+            tok = amd.cpu().numpy()
+        got, gh = lgd.cpu().numpy()[i], hid.cpu().numpy()[:, i]
+    finally:
+        kd.kd_debug_capture_hidden(m, None)
+    assert kd.kd_session_length(m, ids[i]) == CAP
+    err = float(np.abs(got - ref_lg).max())
+    assert err <= LOGIT_TOL, err
+    for l in range(L + 1):
+        rel = float(np.linalg.norm(gh[l] - ref_h[l]) / np.linalg.norm(ref_h[l]))
+        assert rel <= HIDDEN_REL_L2_END_TO_END, (l, rel)
     assert kd.kd_device_status(m) == 0
 
 

@@ -1,0 +1,109 @@
+"""The 8B-shaped decode step with non-unit norm weights, through the C ABI.
+
+The workloads fix every norm weight to 1, which would let a kernel that drops
+the weight, or reads another layer's, pass.  This parity case keeps the 8B
+matrices (random Q8_0, seed 0) and draws every norm vector from its own seeded
+stream (1 + 0.1 N(0, 1): each layer's attention and FFN norm and the output norm
+all differ).  Sessions are pre-filled with 1238 random fp16 positions.
+
+Gates: every one of the 32 layers within 1e-3 relative L2 of the oracle when fed
+the oracle's input to that layer (the layer's attention norm goes through the
+step's own sums-of-squares RMSNorm kernel, its FFN norm through the residual
+writer's sums); one B = 8 step end to end: logits within 5e-2 and hidden states
+within the end-to-end bound for 4 sessions."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+SHAPE = synth.LLAMA3_8B
+PREFILL, CAP = synth.DENSE_8B_CASE["prefill"], synth.DENSE_8B_CASE["capacity"]
+HIDDEN_REL_L2 = 1e-3
+HIDDEN_REL_L2_END_TO_END = 1e-2  # as in test_gpu_8b.py (see the sensitivity test)
+
+
+@pytest.fixture(scope="module")
+def model_norms(kdlib):
+    kd = kdlib
+    w = dict(synth.model_weights(SHAPE, 0), **synth.norm_weights(SHAPE, 11))
+    m = kd.kd_model_load(kd.make_config(SHAPE, 8, CAP), w)
+    kv = {}
+
+    def prefill(i):
+        if i not in kv:
+            kv[i] = synth.kv_prefill(SHAPE, 0, i, PREFILL)
+        return kv[i]
+
+    yield kd, m, w, prefill
+    kd.kd_model_free(m)
+
+
+def bind(kd, m, prefill, sessions):
+    ids = []
+    for i in sessions:
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, *prefill(i), PREFILL)
+        ids.append(sid)
+    torch.cuda.synchronize()
+    return ids
+
+
+def test_8b_seeded_norms_every_layer(model_norms):
+    kd, m, w, prefill = model_norms
+    L, H = SHAPE.n_layers, SHAPE.hidden
+    sessions = (1, 6)
+    om = oracle.OracleModel(SHAPE, w)
+    tok = synth.tokens(0, "8b-norm-layers", len(sessions), SHAPE.vocab)
+    ref_h = []
+    for j, b in enumerate(sessions):
+        c = om.new_cache(PREFILL + 1, *prefill(b))
+        _, _, h = om.step(tok[j:j + 1], [PREFILL], [c], PREFILL + 1, want_hidden=True)
+        ref_h.append(h[0])
+    ref_h = np.stack(ref_h, axis=1)  # [L+1][B][H]
+    ids = bind(kd, m, prefill, sessions)
+    try:
+        x_out = torch.empty(len(sessions), H, device="cuda", dtype=torch.float32)
+        for l in range(L):
+            x_in = torch.from_numpy(np.ascontiguousarray(ref_h[l])).cuda()
+            kd.kd_debug_layer(m, l, ids, [PREFILL] * len(sessions), x_in, x_out)
+            got = x_out.cpu().numpy()
+            for j in range(len(sessions)):
+                rel = np.linalg.norm(got[j] - ref_h[l + 1, j]) / np.linalg.norm(ref_h[l + 1, j])
+                assert rel <= HIDDEN_REL_L2, (l, sessions[j], rel)
+        assert kd.kd_device_status(m) == 0
+    finally:
+        for sid in ids:
+            kd.kd_session_free(m, sid)
+
+
+def test_8b_seeded_norms_step(model_norms):
+    kd, m, w, prefill = model_norms
+    B, L, H, V = 8, SHAPE.n_layers, SHAPE.hidden, SHAPE.vocab
+    checked = (0, 3, 4, 7)
+    ids = bind(kd, m, prefill, range(B))
+    hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+    kd.kd_debug_capture_hidden(m, hid)
+    try:
+        tok = synth.tokens(0, "8b-norm-step", B, V)
+        lg = torch.empty(B, V, device="cuda", dtype=torch.float32)
+        kd.kd_decode_step(m, ids, tok, [PREFILL] * B, lg, None)
+        torch.cuda.synchronize()
+        got, gh = lg.cpu().numpy(), hid.cpu().numpy()
+        om = oracle.OracleModel(SHAPE, w)
+        for b in checked:
+            c = om.new_cache(PREFILL + 1, *prefill(b))
+            ref, _, h = om.step(tok[b:b + 1], [PREFILL], [c], PREFILL + 1, want_hidden=True)
+            err = float(np.abs(got[b] - ref[0]).max())
+            assert err <= 5e-2, (b, err)
+            for l in range(L + 1):
+                rel = np.linalg.norm(gh[l, b] - h[0, l]) / np.linalg.norm(h[0, l])
+                assert rel <= HIDDEN_REL_L2_END_TO_END, (b, l, rel)
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_debug_capture_hidden(m, None)
+        for sid in ids:
+            kd.kd_session_free(m, sid)

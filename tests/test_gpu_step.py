@@ -5,9 +5,10 @@ vocab 512, RoPE theta 1e4, Q8_0 weights as generated), B = 2 sessions with 17
 and 40 pre-filled fp16 positions, 4 greedy steps, seed 0.
 
 Gates: teacher-forced logits within 5e-2 (max abs) of the oracle and per-layer
-hidden states within 1e-3 relative L2; every session's greedy stream and logits
-bit-identical to its isolated B = 1 run; graph replay identical to the direct
-launch train."""
+hidden states within 1e-3 relative L2 -- with the workload's unit norm weights
+and with seeded non-unit ones, different for every layer and norm; every
+session's greedy stream and logits bit-identical to its isolated B = 1 run;
+graph replay identical to the direct launch train."""
 import numpy as np
 import pytest
 
@@ -52,10 +53,16 @@ def tiny():
 
 # 0: schedules chosen per matrix; 2 / 4: every projection forced onto the
 # stream / group schedule (the tiny model alone would only exercise one of them).
+# norms: the workload's unit norm weights, or seeded non-unit ones (1 + 0.1 N(0,1),
+# a different vector for every layer's two norms and the output norm), so that a
+# kernel that dropped the weight or read another layer's would fail.
+@pytest.mark.parametrize("norms", ["unit", "seeded"])
 @pytest.mark.parametrize("flags", [0, 2, 4])
-def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags):
+def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags, norms):
     kd = kdlib
     shape, w = tiny
+    if norms == "seeded":
+        w = dict(w, **synth.norm_weights(shape, 7))
     case = synth.TINY_CASE
     cap = 64
     m = load(kd, shape, w, 4, cap, flags)
