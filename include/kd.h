@@ -42,14 +42,16 @@ enum {
     KD_ERR_NO_FREE_SLOT = -4,  /* every session slot is bound */
     KD_ERR_BAD_SESSION = -5,   /* id out of range, not bound, or repeated within one step */
     KD_ERR_POSITION = -6,      /* position < 0, > the session's length, or >= max_ctx */
-    KD_ERR_BATCH = -7,         /* B outside [1, KD_MAX_BATCH] */
+    KD_ERR_BATCH = -7,         /* B < 1, or above what the call accepts (see each call) */
     KD_ERR_UNSUPPORTED = -8,   /* a shape the kernels do not implement (see kd_config) */
     KD_ERR_DEVICE = -9         /* a kernel reported a device-side fault (bounded wait ran out) */
 };
 
-/* The widest batch with an exact kernel class: memra refuses B > 16 because
- * above it its kernels change numeric configuration and rows are no longer
- * exact (decode_batch.rs, module header). */
+/* The widest batch one launch train takes: memra refuses B > 16 because above
+ * it its kernels change numeric configuration and rows are no longer exact
+ * (decode_batch.rs, module header).  kd_decode_step takes larger batches as
+ * consecutive groups of at most KD_MAX_BATCH rows on the same kernels, so
+ * every row stays exact. */
 #define KD_MAX_BATCH 16
 
 typedef void* kd_stream;          /* cudaStream_t */
@@ -75,6 +77,14 @@ typedef struct {
  * two schedules).  Default: chosen per matrix from its shape and the SM count. */
 #define KD_FLAG_SCHEDULE_STREAM 2
 #define KD_FLAG_SCHEDULE_GROUP 4
+/* Fold the RMSNorm before q|k|v and gate|up into those projections' activation
+ * load (each warp forms its k-range of the normed input from the fp32 residual
+ * and the per-group sums of squares) instead of running it as a kernel of its
+ * own.  The results are bit-identical either way.  Off by default: on GB300 the
+ * folded load (every CTA reading the whole fp32 residual before its first MMA)
+ * measured slower than the separate kernel, whose latency overlaps the next
+ * projection's weight prefetch. */
+#define KD_FLAG_FUSED_NORM 32
 
 /* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
  * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the
@@ -157,6 +167,12 @@ kd_status kd_session_length(const kd_model* m, int32_t session_id, int32_t* len_
 
 /* One batched decode step (memra decode_batch.rs `decode_step_batch`: row b is
  * session b with its own cache and position; every projection runs at m = B).
+ *   B: 1 .. max_sessions.  Up to KD_MAX_BATCH rows go through one launch train;
+ *     a larger B runs as consecutive groups of at most KD_MAX_BATCH rows (rows
+ *     0..15, 16..31, ...), each reading the weights once, with the same
+ *     per-row arithmetic (every row equal to its B = 1 result).  memra refuses
+ *     B > 16 and leaves wider concurrency to its serve scheduler, which splits
+ *     it into groups of at most 16 (decode_batch.rs, `decode_step_batch`). 
  *   session_ids, tokens, positions: host arrays of length B.  Ids must be bound
  *     and distinct; tokens in [0, vocab); 0 <= positions[b] <= length(session)
  *     and positions[b] < max_ctx.  The token is written to the cache at
@@ -185,8 +201,8 @@ kd_status kd_decode_step(kd_model* m, const int32_t* session_ids, const int32_t*
 kd_status kd_debug_capture_hidden(kd_model* m, float* dev_buf);
 
 /* Debug: run decoder layer `layer` alone on the residual rows x_in (device or
- * host fp32 [B][hidden]) for the given sessions at the given positions (same
- * rules as kd_decode_step), writing the layer's output rows to x_out (device or
+ * host fp32 [B][hidden], B <= KD_MAX_BATCH) for the given sessions at the given
+ * positions (same rules as kd_decode_step), writing the layer's output rows to x_out (device or
  * host fp32 [B][hidden]).  Writes that layer's K/V row at each position; does
  * not change any session's length.  The same kernels as a step run, so a layer
  * can be checked on its own against a reference, without errors carried in from

@@ -336,10 +336,21 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     return KD_OK;
 }
 
+// Whether a projection fed by an RMSNorm takes the norm inside its activation
+// load (group schedule, K <= 4096) rather than after a norm kernel of its own.
+static bool fused_norm(const kd_model* m, const PackedQ8& p) {
+    return (m->cfg.flags & KD_FLAG_FUSED_NORM) && p.mode == kd::MMVQ_GROUP &&
+           p.KG <= kd::MMVQ_WARPS * kd::NORM_IN_MAX_KG;
+}
+
 // The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
 // With only_layer >= 0: that layer alone, on residual rows already in m->x and
-// their normed rows in m->xn; no embedding, no head.
-static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1) {
+// their per-group sums of squares in m->ssq; no embedding, no head.
+// Hidden-state capture (kd_debug_capture_hidden) of a chunk of a larger step:
+// its rows start at hrow0 of the step's hB rows.
+static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1,
+                                int hrow0 = 0, int hB = 0) {
+    if (hB == 0) hB = B;
     const kd_config& c = m->cfg;
     const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
     const int F = c.ffn, V = c.vocab;
@@ -401,26 +412,34 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         m->inject_cls = -1;
         return 16;
     };
-    // RMSNorm: the embedding writes the first normed input itself; the residual
-    // writers (o-proj, down) leave per-group sums of squares, and an elementwise
-    // kernel forms the next projection's normed fp16 input m->xn from them.
+    // RMSNorm: the residual writers (embedding, o-proj, down) leave per-group sums
+    // of squares; q|k|v and gate|up form their normed fp16 input from them inside
+    // their activation load (fused_norm), else an elementwise kernel forms m->xn.
     auto resid = [&](kd::MmvqArgs& a) {
         a.y = m->x; a.ld = H; a.ssq_out = m->ssq;
     };
     auto norm = [&](const float* w) {
         return kd::launch_norm_from_ssq(m->x, m->ssq, B, H, w, c.rms_eps, m->xn, pdl, s, tl_next());
     };
+    auto norm_in = [&](kd::MmvqArgs& a, const float* w) {
+        a.nx = m->x; a.nssq = m->ssq; a.nw = w; a.neps = c.rms_eps;
+    };
     const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
     const bool whole = only_layer < 0;
     if (whole)
-        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->norms, c.rms_eps, m->xn, pdl, s, tl_next()));
+        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->ssq, pdl, s, tl_next()));
     if (whole && m->hidden_dbg &&
-        (e = cudaMemcpyAsync(m->hidden_dbg, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)hrow0 * H, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
+                             s)) != cudaSuccess)
         return e;
     for (int l = l0; l < l1; ++l) {
         __half* kc = m->kc + (size_t)l * m->layer_kv;
         __half* vc = m->vc + (size_t)l * m->layer_kv;
+        const float* attn_w = m->norms + (size_t)(2 * l) * H;
+        const bool fq = fused_norm(m, m->qkv[l]);
+        if (!fq) KD_RUN(KD_K_RMSNORM, norm(attn_w));
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
+        if (fq) norm_in(a, attn_w);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
         a.inject_tx = inject(KD_K_QKV);
@@ -441,8 +460,11 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.inject_tx = inject(KD_K_WO);
         a.tl = tl_next();
         KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
-        KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * l + 1) * H));  // the FFN norm
+        const float* ffn_w = m->norms + (size_t)(2 * l + 1) * H;
+        const bool fg = fused_norm(m, m->gu[l]);
+        if (!fg) KD_RUN(KD_K_RMSNORM, norm(ffn_w));
         a = mm(m->gu[l], m->xn);
+        if (fg) norm_in(a, ffn_w);
         a.act = m->act; a.ld = F;
         a.inject_tx = inject(KD_K_GATE_UP);
         a.tl = tl_next();
@@ -452,14 +474,13 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.inject_tx = inject(KD_K_DOWN);
         a.tl = tl_next();
         KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
-        if (whole || l + 1 < l1)  // next layer's attention norm, or the output norm
-            KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(l + 1 < L ? 2 * (l + 1) : 2 * L) * H));
         if (whole && m->hidden_dbg &&
-            (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)(l + 1) * B * H, m->x, (size_t)B * H * 4,
+            (e = cudaMemcpyAsync(m->hidden_dbg + ((size_t)(l + 1) * hB + hrow0) * H, m->x, (size_t)B * H * 4,
                                  cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
             return e;
     }
     if (!whole) return cudaSuccess;
+    KD_RUN(KD_K_RMSNORM, norm(m->norms + (size_t)(2 * L) * H));  // the output norm
     kd::MmvqArgs a = mm(m->head, m->xn);
     a.y = lg; a.ld = V;
     a.inject_tx = inject(KD_K_LM_HEAD);
@@ -604,8 +625,8 @@ kd_status kd_session_load_kv(kd_model* m, int32_t id, const void* k, const void*
 }
 
 static kd_status check_rows(kd_model* m, const char* fn, const int32_t* ids, const int32_t* tokens,
-                            const int32_t* positions, int32_t B) {
-    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "%s: B=%d outside [1, %d]", fn, B, KD_MAX_BATCH);
+                            const int32_t* positions, int32_t B, int32_t max_b) {
+    if (B < 1 || B > max_b) return fail(KD_ERR_BATCH, "%s: B=%d outside [1, %d]", fn, B, max_b);
     if (!ids || !positions) return fail(KD_ERR_INVALID_ARG, "%s: null host array", fn);
     const kd_config& c = m->cfg;
     for (int b = 0; b < B; ++b) {
@@ -646,26 +667,32 @@ kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens,
                          int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
     if (!m) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null model");
     if (!tokens && B >= 1 && B <= KD_MAX_BATCH) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
-    kd_status st0 = check_rows(m, "kd_decode_step", ids, tokens, positions, B);
+    // Any number of distinct bound sessions; above KD_MAX_BATCH the step runs as
+    // consecutive groups of at most KD_MAX_BATCH rows on the same kernels.
+    kd_status st0 = check_rows(m, "kd_decode_step", ids, tokens, positions, B, (int32_t)m->bound.size());
     if (st0 != KD_OK) return st0;
     if (reinterpret_cast<uintptr_t>(logits_out) & 15)
         return fail(KD_ERR_INVALID_ARG, "kd_decode_step: logits_out must be 16-byte aligned");
     const kd_config& c = m->cfg;
     KD_CK(cudaSetDevice(m->dev));
     cudaStream_t s = (cudaStream_t)stream;
-    st0 = stage_descriptor(m, ids, tokens, positions, B, s);
-    if (st0 != KD_OK) return st0;
-
-    float* lg = logits_out ? logits_out : m->logits_ws;
-    if (m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH) || m->inject_cls >= 0) {
-        KD_CK(enqueue_step(m, B, lg, argmax_out, s));
-    } else {
-        cudaGraphExec_t g = nullptr;
-        kd_status st = get_graph(m, B, lg, argmax_out, &g);
-        if (st != KD_OK) return st;
-        KD_CK(cudaGraphLaunch(g, s));
+    const bool direct = m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH) || m->inject_cls >= 0;
+    for (int r0 = 0; r0 < B; r0 += KD_MAX_BATCH) {
+        const int n = std::min(B - r0, KD_MAX_BATCH);
+        st0 = stage_descriptor(m, ids + r0, tokens + r0, positions + r0, n, s);
+        if (st0 != KD_OK) return st0;
+        float* lg = logits_out ? logits_out + (size_t)r0 * c.vocab : m->logits_ws;
+        int* am = argmax_out ? argmax_out + r0 : nullptr;
+        if (direct) {
+            KD_CK(enqueue_step(m, n, lg, am, s, -1, r0, B));
+        } else {
+            cudaGraphExec_t g = nullptr;
+            kd_status st = get_graph(m, n, lg, am, &g);
+            if (st != KD_OK) return st;
+            KD_CK(cudaGraphLaunch(g, s));
+        }
+        KD_CK(cudaEventRecord(m->last_step, s));
     }
-    KD_CK(cudaEventRecord(m->last_step, s));
     for (int b = 0; b < B; ++b) m->len[ids[b]] = positions[b] + 1;
     return KD_OK;
 }
@@ -675,7 +702,7 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const i
     if (!m || !x_in || !x_out) return fail(KD_ERR_INVALID_ARG, "kd_debug_layer: null argument");
     if (layer < 0 || layer >= m->cfg.n_layers)
         return fail(KD_ERR_INVALID_ARG, "kd_debug_layer: layer %d outside [0, %d)", layer, m->cfg.n_layers);
-    kd_status st = check_rows(m, "kd_debug_layer", ids, nullptr, positions, B);
+    kd_status st = check_rows(m, "kd_debug_layer", ids, nullptr, positions, B, KD_MAX_BATCH);
     if (st != KD_OK) return st;
     KD_CK(cudaSetDevice(m->dev));
     cudaStream_t s = (cudaStream_t)stream;
@@ -683,11 +710,9 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const i
     if (st != KD_OK) return st;
     const size_t bytes = (size_t)B * m->cfg.hidden * sizeof(float);
     KD_CK(cudaMemcpyAsync(m->x, x_in, bytes, cudaMemcpyDefault, s));
-    // The layer's attention norm through the step's own norm kernel: sums of
-    // squares per 32-row group (as a residual writer leaves them), then xn.
+    // The per-group sums of squares of the rows (as a residual writer leaves them);
+    // the layer then forms its attention norm from them as in a step.
     KD_CK(kd::launch_ssq_rows(m->x, B, m->cfg.hidden, m->ssq, s));
-    KD_CK(kd::launch_norm_from_ssq(m->x, m->ssq, B, m->cfg.hidden, m->norms + (size_t)(2 * layer) * m->cfg.hidden,
-                                   m->cfg.rms_eps, m->xn, false, s));
     const bool prof = m->prof;
     m->prof = false;
     cudaError_t e = enqueue_step(m, B, nullptr, nullptr, s, layer);
@@ -719,10 +744,13 @@ kd_status kd_profile_timeline(kd_model* m, uint64_t* dev_buf, int32_t max_launch
         const int L = m->cfg.n_layers;
         std::vector<int32_t> cls;
         cls.push_back(KD_K_EMBED);
-        for (int l = 0; l < L; ++l)
-            for (int k : {KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO, KD_K_RMSNORM, KD_K_GATE_UP,
-                          KD_K_DOWN, KD_K_RMSNORM})
-                cls.push_back(k);
+        for (int l = 0; l < L; ++l) {
+            if (!fused_norm(m, m->qkv[l])) cls.push_back(KD_K_RMSNORM);
+            for (int k : {KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO}) cls.push_back(k);
+            if (!fused_norm(m, m->gu[l])) cls.push_back(KD_K_RMSNORM);
+            for (int k : {KD_K_GATE_UP, KD_K_DOWN}) cls.push_back(k);
+        }
+        cls.push_back(KD_K_RMSNORM);
         cls.push_back(KD_K_LM_HEAD);
         cls.push_back(KD_K_ARGMAX);
         for (int i = 0; i < max_launches; ++i) classes_out[i] = i < (int)cls.size() ? cls[i] : -1;

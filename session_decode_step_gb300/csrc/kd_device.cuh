@@ -185,6 +185,39 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- RMSNorm from per-group sums of squares -----------------------------------
+// r = 1 / sqrt(sum_g ssq[g][b] / H + eps) for the H/32 groups a residual writer
+// left: lane l adds groups l, l + 32, ... in order (the first add is exact),
+// then a fixed shuffle tree; every lane returns the same value.  The RMSNorm
+// kernel (rms_factor_from_ssq) and the fused activation load
+// (rms_factor_from_parts, with the lane's values loaded ahead: groups
+// lane + 32 i, i < 4, for H <= 4096) do exactly this arithmetic.
+__device__ __forceinline__ float rms_factor_from_parts(const float (&pre)[NORM_IN_MAX_KG], int lane, int H, float eps) {
+    const int ng = H / 32;
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NORM_IN_MAX_KG; ++i)
+        if (lane + 32 * i < ng) s = __fadd_rn(s, pre[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
+}
+__device__ __forceinline__ void rms_parts_load(const float* ssq, int b, int lane, int H, float (&pre)[NORM_IN_MAX_KG]) {
+    const int ng = H / 32;
+#pragma unroll
+    for (int i = 0; i < NORM_IN_MAX_KG; ++i)
+        pre[i] = lane + 32 * i < ng ? __ldcg(ssq + (size_t)(lane + 32 * i) * MAX_NORM_SLOTS + b) : 0.0f;
+}
+
+__device__ __forceinline__ float rms_factor_from_ssq(const float* ssq, int b, int lane, int H, float eps) {
+    const int ng = H / 32;
+    float s = 0.0f;
+    for (int g = lane; g < ng; g += 32) s = __fadd_rn(s, __ldcg(ssq + (size_t)g * MAX_NORM_SLOTS + b));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
+}
+
 // ---- exact int8 -> fp16 ----------------------------------------------------
 // The repacked weights hold u = q + 128 (0..255).  Placing u under the fp16
 // exponent of 1024 gives the half 1024 + u exactly (the fp16 spacing there is

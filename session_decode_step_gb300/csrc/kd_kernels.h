@@ -45,6 +45,9 @@ constexpr int TL_CTAS = 1024;
 constexpr int TL_WORDS = 4;
 
 constexpr int MAX_NORM_SLOTS = 16;  // sum-of-squares tables hold one entry per session slot 0..15
+// The fused-norm activation load keeps a warp's whole k-range of normed tiles in
+// shared memory: at most this many 128-column k-groups per warp (K <= 4096).
+constexpr int NORM_IN_MAX_KG = 4;
 
 enum MmvqMode : int {
     MMVQ_STREAM = 0,  // warps stream equal contiguous shares; partials of shared groups via global memory
@@ -100,6 +103,14 @@ struct MmvqArgs {
     // warp 0 waits for, so that its bounded wait runs out (no copy is touched).
     int inject_tx;
     unsigned long long* tl;  // timeline records of this launch, or nullptr
+    // RMSNorm fused into the activation load (group schedule only; nx == nullptr
+    // otherwise): x is then xn = fp16(nx * r_b * nw), r_b = 1 / sqrt(sum_g
+    // nssq[g][b] / K + neps), formed by each warp for its own k-groups once, in
+    // the RMSNorm kernel's order and roundings (the same bits as that kernel).
+    const float* nx;     // [B][K] fp32 residual rows
+    const float* nssq;   // [K/32][16] per-group sums of squares the residual writer left
+    const float* nw;     // [K] norm weight
+    float neps;
     int ld;              // row stride (elements) of the epilogue output
     float* y;            // EPI_STORE / EPI_RESID target
     __half* act;         // EPI_SWIGLU target
@@ -161,10 +172,10 @@ cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half*
                              const int* pos, int B, int nkv, int hd, int cap, cudaStream_t s);
 
 // ---- row ops -----------------------------------------------------------------
-// x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and the first
-// layer's normed input xn[b][:] = fp16(x[b] / sqrt(mean(x[b]^2) + eps) * w)
-cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl = nullptr);
+// x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and, as a residual
+// writer leaves them, the per-group sums of squares ssq[g][b] of those rows
+cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq, bool pdl,
+                         cudaStream_t s, unsigned long long* tl = nullptr);
 // ssq[g][b] = sum of x[b][32g .. 32g+31]^2 for rows supplied from outside, in
 // the residual writers' group layout and summation order
 cudaError_t launch_ssq_rows(const float* x, int B, int H, float* ssq, cudaStream_t s);

@@ -89,6 +89,106 @@ __device__ __forceinline__ void lds_x_tile(const uint8_t* xt, int gq, int cq, ui
             xv[kb][nt] = lds_v4(xt + (nt * 2 + (kb >> 1)) * 1024 + row * 128 + ((((kb & 1) * 4 + cq) ^ row) << 4));
 }
 
+// fp16(x * r * w) of two neighbouring elements, as an fp16 pair (first element low)
+__device__ __forceinline__ uint32_t norm_pair(float x0, float x1, float r, float w0, float w1) {
+    const __half2 t = __floats2half2_rn(__fmul_rn(__fmul_rn(x0, r), w0), __fmul_rn(__fmul_rn(x1, r), w1));
+    return *reinterpret_cast<const uint32_t*>(&t);
+}
+
+// The fused activation load: this warp's normed input tiles for k-groups
+// kg0 .. kg0 + nk - 1 (nk <= NORM_IN_MAX_KG), xn[s][k] = fp16(x[s][k] * r_s * w[k])
+// for the launch's sessions (zero for the unused ones), written as the
+// activation tensor map would deliver them: per k-group and 8 sessions, two
+// 64-column halves of [8 rows][128 B], 16-byte chunk c of row r at chunk c ^ r.
+// CTA-collective (every warp calls it, nk may be 0): warp 0 forms the sessions'
+// norm factors r_s (rms_factor_from_ssq's order) into rsm[] while the other
+// warps' x loads are in flight.  Lane (p, c) handles column chunk c (8 columns)
+// of sessions p, p + 2, ...; two k-groups' loads are in flight at a time.
+template <int NT>
+__device__ __forceinline__ void norm_tiles(const MmvqArgs& a, int warp, int lane, int kg0, int nk, uint8_t* xt,
+                                           float* rsm) {
+    constexpr int SPL = 4 * NT;  // sessions per lane
+    const int c = lane & 15, p = lane >> 4;
+    float4 xv[2][SPL][2], wv[2][2];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int kk = k0 + u;
+            if (kk < nk) {
+                const int col = (kg0 + kk) * KGROUP + 8 * c;
+                wv[u][0] = __ldg(reinterpret_cast<const float4*>(a.nw + col));
+                wv[u][1] = __ldg(reinterpret_cast<const float4*>(a.nw + col + 4));
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) {
+                    const int s = p + 2 * j;
+                    if (s < a.B) {
+                        const float* xp = a.nx + (size_t)s * a.K + col;
+                        xv[u][j][0] = __ldcg(reinterpret_cast<const float4*>(xp));
+                        xv[u][j][1] = __ldcg(reinterpret_cast<const float4*>(xp + 4));
+                    }
+                }
+            }
+        }
+    };
+    load(0);
+    if (warp == 0) {
+        // r_s: lane l holds groups l, l + 32, l + 64, l + 96 of every session (a
+        // sums-of-squares row is 16 sessions, 64 bytes), added in that order.
+        const int ng = a.K / 32;
+        float4 pre[NORM_IN_MAX_KG][2 * NT];
+#pragma unroll
+        for (int i = 0; i < NORM_IN_MAX_KG; ++i)
+#pragma unroll
+            for (int q = 0; q < 2 * NT; ++q)
+                pre[i][q] = lane + 32 * i < ng
+                                ? __ldcg(reinterpret_cast<const float4*>(a.nssq + (size_t)(lane + 32 * i) * MAX_NORM_SLOTS) + q)
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int q = 0; q < 2 * NT; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float sv = 0.0f;
+#pragma unroll
+                for (int i = 0; i < NORM_IN_MAX_KG; ++i) {
+                    const float v = e == 0 ? pre[i][q].x : e == 1 ? pre[i][q].y : e == 2 ? pre[i][q].z : pre[i][q].w;
+                    if (lane + 32 * i < ng) sv = __fadd_rn(sv, v);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sv = __fadd_rn(sv, __shfl_xor_sync(FULL_MASK, sv, o));
+                if (lane == 0) rsm[4 * q + e] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sv, (float)a.K), a.neps)));
+            }
+    }
+    __syncthreads();
+    float r[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) r[j] = rsm[p + 2 * j];
+#pragma unroll
+    for (int k0 = 0; k0 < NORM_IN_MAX_KG; k0 += 2) {
+        if (k0 > 0) load(k0);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int kk = k0 + u;
+            if (kk < nk) {
+#pragma unroll
+                for (int j = 0; j < SPL; ++j) {
+                    const int s = p + 2 * j;
+                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                    if (s < a.B) {
+                        o.x = norm_pair(xv[u][j][0].x, xv[u][j][0].y, r[j], wv[u][0].x, wv[u][0].y);
+                        o.y = norm_pair(xv[u][j][0].z, xv[u][j][0].w, r[j], wv[u][0].z, wv[u][0].w);
+                        o.z = norm_pair(xv[u][j][1].x, xv[u][j][1].y, r[j], wv[u][1].x, wv[u][1].y);
+                        o.w = norm_pair(xv[u][j][1].z, xv[u][j][1].w, r[j], wv[u][1].z, wv[u][1].w);
+                    }
+                    const int nt = s >> 3, rr = s & 7;
+                    uint8_t* dst = xt + (size_t)kk * NT * XTILE_BYTES + (nt * 2 + (c >> 3)) * 1024 + rr * 128 +
+                                   (((c & 7) ^ rr) << 4);
+                    *reinterpret_cast<uint4*>(dst) = o;
+                }
+            }
+        }
+    }
+}
+
 // ---- epilogues on single outputs ------------------------------------------
 // Row r (0..31) of row group g, session n, value v.
 __device__ __forceinline__ void epi_store(const MmvqArgs& a, int g, int r, int n, float v) {

@@ -16,13 +16,19 @@ namespace kd {
 // PAIR: a launch with one CTA per group for SMs < G <= 2 * SMs (B <= 8): a
 // shallower ring and the partial buffer laid over it let two CTAs share an SM,
 // so no CTA waits for a second group while others idle.
-// Shared memory: per warp a ring of RD stages, each the stage's weights and its
-// activation tiles; then the barriers and the partial-sum buffer.
-template <int NT, bool PAIR>
+// NIN: the RMSNorm fused into the activation load (MmvqArgs::nx): each warp
+// forms its whole k-range of normed tiles once, after the dependency wait, and
+// keeps them for all its groups; the ring then carries weights only.
+// Shared memory: per warp a ring of RD stages of weights, and its activation
+// tiles (one per ring stage, or NIN: one per k-group of its range); then the
+// barriers and the partial-sum buffer.
+template <int NT, bool PAIR, bool NIN>
 struct CtaSmem {
-    static constexpr int RD = PAIR ? 2 : 3;  // stages in flight per warp (measured best for the step)
+    static_assert(!(PAIR && NIN), "the fused norm's tiles do not fit two CTAs per SM");
+    static constexpr int RD = PAIR || (NIN && NT == 2) ? 2 : 3;  // stages in flight per warp (measured best)
     static constexpr int RS = NT == 1 ? 9 : 16;  // partial-row stride (floats), padded against bank conflicts
-    static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * RD * NT * XTILE_BYTES;  // at a 1024-byte boundary
+    static constexpr int XT = NIN ? NORM_IN_MAX_KG : RD;  // activation tiles per warp
+    static constexpr size_t X_BYTES = (size_t)MMVQ_WARPS * XT * NT * XTILE_BYTES;  // at a 1024-byte boundary
     static constexpr size_t W_OFF = X_BYTES;
     static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
     static constexpr size_t BAR_OFF = W_OFF + RING_BYTES;
@@ -33,19 +39,19 @@ struct CtaSmem {
     static_assert(!PAIR || RED_BYTES <= RING_BYTES, "the partial buffer lies over the ring");
 };
 
-template <int NT, int EPI, bool PAIR>
-__global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
+template <int NT, int EPI, bool PAIR, bool NIN>
+__global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 && !NIN ? 2 : 1)
     mmvq_cta_kernel(const MmvqArgs a, const __grid_constant__ CUtensorMap xm) {
-    using L = CtaSmem<NT, PAIR>;
+    using L = CtaSmem<NT, PAIR, NIN>;
     constexpr int RD = L::RD;
-    constexpr uint32_t SB = STAGE_BYTES + NT * XTILE_BYTES;  // bytes a stage's barrier waits for
+    constexpr uint32_t SB = STAGE_BYTES + (NIN ? 0 : NT * XTILE_BYTES);  // bytes a stage's barrier waits for
     static_assert(!PAIR || NT == 1, "two CTAs per SM need the one-tile register budget");
     extern __shared__ uint8_t smem_raw[];
     tl_entry(a.tl);
     uint8_t* smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
-    uint8_t* xring = smem + (size_t)warp * RD * NT * XTILE_BYTES;
+    uint8_t* xring = smem + (size_t)warp * L::XT * NT * XTILE_BYTES;
     uint8_t* ring = smem + L::W_OFF + (size_t)warp * RD * STAGE_BYTES;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * RD;
     float* red = reinterpret_cast<float*>(smem + L::RED_OFF);  // [warp][32 rows][RS]
@@ -85,9 +91,15 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(a.tl);
-    if (lane == 0)
-        for (int i = 0; i < RD && i < total; ++i)
-            tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);
+    if constexpr (NIN) {
+        // the warp's normed k-range, once (the partial buffer holds the norm factors meanwhile)
+        norm_tiles<NT>(a, warp, lane, kg0, ngrp > 0 ? nk : 0, xring, red);
+        __syncthreads();  // red is the partial buffer again
+    } else {
+        if (lane == 0)
+            for (int i = 0; i < RD && i < total; ++i)
+                tma_x_tile<NT>(xring + i * NT * XTILE_BYTES, &xm, kg0 + i % nk, &bar[i]);
+    }
 
     int sidx = 0, slot = 0;
     uint32_t phase = 0;
@@ -126,12 +138,13 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
                 break;
             }
             uint4 xv[4][NT];
-            lds_x_tile<NT>(xring + slot * NT * XTILE_BYTES, gq, cq, xv);
+            lds_x_tile<NT>(xring + (NIN ? kk : slot) * NT * XTILE_BYTES, gq, cq, xv);
             mma_stage<NT>(ring + slot * STAGE_BYTES, lane, gq, xv, acc);
             __syncwarp();
             if (lane == 0 && sidx + RD < total) {
                 issue_w(slot);
-                tma_x_tile<NT>(xring + slot * NT * XTILE_BYTES, &xm, kg0 + (sidx + RD) % nk, &bar[slot]);
+                if constexpr (!NIN)
+                    tma_x_tile<NT>(xring + slot * NT * XTILE_BYTES, &xm, kg0 + (sidx + RD) % nk, &bar[slot]);
             }
             if (++slot == RD) { slot = 0; phase ^= 1u; }
         }
@@ -184,40 +197,46 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 ? 2 : 1)
     tl_exit(a.tl);
 }
 
-template <int NT, int EPI, bool PAIR>
+template <int NT, int EPI, bool PAIR, bool NIN>
 static cudaError_t cta_attr() {
-    cudaError_t e = cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)CtaSmem<NT, PAIR>::TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR, NIN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)CtaSmem<NT, PAIR, NIN>::TOTAL);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(mmvq_cta_kernel<NT, EPI, PAIR, NIN>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
-template <int NT, int EPI, bool PAIR>
+template <int NT, int EPI, bool PAIR, bool NIN>
 static cudaError_t cta_launch(const MmvqArgs& a, const CUtensorMap& xm, int grid, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(MMVQ_WARPS * 32);
-    cfg.dynamicSmemBytes = CtaSmem<NT, PAIR>::TOTAL;
+    cfg.dynamicSmemBytes = CtaSmem<NT, PAIR, NIN>::TOTAL;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI, PAIR>, a, xm);
+    return cudaLaunchKernelEx(&cfg, mmvq_cta_kernel<NT, EPI, PAIR, NIN>, a, xm);
 }
 
 #define KD_CTA_CASES(X, NT_, PAIR_) \
-    X(NT_, EPI_STORE, PAIR_) X(NT_, EPI_SWIGLU, PAIR_) X(NT_, EPI_QKV, PAIR_) X(NT_, EPI_RESID, PAIR_)
+    X(NT_, EPI_STORE, PAIR_, false) X(NT_, EPI_SWIGLU, PAIR_, false) X(NT_, EPI_QKV, PAIR_, false) \
+    X(NT_, EPI_RESID, PAIR_, false)
+// the fused norm feeds the projections after an RMSNorm: q|k|v and gate|up
+#define KD_CTA_NIN_CASES(X, NT_) X(NT_, EPI_SWIGLU, false, true) X(NT_, EPI_QKV, false, true)
 
 cudaError_t mmvq_cta_init_attributes() {
     cudaError_t e;
-#define KD_A(NT_, EPI_, PAIR_) \
-    if ((e = cta_attr<NT_, EPI_, PAIR_>()) != cudaSuccess) return e;
+#define KD_A(NT_, EPI_, PAIR_, NIN_) \
+    if ((e = cta_attr<NT_, EPI_, PAIR_, NIN_>()) != cudaSuccess) return e;
     KD_CTA_CASES(KD_A, 1, false)
     KD_CTA_CASES(KD_A, 2, false)
     KD_CTA_CASES(KD_A, 1, true)
+    KD_CTA_NIN_CASES(KD_A, 1)
+    KD_CTA_NIN_CASES(KD_A, 2)
 #undef KD_A
     return cudaSuccess;
 }
@@ -225,20 +244,25 @@ cudaError_t mmvq_cta_init_attributes() {
 // One CTA per group when the groups outnumber the SMs by at most 2x and the
 // one-tile kernel is used (two CTAs fit an SM); otherwise min(G, SMs) CTAs that
 // each take groups c, c + grid, ...
-int mmvq_cta_grid(int G, int B, int num_sms, bool* pair) {
-    *pair = B <= 8 && G > num_sms && G <= 2 * num_sms;
+int mmvq_cta_grid(int G, int B, int num_sms, bool fused_norm, bool* pair) {
+    *pair = !fused_norm && B <= 8 && G > num_sms && G <= 2 * num_sms;
     return *pair ? G : (G < num_sms ? G : num_sms);
 }
 
 cudaError_t launch_mmvq_cta(const MmvqArgs& a, const CUtensorMap& xm, int epi, int num_sms, bool pdl, cudaStream_t s) {
-    const bool wide = a.B > 8;
+    const bool wide = a.B > 8, nin = a.nx != nullptr;
+    if (nin && (a.KG > MMVQ_WARPS * NORM_IN_MAX_KG || (epi != EPI_QKV && epi != EPI_SWIGLU)))
+        return cudaErrorInvalidValue;
     bool pair = false;
-    const int grid = mmvq_cta_grid(a.G, a.B, num_sms, &pair);
-#define KD_L(NT_, EPI_, PAIR_) \
-    if (epi == EPI_ && (NT_ == 2) == wide && PAIR_ == pair) return cta_launch<NT_, EPI_, PAIR_>(a, xm, grid, pdl, s);
+    const int grid = mmvq_cta_grid(a.G, a.B, num_sms, nin, &pair);
+#define KD_L(NT_, EPI_, PAIR_, NIN_)                                  \
+    if (epi == EPI_ && (NT_ == 2) == wide && PAIR_ == pair && NIN_ == nin) \
+        return cta_launch<NT_, EPI_, PAIR_, NIN_>(a, xm, grid, pdl, s);
     KD_CTA_CASES(KD_L, 1, false)
     KD_CTA_CASES(KD_L, 2, false)
     KD_CTA_CASES(KD_L, 1, true)
+    KD_CTA_NIN_CASES(KD_L, 1)
+    KD_CTA_NIN_CASES(KD_L, 2)
 #undef KD_L
     return cudaErrorInvalidValue;
 }

@@ -15,106 +15,22 @@ namespace kd {
 
 constexpr int EMBED_THREADS = 256;
 
-// 1 / sqrt(mean(x^2) + eps) of a row from each thread's share of its sum of
-// squares, added in a fixed order: a fixed shuffle tree, then warps in order.
-__device__ __forceinline__ float block_rms_factor(float ss_thread, int H, float eps) {
-    __shared__ float wsum[EMBED_THREADS / 32];
-    __shared__ float rsh;
-    const int tid = threadIdx.x;
-    float s = ss_thread;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
-    if ((tid & 31) == 0) wsum[tid >> 5] = s;
-    __syncthreads();
-    if (tid == 0) {
-        float t = wsum[0];
-        for (int i = 1; i < EMBED_THREADS / 32; ++i) t = __fadd_rn(t, wsum[i]);
-        rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), eps)));
-    }
-    __syncthreads();
-    return rsh;
-}
-
-// out[i] = fp16(x[i] / sqrt(mean(x^2) + eps) * w[i]) for the row x[0..H) already
-// in global memory (written by this CTA); ss_thread: this thread's share of the
-// sum of squares (its elements tid, tid + 256, ... in order).
-__device__ __forceinline__ void norm_row(const float* x, int H, const float* w, float eps, __half* out,
-                                         float ss_thread) {
-    const int tid = threadIdx.x;
-    const float r = block_rms_factor(ss_thread, H, eps);
-    constexpr int U = 16;  // loads issued together
-    for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
-        float xv[U], wv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + tid + EMBED_THREADS * u;
-            xv[u] = i < H ? x[i] : 0.0f;
-            wv[u] = i < H ? w[i] : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + tid + EMBED_THREADS * u;
-            if (i < H) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(xv[u], r), wv[u]));
-        }
-    }
-}
-
-// x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), then the
-// first layer's normed input xn[b] = fp16(rmsnorm(x[b]) * w).
+// x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), and the
+// per-group sums of squares ssq[g][b] of the row, as a residual writer leaves
+// them for the next RMSNorm: warp w holds elements 256u + 32w + lane, i.e.
+// group 8u + w with lane = row, added by the same shuffle tree.
 __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __restrict__ emb,
                                                               const int* __restrict__ token, int H,
-                                                              float* __restrict__ x, const float* __restrict__ w,
-                                                              float eps, __half* __restrict__ xn,
+                                                              float* __restrict__ x, float* __restrict__ ssq,
                                                               unsigned long long* tl) {
     tl_entry(tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(tl);
-    const int b = blockIdx.x, tid = threadIdx.x;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float* xr = x + (size_t)b * H;
-    constexpr int U = 16;  // elements per thread whose loads are issued together
-    if (H <= EMBED_THREADS * U) {
-        // The whole row in registers: the norm's weights load with the token's
-        // row, and the norm reads x from registers (the same arithmetic as below).
-        float wv[U], xv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + EMBED_THREADS * u;
-            wv[u] = i < H ? w[i] : 0.0f;
-        }
-        const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
-        int8_t q[U];
-        unsigned short dbits[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + EMBED_THREADS * u;
-            const uint8_t* blk = row + (i >> 5) * 34;
-            q[u] = i < H ? (int8_t)blk[2 + (i & 31)] : (int8_t)0;
-            dbits[u] = i < H ? (unsigned short)(blk[0] | (blk[1] << 8)) : (unsigned short)0;
-        }
-        float s = 0.0f;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + EMBED_THREADS * u;
-            const __half_raw hr{dbits[u]};
-            xv[u] = __fmul_rn((float)q[u], __half2float(__half(hr)));
-            if (i < H) {
-                xr[i] = xv[u];
-                s = __fmaf_rn(xv[u], xv[u], s);
-            }
-        }
-        const float r = block_rms_factor(s, H, eps);
-        __half* out = xn + (size_t)b * H;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + EMBED_THREADS * u;
-            if (i < H) out[i] = __float2half_rn(__fmul_rn(__fmul_rn(xv[u], r), wv[u]));
-        }
-        tl_exit(tl);
-        return;
-    }
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
-    float s = 0.0f;
+    constexpr int U = 16;  // elements per thread whose loads are issued together
     for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
         int8_t q[U];
         unsigned short dbits[U];
@@ -128,15 +44,17 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int i = i0 + tid + EMBED_THREADS * u;
-            if (i < H) {
+            if (i0 + EMBED_THREADS * u + 32 * warp < H) {  // the warp's 32 elements: one whole group
                 const __half_raw hr{dbits[u]};
                 const float v = __fmul_rn((float)q[u], __half2float(__half(hr)));
                 xr[i] = v;
-                s = __fmaf_rn(v, v, s);
+                float s = __fmul_rn(v, v);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
+                if (lane == 0) ssq[(size_t)(i >> 5) * MAX_NORM_SLOTS + b] = s;
             }
         }
     }
-    norm_row(xr, H, w, eps, xn + (size_t)b * H, s);  // each thread re-reads only what it wrote
     tl_exit(tl);
 }
 
@@ -186,24 +104,8 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_from_ssq_kernel(const float
     const float4 v = i < H ? *reinterpret_cast<const float4*>(x + (size_t)b * H + i) : make_float4(0, 0, 0, 0);
     const float4 g = i < H ? *reinterpret_cast<const float4*>(w + i) : make_float4(0, 0, 0, 0);
     if (tid < 32) {
-        // lane l adds groups l, l + 32, l + 64, ... in order; the loads of 8 of
-        // them are issued together
-        const int ng = H / 32;
-        float s = 0.0f;
-        for (int g0 = 0; g0 < ng; g0 += 8 * 32) {
-            float part[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int gi = g0 + tid + 32 * j;
-                part[j] = gi < ng ? ssq[(size_t)gi * MAX_NORM_SLOTS + b] : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (g0 + tid + 32 * j < ng) s = __fadd_rn(s, part[j]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
-        if (tid == 0) rsh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
+        const float r = rms_factor_from_ssq(ssq, b, tid, H, eps);  // the shared order (kd_device.cuh)
+        if (tid == 0) rsh = r;
     }
     __syncthreads();
     if (i < H) {
@@ -312,15 +214,15 @@ static void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pd
     cfg.numAttrs = pdl ? 1 : 0;
 }
 
-cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, const float* w,
-                         float eps, __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl) {
+cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq, bool pdl,
+                         cudaStream_t s, unsigned long long* tl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
     cfg.gridDim = dim3(B);
     cfg.blockDim = dim3(EMBED_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, w, eps, xn, tl);
+    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, ssq, tl);
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,

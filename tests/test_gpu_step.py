@@ -52,12 +52,13 @@ def tiny():
 
 
 # 0: schedules chosen per matrix; 2 / 4: every projection forced onto the
-# stream / group schedule (the tiny model alone would only exercise one of them).
+# stream / group schedule (the tiny model alone would only exercise one of them);
+# 32: the RMSNorm folded into the q|k|v and gate|up activation load.
 # norms: the workload's unit norm weights, or seeded non-unit ones (1 + 0.1 N(0,1),
 # a different vector for every layer's two norms and the output norm), so that a
 # kernel that dropped the weight or read another layer's would fail.
 @pytest.mark.parametrize("norms", ["unit", "seeded"])
-@pytest.mark.parametrize("flags", [0, 2, 4])
+@pytest.mark.parametrize("flags", [0, 2, 4, 32])
 def test_tiny_teacher_forced_against_oracle(kdlib, tiny, flags, norms):
     kd = kdlib
     shape, w = tiny
@@ -145,8 +146,9 @@ def greedy_stream(kd, m, ids, lens, tok0, steps, V):
     return np.array(toks), np.array(logits)
 
 
-# graph replay (auto schedules), kernel-by-kernel launches, and each schedule forced
-@pytest.mark.parametrize("flags", [0, 1, 2, 4])
+# graph replay (auto schedules), kernel-by-kernel launches, each schedule forced,
+# and the folded norm
+@pytest.mark.parametrize("flags", [0, 1, 2, 4, 32])
 def test_tiny_batch_invariance(kdlib, tiny, flags):
     kd = kdlib
     shape, w = tiny
@@ -226,6 +228,74 @@ def test_tiny_errors_change_no_state(kdlib, tiny):
             kd.kd_session_length(m, a)
         assert kd.kd_session_bind(m) == a  # lowest free slot, length 0 again
         assert kd.kd_session_length(m, a) == 0
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
+def test_tiny_fused_norm_bitwise_equals_norm_kernel(kdlib, tiny):
+    """The RMSNorm folded into the q|k|v and gate|up activation load gives the
+    same bits as the unfused train (the norm as a kernel of its own, then the
+    projection reading its fp16 output): logits and every layer's hidden state,
+    over several steps, with seeded non-unit norm weights."""
+    kd = kdlib
+    shape, w = tiny
+    w = dict(w, **synth.norm_weights(shape, 5))
+    cap, lens = 64, [17, 40, 3]
+    tok0 = synth.tokens(0, "tiny-fuse", len(lens), shape.vocab)
+    runs = []
+    for flags in (0, 32):
+        m = load(kd, shape, w, 4, cap, flags)
+        try:
+            ids = bind_prefilled(kd, m, shape, lens)
+            B, L, H = len(lens), shape.n_layers, shape.hidden
+            hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+            kd.kd_debug_capture_hidden(m, hid)
+            tok, out = tok0.copy(), []
+            for step in range(4):
+                lg, am = gpu_step(kd, m, ids, tok, [n + step for n in lens], shape.vocab)
+                out.append((lg.view(np.uint32).copy(), hid.cpu().numpy().view(np.uint32).copy()))
+                tok = am
+            runs.append(out)
+        finally:
+            kd.kd_model_free(m)
+    for step, ((l0, h0), (l1, h1)) in enumerate(zip(*runs)):
+        assert np.array_equal(l0, l1), step
+        assert np.array_equal(h0, h1), step
+
+
+def test_tiny_batch_above_16_runs_in_groups(kdlib, tiny):
+    """B = 37 > 16: the step runs as groups of 16, 16 and 5 rows on the same
+    kernels.  Every session's greedy tokens and logit bits, and its hidden states
+    (captured across the groups), equal its run alone at B = 1."""
+    kd = kdlib
+    shape, w = tiny
+    cap, steps, B = 64, 3, 37
+    lens = [(5 * i + 3) % 50 for i in range(B)]
+    tok0 = synth.tokens(0, "tiny-chunks", B, shape.vocab)
+    m = load(kd, shape, w, 40, cap)
+    try:
+        L, H = shape.n_layers, shape.hidden
+        ids = bind_prefilled(kd, m, shape, lens)
+        hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+        kd.kd_debug_capture_hidden(m, hid)
+        gpu_step(kd, m, ids, tok0, lens, shape.vocab)
+        batch_hidden = hid.cpu().numpy().view(np.uint32).copy()
+        kd.kd_debug_capture_hidden(m, None)
+        batch_t, batch_l = greedy_stream(kd, m, ids, lens, tok0, steps, shape.vocab)  # rewinds to lens
+        for sid in ids:
+            kd.kd_session_free(m, sid)
+        one = torch.empty(L + 1, 1, H, device="cuda", dtype=torch.float32)
+        for b in range(B):
+            (sid,) = bind_prefilled(kd, m, shape, [lens[b]], first_session=b)
+            kd.kd_debug_capture_hidden(m, one)
+            gpu_step(kd, m, [sid], tok0[b:b + 1], [lens[b]], shape.vocab)
+            assert np.array_equal(one.cpu().numpy().view(np.uint32)[:, 0], batch_hidden[:, b]), b
+            kd.kd_debug_capture_hidden(m, None)
+            t1, l1 = greedy_stream(kd, m, [sid], [lens[b]], tok0[b:b + 1], steps, shape.vocab)
+            assert np.array_equal(t1[:, 0], batch_t[:, b]), b
+            assert np.array_equal(l1[:, 0].view(np.uint32), batch_l[:, b].view(np.uint32)), b
+            kd.kd_session_free(m, sid)
         assert kd.kd_device_status(m) == 0
     finally:
         kd.kd_model_free(m)
