@@ -481,6 +481,113 @@ def run_op_long(args):
     return dict(op="long_context_step", **time_long(args.steps, args.warmup))
 
 
+def run_op_step(args):
+    """The 8B-shaped step (hidden 4096, 32/8 heads of 128, FFN 14336, vocab 128256) with
+    `--layers` decoder layers, B = `--batch` sessions pre-filled to 1238 positions: the
+    same kernels and launch train at a depth whose device footprint (about 1.6 GB at 2
+    layers) suits profiler captures of single launches."""
+    import dataclasses
+
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    shape = dataclasses.replace(synth.LLAMA3_8B, name=f"llama3-8b-shaped-{args.layers}L", n_layers=args.layers)
+    B = args.batch
+    w = synth.model_weights(shape, seed=0)
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=B, max_ctx=CAPACITY), w)
+    ids = []
+    for i in range(B):
+        k, v = synth.kv_prefill(shape, 0, i, PREFILL)
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, k, v, PREFILL)
+        ids.append(sid)
+    tok = synth.tokens(0, "bench", B, shape.vocab)
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        kd.kd_decode_step(m, ids, tok, np.full(B, PREFILL + i, np.int32), None, am, st)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        kd.kd_decode_step(m, ids, tok, np.full(B, PREFILL + (args.warmup + i) % WINDOW, np.int32), None, am, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    status = kd.kd_device_status(m)
+    kd.kd_model_free(m)
+    return {"op": "step", "layers": args.layers, "B": B, "steps": args.steps,
+            "ms_per_step": round(e0.elapsed_time(e1) / args.steps, 4), "device_status": status}
+
+
+def run_op_timeline(args):
+    """Where the graph-replayed step's time goes: per-CTA global-timer stamps of every
+    launch (kd_profile_timeline) of the 8B-shaped step at B = --batch (1238 positions),
+    summarised per kernel class over the middle layers (medians): `run` = the first
+    CTA's dependency release to the last CTA's end, `gap` = that end to the next
+    kernel's first release, `early` = the first CTA's entry to the release."""
+    import torch
+
+    import session_decode_step_gb300 as kd
+    from session_decode_step_gb300 import build as kbuild
+    kbuild.build()
+    torch.cuda.set_device(0)
+    shape = synth.LLAMA3_8B
+    B = args.batch
+    w = synth.model_weights(shape, seed=0)
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=B, max_ctx=CAPACITY), w)
+    ids = []
+    for i in range(B):
+        k, v = synth.kv_prefill(shape, 0, i, PREFILL)
+        sid = kd.kd_session_bind(m)
+        kd.kd_session_load_kv(m, sid, k, v, PREFILL)
+        ids.append(sid)
+    tok = synth.tokens(0, "bench", B, shape.vocab)
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    nmax = 1 + shape.n_layers * 8 + 3
+    buf = torch.zeros(nmax, kd.KD_TIMELINE_CTAS, 4, dtype=torch.int64, device="cuda")
+    classes = kd.kd_profile_timeline(m, buf, nmax)
+    n_launch = sum(c is not None for c in classes)
+    per_layer = (n_launch - 4) // shape.n_layers  # embed, then layers, then output norm, lm_head, argmax
+    stats, steps_ns = {}, []
+    for i in range(max(3, args.warmup) + args.steps):
+        buf.zero_()
+        kd.kd_decode_step(m, ids, tok, np.full(B, PREFILL + i % WINDOW, np.int32), None, am, st)
+        torch.cuda.synchronize()
+        if i < max(3, args.warmup):
+            continue
+        t = buf.cpu().numpy()
+        rows = []
+        for j in range(n_launch):
+            r = t[j][t[j][:, 0] > 0]
+            rows.append((int(r[:, 0].min()), int(r[:, 1].min()), int(r[:, 2].max()), len(r)))
+        steps_ns.append(rows[-1][2] - rows[0][0])
+        for j in range(1 + 2 * per_layer, 1 + (shape.n_layers - 2) * per_layer):
+            name = classes[j]
+            if name == "rmsnorm":
+                name += "_ffn" if classes[j + 1] == "gate_up" else "_attn"
+            d = stats.setdefault(name, {"run": [], "gap": [], "early": [], "ctas": rows[j][3]})
+            d["run"].append((rows[j][2] - rows[j][1]) / 1e3)
+            d["gap"].append((rows[j + 1][1] - rows[j][2]) / 1e3)
+            d["early"].append((rows[j][1] - rows[j][0]) / 1e3)
+        for j, name in ((0, "embed"), (n_launch - 3, "rmsnorm_out"), (n_launch - 2, "lm_head"), (n_launch - 1, "argmax")):
+            d = stats.setdefault(name, {"run": [], "gap": [], "early": [], "ctas": rows[j][3]})
+            d["run"].append((rows[j][2] - rows[j][1]) / 1e3)
+            d["gap"].append((rows[j + 1][1] - rows[j][2]) / 1e3 if j + 1 < n_launch else 0.0)
+            d["early"].append((rows[j][1] - rows[j][0]) / 1e3)
+    kd.kd_profile_timeline(m, None)
+    kd.kd_model_free(m)
+    summ = {k: {"run_us": round(statistics.median(v["run"]), 2), "gap_us": round(statistics.median(v["gap"]), 2),
+                "early_us": round(statistics.median(v["early"]), 2), "ctas": v["ctas"]} for k, v in stats.items()}
+    layer_us = sum(v["run_us"] + v["gap_us"] for k, v in summ.items()
+                   if k not in ("embed", "rmsnorm_out", "lm_head", "argmax"))
+    return {"op": "timeline", "B": B, "steps": args.steps, "step_us": round(statistics.median(steps_ns) / 1e3, 1),
+            "launches_per_step": n_launch, "layer_us": round(layer_us, 2), "classes": summ}
+
+
 def other_workloads(steps, warmup, w):
     """The workloads other than the headline one, measured in the same run: the
     long-context step, the isolated mmvq at every m, the isolated ragged attention."""
@@ -544,15 +651,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the long-context, isolated-mmvq and isolated-attention measurements")
-    ap.add_argument("--op", choices=["mmvq", "attn", "long"],
-                    help="time one kernel family in isolation, or the long-context step")
+    ap.add_argument("--op", choices=["mmvq", "attn", "long", "step", "timeline"],
+                    help="time one kernel family in isolation, the long-context step, the 8B-shaped step "
+                         "at --layers depth, or the per-kernel in-step timeline of the 8B-shaped step")
+    ap.add_argument("--layers", type=int, default=2, help="decoder layers of --op step")
     ap.add_argument("--rows", type=int, default=4096)
     ap.add_argument("--cols", type=int, default=14336)
     ap.add_argument("--m", type=int, default=8)
     ap.add_argument("--cap", type=int, default=32768)
     args = ap.parse_args()
     if args.op:
-        r = {"mmvq": run_op_mmvq, "attn": run_op_attn, "long": run_op_long}[args.op](args)
+        r = {"mmvq": run_op_mmvq, "attn": run_op_attn, "long": run_op_long, "step": run_op_step,
+             "timeline": run_op_timeline}[args.op](args)
         print(json.dumps(r), flush=True)
         return
     args.warmup = max(args.warmup, 3)
