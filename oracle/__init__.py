@@ -81,6 +81,11 @@ def _declare(L):
     L.kdo_silu.restype = C.c_double
     L.kdo_argmax_f32.argtypes = [_f32p, C.c_int32]
     L.kdo_argmax_f32.restype = C.c_int32
+    L.kdo_philox4x64_10.argtypes = [C.POINTER(C.c_uint64), C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]
+    L.kdo_gumbel_perturbed.argtypes = [C.c_float, C.c_int32, C.c_float, C.c_uint64, C.c_uint64]
+    L.kdo_gumbel_perturbed.restype = C.c_float
+    L.kdo_sample_f32.argtypes = [_f32p, C.c_int32, C.c_float, C.c_uint64, C.c_uint64]
+    L.kdo_sample_f32.restype = C.c_int32
     L.kdo_session_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32,
                                    C.c_int32, _u16p, _u16p, C.c_int32, _f32p, _f32p]
     L.kdo_session_step.restype = C.c_int32
@@ -158,6 +163,25 @@ def silu(y: float) -> float:
 def argmax_f32(v: np.ndarray) -> int:
     v = np.ascontiguousarray(v, dtype=np.float32)
     return int(lib().kdo_argmax_f32(_p(v, _f32p), v.size))
+
+
+def philox4x64_10(counter, key) -> list:
+    """The four 64-bit words of the Philox4x64-10 block at `counter` (4 words) under `key` (2 words)."""
+    c = (C.c_uint64 * 4)(*[int(x) for x in counter])
+    k = (C.c_uint64 * 2)(*[int(x) for x in key])
+    o = (C.c_uint64 * 4)()
+    lib().kdo_philox4x64_10(c, k, o)
+    return list(o)
+
+
+def gumbel_perturbed(logit: float, v: int, temperature: float, seed: int, counter: int) -> float:
+    return float(lib().kdo_gumbel_perturbed(float(logit), int(v), float(temperature), int(seed), int(counter)))
+
+
+def sample_f32(logits: np.ndarray, temperature: float, seed: int, counter: int) -> int:
+    """One temperature draw over an fp32 logit row (temperature <= 0: the greedy argmax)."""
+    v = np.ascontiguousarray(logits, dtype=np.float32)
+    return int(lib().kdo_sample_f32(_p(v, _f32p), v.size, float(temperature), int(seed), int(counter)))
 
 
 # ---------------------------------------------------------------------------

@@ -189,6 +189,73 @@ KDO_EXPORT int32_t kdo_argmax_f32(const float* v, int32_t n) {
 }
 
 /* ---------------------------------------------------------------------------
+ * Device temperature sampling (memra-engine decode_batch.rs,
+ * `decode_step_batch_sampled`: a Gumbel perturbation keyed by (seed, counter,
+ * temperature) followed by the same argmax is one categorical draw from
+ * softmax(logits / temperature); temperature <= 0 is the greedy argmax; the
+ * draw depends on (seed, counter) only, never on the rest of the batch).
+ *
+ * The pages name Philox as the counter-based generator and fix nothing else;
+ * the reading taken: Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC'11), vocabulary entry v drawing word
+ * v mod 4 of the block at counter (v / 4, counter, 0, 0) under key (seed, 0);
+ * u = (top 24 bits + 1/2) / 2^24, g = -log(-log u), z = logit / T + g, all in
+ * fp32 (the decision is taken in the kernel's precision); the pick is the
+ * argmax of z with the greedy rule's ties and NaN handling.
+ * ------------------------------------------------------------------------- */
+static void mul64_hilo(uint64_t a, uint64_t b, uint64_t* hi, uint64_t* lo) {
+    /* 64 x 64 -> 128 from 32-bit halves */
+    const uint64_t a0 = a & 0xffffffffu, a1 = a >> 32, b0 = b & 0xffffffffu, b1 = b >> 32;
+    const uint64_t p00 = a0 * b0, p01 = a0 * b1, p10 = a1 * b0, p11 = a1 * b1;
+    const uint64_t mid = (p00 >> 32) + (p01 & 0xffffffffu) + (p10 & 0xffffffffu);
+    *lo = (mid << 32) | (p00 & 0xffffffffu);
+    *hi = p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+}
+
+/* Philox4x64 with 10 rounds: each round multiplies words 0 and 2 by the two
+ * round multipliers, mixes the high halves with words 1 and 3 and the key,
+ * and permutes; the key is bumped by the two Weyl constants between rounds. */
+KDO_EXPORT void kdo_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) { k0 += W0; k1 += W1; }
+        uint64_t hi0, lo0, hi1, lo1;
+        mul64_hilo(M0, c0, &hi0, &lo0);
+        mul64_hilo(M1, c2, &hi1, &lo1);
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The perturbed value of vocabulary entry v (fp32). */
+KDO_EXPORT float kdo_gumbel_perturbed(float logit, int32_t v, float temperature, uint64_t seed, uint64_t counter) {
+    const uint64_t ctr[4] = {(uint64_t)(v / 4), counter, 0, 0}, key[2] = {seed, 0};
+    uint64_t w[4];
+    kdo_philox4x64_10(ctr, key, w);
+    const float u = ((float)(w[v % 4] >> 40) + 0.5f) * 0x1p-24f;  /* in (0, 1), exact */
+    const float g = -logf(-logf(u));
+    return logit / temperature + g;
+}
+
+/* One draw per the reading above: the index, or -1 if every logit is NaN. */
+KDO_EXPORT int32_t kdo_sample_f32(const float* logits, int32_t n, float temperature, uint64_t seed,
+                                  uint64_t counter) {
+    if (!(temperature > 0.0f)) return kdo_argmax_f32(logits, n);
+    int32_t best = -1;
+    float bv = 0.0f;
+    for (int32_t i = 0; i < n; ++i) {
+        if (isnan(logits[i])) continue;
+        const float z = kdo_gumbel_perturbed(logits[i], i, temperature, seed, counter);
+        if (isnan(z)) continue;
+        if (best < 0 || z > bv) { best = i; bv = z; }
+    }
+    return best;
+}
+
+/* ---------------------------------------------------------------------------
  * The model and one decode step.
  * ------------------------------------------------------------------------- */
 typedef struct {
