@@ -189,6 +189,33 @@ kd_status kd_decode_step(kd_model* m, const int32_t* session_ids, const int32_t*
                          const int32_t* positions, int32_t B, float* logits_out,
                          int32_t* argmax_out, kd_stream stream);
 
+/* Per-row sampling parameters (memra decode_batch.rs `decode_step_batch_sampled`:
+ * a Gumbel perturbation keyed by (seed, counter) and the temperature, then the
+ * same argmax, is one categorical draw from softmax(logits / temperature); the
+ * draw depends on (seed, counter) only, not on the rest of the batch).
+ *   temperature <= 0 (or NaN): the greedy pick of kd_decode_step.
+ *   temperature > 0: the index of the largest z_v = logit_v / temperature - log(-log u_v)
+ *     (fp32; ties to the lowest index, NaN never wins), u_v = (top 24 bits of w + 1/2) / 2^24
+ *     where w is word v mod 4 of the Philox4x64-10 block (Salmon et al., "Parallel
+ *     random numbers: as easy as 1, 2, 3", SC'11) at counter {v / 4, counter, 0, 0}
+ *     under key {seed, 0}.
+ * The same (logits, temperature, seed, counter) always give the same token. */
+typedef struct {
+    float temperature;
+    uint32_t reserved;  /* 0 */
+    uint64_t seed;
+    uint64_t counter;
+} kd_sample_params;
+
+/* kd_decode_step with device-side temperature sampling: row b's token is drawn
+ * per params[b] (host array of B) and written to token_out[b] (device int32 [B],
+ * required).  Everything else, including logits_out (the undisturbed logits),
+ * as for kd_decode_step.  Errors as for kd_decode_step; KD_ERR_INVALID_ARG for
+ * a null params or token_out. */
+kd_status kd_decode_step_sampled(kd_model* m, const int32_t* session_ids, const int32_t* tokens,
+                                 const int32_t* positions, int32_t B, const kd_sample_params* params,
+                                 float* logits_out, int32_t* token_out, kd_stream stream);
+
 /* Debug: when dev_buf is not NULL, later steps also write the residual stream
  * after the embedding and after every layer to dev_buf, device fp32
  * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off.
@@ -319,6 +346,16 @@ kd_status kd_mmvq_schedule(int32_t rows, int32_t cols, int32_t num_sms, int32_t*
 #define KD_ARGMAX_WORKSPACE_BYTES 256
 kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, void* workspace,
                     kd_stream stream);
+
+/* Temperature sampling over logit rows, as kd_decode_step_sampled's pick:
+ * out[b] drawn per params[b] (host array of B, see kd_sample_params; the
+ * parameters are copied on the call).  logits: device fp32 [B][V], 16-byte
+ * aligned, V a multiple of 4; out: device int32 [B]; B in [1, KD_MAX_BATCH];
+ * workspace: device memory of KD_SAMPLE_WORKSPACE_BYTES, 16-byte aligned, owned
+ * by the caller, used by one call at a time. */
+#define KD_SAMPLE_WORKSPACE_BYTES 1024
+kd_status kd_sample(const float* logits, int32_t B, int32_t V, const kd_sample_params* params, int32_t* out,
+                    void* workspace, kd_stream stream);
 
 /* Bytes of device workspace kd_attn_append_decode needs for these sizes. */
 size_t kd_attn_workspace_bytes(int32_t B, int32_t n_heads, int32_t head_dim, int32_t cap);

@@ -51,6 +51,19 @@ class KdWeights(C.Structure):
                 ("attn_norm", _fpp), ("ffn_norm", _fpp)]
 
 
+class KdSampleParams(C.Structure):
+    _fields_ = [("temperature", C.c_float), ("reserved", C.c_uint32), ("seed", C.c_uint64), ("counter", C.c_uint64)]
+
+
+def sample_params(temperatures, seeds, counters):
+    """A host array of kd_sample_params from per-row temperatures, seeds and counters."""
+    t = list(np.asarray(temperatures, dtype=np.float32).reshape(-1))
+    arr = (KdSampleParams * len(t))()
+    for i, (tt, sd, ct) in enumerate(zip(t, seeds, counters)):
+        arr[i] = KdSampleParams(float(tt), 0, int(sd), int(ct))
+    return arr
+
+
 _lib = None
 
 
@@ -83,6 +96,8 @@ def lib():
             "kd_q8_matrix_free": [_vp],
             "kd_mmvq": [_vp, _vp, i32, _vp, _vp],
             "kd_argmax": [_vp, i32, i32, _vp, _vp, _vp],
+            "kd_sample": [_vp, i32, i32, _vp, _vp, _vp, _vp],
+            "kd_decode_step_sampled": [_vp, i32p, i32p, i32p, i32, _vp, _vp, _vp, _vp],
             "kd_mmvq_schedule": [i32, i32, i32, i32p, i32p, i32p],
             "kd_attn_append_decode": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                       i32, _vp, _vp, C.c_size_t, _vp],
@@ -218,6 +233,20 @@ def kd_decode_step(m, session_ids, tokens, positions, logits_out=None, argmax_ou
                                 _stream(stream)))
 
 
+def kd_decode_step_sampled(m, session_ids, tokens, positions, params, logits_out=None, token_out=None, stream=None):
+    """One batched step with device temperature sampling: params from sample_params(); token_out a
+    device int32 [B] tensor (required)."""
+    ids = _i32(session_ids)
+    B = ids.size
+    tok, pos = _i32(tokens, B), _i32(positions, B)
+    if len(params) != B:
+        raise ValueError(f"expected {B} sampling parameter rows, got {len(params)}")
+    i32p = C.POINTER(C.c_int32)
+    _check(lib().kd_decode_step_sampled(m, ids.ctypes.data_as(i32p), tok.ctypes.data_as(i32p),
+                                        pos.ctypes.data_as(i32p), B, C.cast(params, _vp), _ptr(logits_out),
+                                        _ptr(token_out), _stream(stream)))
+
+
 def kd_debug_capture_hidden(m, buf):
     _check(lib().kd_debug_capture_hidden(m, _ptr(buf)))
 
@@ -308,6 +337,18 @@ def kd_mmvq_schedule(rows: int, cols: int, num_sms: int):
 def kd_argmax(logits, B: int, V: int, out, workspace, stream=None):
     """logits: device fp32 [B][V]; out: device int32 [B]; workspace: KD_ARGMAX_WORKSPACE_BYTES of device memory."""
     _check(lib().kd_argmax(_ptr(logits), int(B), int(V), _ptr(out), _ptr(workspace), _stream(stream)))
+
+
+KD_SAMPLE_WORKSPACE_BYTES = 1024
+
+
+def kd_sample(logits, B: int, V: int, params, out, workspace, stream=None):
+    """logits: device fp32 [B][V]; params: sample_params(...) of B rows; out: device int32 [B];
+    workspace: KD_SAMPLE_WORKSPACE_BYTES of device memory."""
+    if len(params) != B:
+        raise ValueError(f"expected {B} sampling parameter rows, got {len(params)}")
+    _check(lib().kd_sample(_ptr(logits), int(B), int(V), C.cast(params, _vp), _ptr(out), _ptr(workspace),
+                           _stream(stream)))
 
 
 def kd_attn_workspace_bytes(B: int, n_heads: int, head_dim: int, cap: int) -> int:

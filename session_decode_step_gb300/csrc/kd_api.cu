@@ -68,7 +68,8 @@ cudaError_t init_device_attributes(int dev) {
 }
 
 constexpr int RING = 4;        // pinned staging slots for the per-step descriptor
-constexpr int DESC_INTS = 3 * KD_MAX_BATCH;  // slot[16], token[16], pos[16]
+// slot[16], token[16], pos[16], then the rows' sampling parameters (kd::SAMP_INTS words)
+constexpr int DESC_INTS = 3 * KD_MAX_BATCH + kd::SAMP_INTS;
 
 // Source-row maps of the packed tiles (see the layout note in kd_kernels.h).
 std::vector<int> tiles_natural(int rows) {
@@ -162,7 +163,7 @@ struct kd_model {
     cudaStream_t cap_stream = nullptr;
     std::vector<uint8_t> bound;
     std::vector<int32_t> len;
-    std::map<std::tuple<int, float*, int*, unsigned long long*>, cudaGraphExec_t> graphs;
+    std::map<std::tuple<int, float*, int*, unsigned long long*, bool>, cudaGraphExec_t> graphs;
     float* hidden_dbg = nullptr;
     int inject_cls = -1;      // debug fault hook: kernel class whose next launch's bounded wait runs out
     unsigned long long* tl = nullptr;  // timeline records (kd_profile_timeline), or nullptr
@@ -348,8 +349,9 @@ static bool fused_norm(const kd_model* m, const PackedQ8& p) {
 // their per-group sums of squares in m->ssq; no embedding, no head.
 // Hidden-state capture (kd_debug_capture_hidden) of a chunk of a larger step:
 // its rows start at hrow0 of the step's hB rows.
+// sampled: the pick applies each row's sampling parameters (staged with the descriptor).
 static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStream_t s, int only_layer = -1,
-                                int hrow0 = 0, int hB = 0) {
+                                int hrow0 = 0, int hB = 0, bool sampled = false) {
     if (hB == 0) hB = B;
     const kd_config& c = m->cfg;
     const int L = c.n_layers, H = c.hidden, nh = c.n_heads, nkv = c.n_kv_heads, hd = c.head_dim;
@@ -489,13 +491,13 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     if (am)
         KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, m->amax_keys,
                                               reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s,
-                                              tl_next()));
+                                              tl_next(), sampled ? m->desc + 3 * KD_MAX_BATCH : nullptr));
 #undef KD_RUN
     return cudaSuccess;
 }
 
-static kd_status get_graph(kd_model* m, int B, float* lg, int* am, cudaGraphExec_t* out) {
-    auto key = std::make_tuple(B, lg, am, m->tl);
+static kd_status get_graph(kd_model* m, int B, float* lg, int* am, bool sampled, cudaGraphExec_t* out) {
+    auto key = std::make_tuple(B, lg, am, m->tl, sampled);
     auto it = m->graphs.find(key);
     if (it != m->graphs.end()) {
         *out = it->second;
@@ -509,7 +511,7 @@ static kd_status get_graph(kd_model* m, int B, float* lg, int* am, cudaGraphExec
     }
     cudaGraph_t graph = nullptr;
     KD_CK(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = enqueue_step(m, B, lg, am, m->cap_stream);
+    cudaError_t e = enqueue_step(m, B, lg, am, m->cap_stream, -1, 0, 0, sampled);
     cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
     if (e != cudaSuccess || e2 != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
@@ -646,7 +648,7 @@ static kd_status check_rows(kd_model* m, const char* fn, const int32_t* ids, con
 // Stage the [slot | token | pos] descriptor through a pinned ring slot no earlier
 // copy still reads, ordered after the model's previous step.
 static kd_status stage_descriptor(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
-                                  int32_t B, cudaStream_t s) {
+                                  int32_t B, cudaStream_t s, const kd_sample_params* sp = nullptr) {
     const int ri = m->ring_i;
     KD_CK(cudaEventSynchronize(m->ring_ev[ri]));
     int32_t* d = m->pinned + (size_t)ri * DESC_INTS;
@@ -655,6 +657,14 @@ static kd_status stage_descriptor(kd_model* m, const int32_t* ids, const int32_t
         d[b] = ids[b];
         d[KD_MAX_BATCH + b] = tokens ? tokens[b] : 0;
         d[2 * KD_MAX_BATCH + b] = positions[b];
+        if (sp) {  // the layout launch_argmax documents
+            int32_t* q = d + 3 * KD_MAX_BATCH;
+            std::memcpy(&q[b], &sp[b].temperature, sizeof(float));
+            q[16 + 2 * b] = (int32_t)(uint32_t)sp[b].seed;
+            q[17 + 2 * b] = (int32_t)(uint32_t)(sp[b].seed >> 32);
+            q[48 + 2 * b] = (int32_t)(uint32_t)sp[b].counter;
+            q[49 + 2 * b] = (int32_t)(uint32_t)(sp[b].counter >> 32);
+        }
     }
     KD_CK(cudaStreamWaitEvent(s, m->last_step, 0));
     KD_CK(cudaMemcpyAsync(m->desc, d, DESC_INTS * sizeof(int32_t), cudaMemcpyHostToDevice, s));
@@ -663,31 +673,33 @@ static kd_status stage_descriptor(kd_model* m, const int32_t* ids, const int32_t
     return KD_OK;
 }
 
-kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
-                         int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
-    if (!m) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null model");
-    if (!tokens && B >= 1 && B <= KD_MAX_BATCH) return fail(KD_ERR_INVALID_ARG, "kd_decode_step: null host array");
+// One step, greedy (sp == nullptr) or with each row's sampling parameters.
+static kd_status decode_impl(kd_model* m, const char* fn, const int32_t* ids, const int32_t* tokens,
+                             const int32_t* positions, int32_t B, const kd_sample_params* sp, float* logits_out,
+                             int32_t* argmax_out, kd_stream stream) {
+    if (!m) return fail(KD_ERR_INVALID_ARG, "%s: null model", fn);
+    if (!tokens && B >= 1) return fail(KD_ERR_INVALID_ARG, "%s: null host array", fn);
     // Any number of distinct bound sessions; above KD_MAX_BATCH the step runs as
     // consecutive groups of at most KD_MAX_BATCH rows on the same kernels.
-    kd_status st0 = check_rows(m, "kd_decode_step", ids, tokens, positions, B, (int32_t)m->bound.size());
+    kd_status st0 = check_rows(m, fn, ids, tokens, positions, B, (int32_t)m->bound.size());
     if (st0 != KD_OK) return st0;
     if (reinterpret_cast<uintptr_t>(logits_out) & 15)
-        return fail(KD_ERR_INVALID_ARG, "kd_decode_step: logits_out must be 16-byte aligned");
+        return fail(KD_ERR_INVALID_ARG, "%s: logits_out must be 16-byte aligned", fn);
     const kd_config& c = m->cfg;
     KD_CK(cudaSetDevice(m->dev));
     cudaStream_t s = (cudaStream_t)stream;
     const bool direct = m->hidden_dbg || m->prof || (c.flags & KD_FLAG_NO_GRAPH) || m->inject_cls >= 0;
     for (int r0 = 0; r0 < B; r0 += KD_MAX_BATCH) {
         const int n = std::min(B - r0, KD_MAX_BATCH);
-        st0 = stage_descriptor(m, ids + r0, tokens + r0, positions + r0, n, s);
+        st0 = stage_descriptor(m, ids + r0, tokens + r0, positions + r0, n, s, sp ? sp + r0 : nullptr);
         if (st0 != KD_OK) return st0;
         float* lg = logits_out ? logits_out + (size_t)r0 * c.vocab : m->logits_ws;
         int* am = argmax_out ? argmax_out + r0 : nullptr;
         if (direct) {
-            KD_CK(enqueue_step(m, n, lg, am, s, -1, r0, B));
+            KD_CK(enqueue_step(m, n, lg, am, s, -1, r0, B, sp != nullptr));
         } else {
             cudaGraphExec_t g = nullptr;
-            kd_status st = get_graph(m, n, lg, am, &g);
+            kd_status st = get_graph(m, n, lg, am, sp != nullptr, &g);
             if (st != KD_OK) return st;
             KD_CK(cudaGraphLaunch(g, s));
         }
@@ -695,6 +707,18 @@ kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens,
     }
     for (int b = 0; b < B; ++b) m->len[ids[b]] = positions[b] + 1;
     return KD_OK;
+}
+
+kd_status kd_decode_step(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
+                         int32_t B, float* logits_out, int32_t* argmax_out, kd_stream stream) {
+    return decode_impl(m, "kd_decode_step", ids, tokens, positions, B, nullptr, logits_out, argmax_out, stream);
+}
+
+kd_status kd_decode_step_sampled(kd_model* m, const int32_t* ids, const int32_t* tokens, const int32_t* positions,
+                                 int32_t B, const kd_sample_params* params, float* logits_out, int32_t* token_out,
+                                 kd_stream stream) {
+    if (!params || !token_out) return fail(KD_ERR_INVALID_ARG, "kd_decode_step_sampled: null params or token_out");
+    return decode_impl(m, "kd_decode_step_sampled", ids, tokens, positions, B, params, logits_out, token_out, stream);
 }
 
 kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const int32_t* positions, int32_t B,
@@ -936,6 +960,35 @@ kd_status kd_argmax(const float* logits, int32_t B, int32_t V, int32_t* out, voi
     auto* keys = reinterpret_cast<unsigned long long*>(workspace);
     KD_CK(cudaMemsetAsync(keys, 0, (KD_MAX_BATCH + 1) * sizeof(unsigned long long), s));
     KD_CK(kd::launch_argmax(logits, B, V, out, keys, reinterpret_cast<unsigned*>(keys + KD_MAX_BATCH), false, s));
+    return KD_OK;
+}
+
+kd_status kd_sample(const float* logits, int32_t B, int32_t V, const kd_sample_params* params, int32_t* out,
+                    void* workspace, kd_stream stream) {
+    if (!logits || !params || !out || !workspace) return fail(KD_ERR_INVALID_ARG, "kd_sample: null argument");
+    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_sample: B=%d outside [1, %d]", B, KD_MAX_BATCH);
+    if (V < 1 || V % 4) return fail(KD_ERR_INVALID_ARG, "kd_sample: V=%d must be a positive multiple of 4", V);
+    if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(workspace)) & 15)
+        return fail(KD_ERR_INVALID_ARG, "kd_sample: logits and workspace must be 16-byte aligned");
+    static_assert(256 + kd::SAMP_INTS * sizeof(int32_t) <= KD_SAMPLE_WORKSPACE_BYTES, "sample workspace");
+    int32_t q[kd::SAMP_INTS] = {};
+    for (int b = 0; b < B; ++b) {
+        std::memcpy(&q[b], &params[b].temperature, sizeof(float));
+        q[16 + 2 * b] = (int32_t)(uint32_t)params[b].seed;
+        q[17 + 2 * b] = (int32_t)(uint32_t)(params[b].seed >> 32);
+        q[48 + 2 * b] = (int32_t)(uint32_t)params[b].counter;
+        q[49 + 2 * b] = (int32_t)(uint32_t)(params[b].counter >> 32);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0;
+    KD_CK(cudaGetDevice(&dev));
+    KD_CK(init_device_attributes(dev));
+    auto* keys = reinterpret_cast<unsigned long long*>(workspace);
+    int* dq = reinterpret_cast<int*>(reinterpret_cast<char*>(workspace) + 256);
+    KD_CK(cudaMemsetAsync(keys, 0, (KD_MAX_BATCH + 1) * sizeof(unsigned long long), s));
+    KD_CK(cudaMemcpyAsync(dq, q, sizeof q, cudaMemcpyHostToDevice, s));
+    KD_CK(kd::launch_argmax(logits, B, V, out, keys, reinterpret_cast<unsigned*>(keys + KD_MAX_BATCH), false, s,
+                            nullptr, dq));
     return KD_OK;
 }
 

@@ -187,8 +187,14 @@ cudaError_t rowops_init_attributes();
 // out[b] = argmax_v logits[b][v] (ties -> lowest v, NaN never wins, -1 if none).
 // keys [>= B] and done: device scratch that is zero before the first launch;
 // every launch leaves it zero again.  V must be a multiple of 4.
+// samp (nullable, device, SAMP_INTS words): per-row temperature sampling --
+// words [0, 16) the rows' temperatures (fp32 bits; <= 0 greedy), [16 + 2b, 17 + 2b]
+// row b's seed (low, high 32 bits), [48 + 2b, 49 + 2b] its counter.  A row with
+// temperature T > 0 takes the argmax of logit / T plus Gumbel noise from
+// Philox4x64-10 (see kd_sample_params in kd.h).
+constexpr int SAMP_INTS = 80;
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
-                          bool pdl, cudaStream_t s, unsigned long long* tl = nullptr);
+                          bool pdl, cudaStream_t s, unsigned long long* tl = nullptr, const int* samp = nullptr);
 
 // Device address of the allocation-free attention call's fault word on device
 // dev, or nullptr if that call has not run on the device yet.

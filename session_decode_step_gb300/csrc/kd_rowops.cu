@@ -148,9 +148,40 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
     return ((unsigned long long)ord << 32) | (unsigned long long)(~(unsigned)i);
 }
 
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 64 x 64
+// -> 128 multiplies mixing the four counter words with the key, the key bumped
+// by the two Weyl constants between rounds.  Returns the block's four words.
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
+                                              uint64_t k1, uint64_t (&w)[4]) {
+    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0, hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    w[0] = c0; w[1] = c1; w[2] = c2; w[3] = c3;
+}
+
+// logit / T - log(-log u), u = (top 24 bits of w + 1/2) / 2^24 (exact, in (0, 1)).
+__device__ __forceinline__ float gumbel_perturb(float logit, float T, uint64_t w) {
+    const float u = __fmul_rn(__fadd_rn((float)(unsigned)(w >> 40), 0.5f), 0x1p-24f);
+    const float g = -logf(-logf(u));
+    return __fadd_rn(__fdiv_rn(logit, T), g);
+}
+
 __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __restrict__ logits, int V,
                                                                 unsigned long long* keys, unsigned* done,
-                                                                int* __restrict__ out, unsigned long long* tl) {
+                                                                int* __restrict__ out, unsigned long long* tl,
+                                                                const int* __restrict__ samp) {
     __shared__ unsigned long long wbest[ARGMAX_THREADS / 32];
     __shared__ bool last;
     tl_entry(tl);
@@ -165,6 +196,26 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __r
     for (int h = 0; h < 2; ++h) {
         const int i = i0 + h * ARGMAX_THREADS * 4;
         v[h] = i < V ? __ldcg(reinterpret_cast<const float4*>(row + i)) : make_float4(NAN, NAN, NAN, NAN);
+    }
+    // Temperature sampling: the row's entries get their Gumbel perturbation
+    // (entry v: word v mod 4 of the Philox block at counter (v / 4, counter, 0, 0)
+    // under key (seed, 0)); the pick is then the same argmax.
+    const float T = samp ? __int_as_float(samp[b]) : 0.0f;
+    if (T > 0.0f) {
+        const uint64_t seed = ((uint64_t)(unsigned)samp[17 + 2 * b] << 32) | (unsigned)samp[16 + 2 * b];
+        const uint64_t ctr = ((uint64_t)(unsigned)samp[49 + 2 * b] << 32) | (unsigned)samp[48 + 2 * b];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = i0 + h * ARGMAX_THREADS * 4;
+            if (i < V) {
+                uint64_t w[4];
+                philox4x64_10((uint64_t)(i >> 2), ctr, 0, 0, seed, 0, w);
+                v[h].x = gumbel_perturb(v[h].x, T, w[0]);
+                v[h].y = gumbel_perturb(v[h].y, T, w[1]);
+                v[h].z = gumbel_perturb(v[h].z, T, w[2]);
+                v[h].w = gumbel_perturb(v[h].w, T, w[3]);
+            }
+        }
     }
     unsigned long long best = 0ull;
 #pragma unroll
@@ -226,7 +277,7 @@ cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,
-                          bool pdl, cudaStream_t s, unsigned long long* tl) {
+                          bool pdl, cudaStream_t s, unsigned long long* tl, const int* samp) {
     if (V % 4) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -234,7 +285,7 @@ cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned 
     cfg.gridDim = dim3((V + ARGMAX_CHUNK - 1) / ARGMAX_CHUNK, B);
     cfg.blockDim = dim3(ARGMAX_THREADS);
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, keys, done, out, tl);
+    return cudaLaunchKernelEx(&cfg, argmax_kernel, logits, V, keys, done, out, tl, samp);
 }
 
 }  // namespace kd
