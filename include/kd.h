@@ -85,6 +85,11 @@ typedef struct {
  * measured slower than the separate kernel, whose latency overlaps the next
  * projection's weight prefetch. */
 #define KD_FLAG_FUSED_NORM 32
+/* The unfused train: every projection stores its plain fp32 result, and RoPE +
+ * KV append, SwiGLU and the residual add with the norm's sums of squares run
+ * as kernels of their own.  Bit-identical to the fused epilogues; for testing
+ * and measurement. */
+#define KD_FLAG_UNFUSED 64
 
 /* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
  * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the

@@ -153,6 +153,8 @@ struct kd_model {
     float* apart = nullptr;   // attention split partials
     int max_splits = 0;
     float* logits_ws = nullptr;
+    float* yraw = nullptr;    // the unfused train's plain projection results [16][max rows]
+    int yraw_ld = 0;
     int* err = nullptr;
     unsigned long long* amax_keys = nullptr;  // argmax scratch: [KD_MAX_BATCH] keys, then a counter (zero between launches)
     int* desc = nullptr;      // device [slot16 | token16 | pos16]
@@ -321,6 +323,10 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
         return fail(KD_ERR_UNSUPPORTED, "max_ctx %d exceeds %d positions", cap, kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
     KD_CK(m->alloc(&m->apart, (size_t)MB * nh * m->max_splits * kd::ATT_REC(hd) * sizeof(float)));
     KD_CK(m->alloc(&m->logits_ws, (size_t)MB * V * sizeof(float)));
+    if (c.flags & KD_FLAG_UNFUSED) {
+        m->yraw_ld = std::max({(nh + 2 * nkv) * hd, 2 * F, H});
+        KD_CK(m->alloc(&m->yraw, (size_t)MB * m->yraw_ld * sizeof(float)));
+    }
     KD_CK(m->alloc(&m->err, sizeof(int)));
     KD_CK(m->alloc(&m->amax_keys, (KD_MAX_BATCH + 1) * sizeof(unsigned long long)));
     KD_CK(cudaMemset(m->amax_keys, 0, (KD_MAX_BATCH + 1) * sizeof(unsigned long long)));
@@ -340,7 +346,7 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
 // Whether a projection fed by an RMSNorm takes the norm inside its activation
 // load (group schedule, K <= 4096) rather than after a norm kernel of its own.
 static bool fused_norm(const kd_model* m, const PackedQ8& p) {
-    return (m->cfg.flags & KD_FLAG_FUSED_NORM) && p.mode == kd::MMVQ_GROUP &&
+    return (m->cfg.flags & KD_FLAG_FUSED_NORM) && !(m->cfg.flags & KD_FLAG_UNFUSED) && p.mode == kd::MMVQ_GROUP &&
            p.KG <= kd::MMVQ_WARPS * kd::NORM_IN_MAX_KG;
 }
 
@@ -426,6 +432,18 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     auto norm_in = [&](kd::MmvqArgs& a, const float* w) {
         a.nx = m->x; a.nssq = m->ssq; a.nw = w; a.neps = c.rms_eps;
     };
+    // A projection with its epilogue; in the unfused train, the plain result to
+    // m->yraw and the epilogue as a kernel of its own.
+    const bool unfused = (c.flags & KD_FLAG_UNFUSED) != 0;
+    auto proj = [&](const kd::MmvqArgs& a, const CUtensorMap& xm, int mode, int epi) -> cudaError_t {
+        if (!unfused) return kd::launch_mmvq(a, xm, mode, epi, m->num_sms, pdl, s);
+        kd::MmvqArgs st = a;
+        st.y = m->yraw;
+        st.ld = m->yraw_ld;
+        cudaError_t r = kd::launch_mmvq(st, xm, mode, kd::EPI_STORE, m->num_sms, pdl, s);
+        if (r != cudaSuccess) return r;
+        return kd::launch_unfused_epilogue(a, m->yraw, m->yraw_ld, epi, s);
+    };
     const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
     const bool whole = only_layer < 0;
     if (whole)
@@ -446,7 +464,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
         a.inject_tx = inject(KD_K_QKV);
         a.tl = tl_next();
-        KD_RUN(KD_K_QKV, kd::launch_mmvq(a, m->map_xn, m->qkv[l].mode, kd::EPI_QKV, m->num_sms, pdl, s));
+        KD_RUN(KD_K_QKV, proj(a, m->map_xn, m->qkv[l].mode, kd::EPI_QKV));
         kd::AttnArgs t{};
         t.q = m->q; t.kc = kc; t.vc = vc; t.row0 = (long)l * c.max_sessions * nkv * c.max_ctx;
         t.slot = slot; t.pos = pos; t.B = B; t.nh = nh; t.nkv = nkv;
@@ -461,7 +479,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         resid(a);
         a.inject_tx = inject(KD_K_WO);
         a.tl = tl_next();
-        KD_RUN(KD_K_WO, kd::launch_mmvq(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_WO, proj(a, m->map_attn, m->wo[l].mode, kd::EPI_RESID));
         const float* ffn_w = m->norms + (size_t)(2 * l + 1) * H;
         const bool fg = fused_norm(m, m->gu[l]);
         if (!fg) KD_RUN(KD_K_RMSNORM, norm(ffn_w));
@@ -470,12 +488,12 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         a.act = m->act; a.ld = F;
         a.inject_tx = inject(KD_K_GATE_UP);
         a.tl = tl_next();
-        KD_RUN(KD_K_GATE_UP, kd::launch_mmvq(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU, m->num_sms, pdl, s));
+        KD_RUN(KD_K_GATE_UP, proj(a, m->map_xn, m->gu[l].mode, kd::EPI_SWIGLU));
         a = mm(m->down[l], m->act);
         resid(a);
         a.inject_tx = inject(KD_K_DOWN);
         a.tl = tl_next();
-        KD_RUN(KD_K_DOWN, kd::launch_mmvq(a, m->map_act, m->down[l].mode, kd::EPI_RESID, m->num_sms, pdl, s));
+        KD_RUN(KD_K_DOWN, proj(a, m->map_act, m->down[l].mode, kd::EPI_RESID));
         if (whole && m->hidden_dbg &&
             (e = cudaMemcpyAsync(m->hidden_dbg + ((size_t)(l + 1) * hB + hrow0) * H, m->x, (size_t)B * H * 4,
                                  cudaMemcpyDeviceToDevice, s)) != cudaSuccess)

@@ -129,6 +129,10 @@ cudaError_t launch_mmvq(const MmvqArgs& a, const CUtensorMap& xmap, int mode, in
                         cudaStream_t s);
 // Smallest dynamic shared memory any mmvq launch needs (for occupancy checks).
 cudaError_t mmvq_init_attributes();
+// The unfused train: apply epilogue `epi` (EPI_QKV, EPI_SWIGLU or EPI_RESID, with
+// a's epilogue fields) to a projection's plain result y [B][ldy] (rows in the
+// packed order), as the fused epilogue does.
+cudaError_t launch_unfused_epilogue(const MmvqArgs& a, const float* y, int ldy, int epi, cudaStream_t s);
 
 // ---- attention -------------------------------------------------------------
 constexpr int ATT_CHUNK = 64;        // keys per split; fixed, so a session's splits depend on its length only

@@ -10,7 +10,9 @@ Gates: every one of the 32 layers within 1e-3 relative L2 of the oracle when fed
 the oracle's input to that layer (the layer's attention norm goes through the
 step's own sums-of-squares RMSNorm kernel, its FFN norm through the residual
 writer's sums); one B = 8 step end to end: logits within 5e-2 and hidden states
-within the end-to-end bound for 4 sessions."""
+within the end-to-end bound for 4 sessions; and the fused step bit-identical to
+the unfused train (every epilogue as a kernel of its own; the RMSNorm folded
+into the projections' activation load) over two B = 8 steps."""
 import numpy as np
 import pytest
 
@@ -107,3 +109,39 @@ def test_8b_seeded_norms_step(model_norms):
         kd.kd_debug_capture_hidden(m, None)
         for sid in ids:
             kd.kd_session_free(m, sid)
+
+
+def test_8b_fused_step_bitwise_equal_unfused_and_folded_norm(model_norms):
+    kd, m, w, prefill = model_norms
+    B, L, H, V = 8, SHAPE.n_layers, SHAPE.hidden, SHAPE.vocab
+    tok0 = synth.tokens(0, "8b-unfused", B, V)
+
+    def run(model):
+        ids = bind(kd, model, prefill, range(B))
+        hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+        lg = torch.empty(B, V, device="cuda", dtype=torch.float32)
+        am = torch.empty(B, device="cuda", dtype=torch.int32)
+        kd.kd_debug_capture_hidden(model, hid)
+        out, tok = [], tok0.copy()
+        try:
+            for step in range(2):
+                kd.kd_decode_step(model, ids, tok, [PREFILL + step] * B, lg, am)
+                out.append((lg.cpu().numpy().view(np.uint32).copy(), hid.cpu().numpy().view(np.uint32).copy()))
+                tok = am.cpu().numpy()
+        finally:
+            kd.kd_debug_capture_hidden(model, None)
+            for sid in ids:
+                kd.kd_session_free(model, sid)
+        return out
+
+    ref = run(m)
+    for flags in (64, 32):  # the unfused train; the RMSNorm folded into the projections' load
+        other = kd.kd_model_load(kd.make_config(SHAPE, 8, CAP, flags), w)
+        try:
+            got = run(other)
+            assert kd.kd_device_status(other) == 0
+        finally:
+            kd.kd_model_free(other)
+        for step, ((l0, h0), (l1, h1)) in enumerate(zip(ref, got)):
+            assert np.array_equal(h0, h1), (flags, step)
+            assert np.array_equal(l0, l1), (flags, step)

@@ -299,3 +299,38 @@ def test_tiny_batch_above_16_runs_in_groups(kdlib, tiny):
         assert kd.kd_device_status(m) == 0
     finally:
         kd.kd_model_free(m)
+
+
+def test_tiny_fused_epilogues_bitwise_equal_unfused_train(kdlib, tiny):
+    """Each fusion of the step against its unfused sequence, bit for bit: RoPE and
+    the KV append in the q|k|v epilogue, SwiGLU in the gate|up epilogue, the
+    residual add and the next norm's sums of squares in the o-proj and down
+    epilogues (KD_FLAG_UNFUSED runs them as kernels of their own after plain
+    projections, with the group schedule's summation order).  Logits, every
+    hidden state and the appended cache rows (through later steps' attention),
+    several steps, seeded norm weights."""
+    kd = kdlib
+    shape, w = tiny
+    w = dict(w, **synth.norm_weights(shape, 9))
+    cap, lens = 64, [17, 40, 3]
+    tok0 = synth.tokens(0, "tiny-unfused", len(lens), shape.vocab)
+    runs = []
+    for flags in (0, 64):
+        m = load(kd, shape, w, 4, cap, flags)
+        try:
+            ids = bind_prefilled(kd, m, shape, lens)
+            B, L, H = len(lens), shape.n_layers, shape.hidden
+            hid = torch.empty(L + 1, B, H, device="cuda", dtype=torch.float32)
+            kd.kd_debug_capture_hidden(m, hid)
+            tok, out = tok0.copy(), []
+            for step in range(5):
+                lg, am = gpu_step(kd, m, ids, tok, [n + step for n in lens], shape.vocab)
+                out.append((lg.view(np.uint32).copy(), hid.cpu().numpy().view(np.uint32).copy()))
+                tok = am
+            runs.append(out)
+            assert kd.kd_device_status(m) == 0
+        finally:
+            kd.kd_model_free(m)
+    for step, ((l0, h0), (l1, h1)) in enumerate(zip(*runs)):
+        assert np.array_equal(h0, h1), step
+        assert np.array_equal(l0, l1), step
