@@ -55,7 +55,8 @@ _i32p = C.POINTER(C.c_int32)
 class KdoConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("hidden", C.c_int32), ("n_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
-                ("vocab", C.c_int32), ("rope_theta", C.c_double), ("rms_eps", C.c_double)]
+                ("vocab", C.c_int32), ("rope_theta", C.c_double), ("rms_eps", C.c_double),
+                ("kv_q8_0", C.c_int32)]
 
 
 class KdoWeights(C.Structure):
@@ -77,6 +78,8 @@ def _declare(L):
     L.kdo_rope_neox.argtypes = [_f64p, C.c_int32, C.c_int32, C.c_double]
     L.kdo_attention_head.argtypes = [_f64p, _u16p, _u16p, C.c_int32, C.c_int32, C.c_int64,
                                      C.c_double, _f64p]
+    L.kdo_q8_0_quantize_f32.argtypes = [_f32p, C.c_int32, _u8p]
+    L.kdo_attention_head_q8.argtypes = [_f64p, _u8p, _u8p, C.c_int32, C.c_int32, C.c_int64, C.c_double, _f64p]
     L.kdo_silu.argtypes = [C.c_double]
     L.kdo_silu.restype = C.c_double
     L.kdo_argmax_f32.argtypes = [_f32p, C.c_int32]
@@ -87,13 +90,13 @@ def _declare(L):
     L.kdo_sample_f32.argtypes = [_f32p, C.c_int32, C.c_float, C.c_uint64, C.c_uint64]
     L.kdo_sample_f32.restype = C.c_int32
     L.kdo_session_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32,
-                                   C.c_int32, _u16p, _u16p, C.c_int32, _f32p, _f32p]
+                                   C.c_int32, C.c_void_p, C.c_void_p, C.c_int32, _f32p, _f32p]
     L.kdo_session_step.restype = C.c_int32
     L.kdo_layer_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32, C.c_int32,
-                                 _u16p, _u16p, C.c_int32, _f64p]
+                                 C.c_void_p, C.c_void_p, C.c_int32, _f64p]
     L.kdo_layer_step.restype = C.c_int32
     L.kdo_decode_step.argtypes = [C.POINTER(KdoConfig), C.POINTER(KdoWeights), C.c_int32,
-                                  _i32p, _i32p, C.POINTER(_u16p), C.POINTER(_u16p), C.c_int32,
+                                  _i32p, _i32p, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int32,
                                   _f32p, _f32p, _i32p]
     L.kdo_decode_step.restype = C.c_int32
 
@@ -156,6 +159,27 @@ def attention_head(q: np.ndarray, K16: np.ndarray, V16: np.ndarray) -> np.ndarra
     return out
 
 
+def q8_0_quantize_f32(x: np.ndarray) -> np.ndarray:
+    """Canonical Q8_0 blocks (uint8 [n/32][34]) of fp32 values, quantised in fp32."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.empty((x.size // 32, 34), dtype=np.uint8)
+    lib().kdo_q8_0_quantize_f32(_p(x, _f32p), x.size, _p(out, _u8p))
+    return out
+
+
+def attention_head_q8(q: np.ndarray, Kq: np.ndarray, Vq: np.ndarray) -> np.ndarray:
+    """q [hd] float64; Kq/Vq uint8 Q8_0 rows [t_kv][hd/32][34]."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    Kq = np.ascontiguousarray(Kq, dtype=np.uint8)
+    Vq = np.ascontiguousarray(Vq, dtype=np.uint8)
+    t = Kq.shape[0]
+    hd = q.size
+    out = np.empty(hd, dtype=np.float64)
+    lib().kdo_attention_head_q8(_p(q, _f64p), _p(Kq, _u8p), _p(Vq, _u8p), t, hd, (hd // 32) * 34,
+                                1.0 / np.sqrt(hd), _p(out, _f64p))
+    return out
+
+
 def silu(y: float) -> float:
     return lib().kdo_silu(float(y))
 
@@ -190,12 +214,13 @@ def sample_f32(logits: np.ndarray, temperature: float, seed: int, counter: int) 
 class OracleModel:
     """Holds references to the host weights (canonical Q8_0) of one model."""
 
-    def __init__(self, shape, weights: dict):
+    def __init__(self, shape, weights: dict, kv_q8_0: bool = False):
         self.shape = shape
         self.w = weights
+        self.kv_q8_0 = bool(kv_q8_0)
         s = shape
         self.cfg = KdoConfig(s.n_layers, s.hidden, s.n_heads, s.n_kv_heads, s.head_dim,
-                             s.ffn, s.vocab, s.rope_theta, s.rms_eps)
+                             s.ffn, s.vocab, s.rope_theta, s.rms_eps, 1 if kv_q8_0 else 0)
         L = s.n_layers
 
         def arr(key, t):
@@ -218,23 +243,36 @@ class OracleModel:
                              t["ffn_norm"])
 
     def new_cache(self, cap: int, k_prefill=None, v_prefill=None):
-        """A session's fp16 KV cache [L][n_kv][cap][hd] (uint16 bits), optionally pre-filled."""
+        """A session's KV cache, optionally pre-filled from fp16 bits [L][n_kv][n][hd]:
+        fp16 [L][n_kv][cap][hd] (uint16 bits), or with kv_q8_0 Q8_0 rows
+        [L][n_kv][cap][hd/32][34] (the pre-filled rows quantised from their fp16 values)."""
         s = self.shape
-        k = np.zeros((s.n_layers, s.n_kv_heads, cap, s.head_dim), dtype=np.uint16)
+        if not self.kv_q8_0:
+            k = np.zeros((s.n_layers, s.n_kv_heads, cap, s.head_dim), dtype=np.uint16)
+            v = np.zeros_like(k)
+            if k_prefill is not None:
+                n = k_prefill.shape[2]
+                k[:, :, :n] = k_prefill
+                v[:, :, :n] = v_prefill
+            return k, v
+        nb = s.head_dim // 32
+        k = np.zeros((s.n_layers, s.n_kv_heads, cap, nb, 34), dtype=np.uint8)
         v = np.zeros_like(k)
         if k_prefill is not None:
             n = k_prefill.shape[2]
-            k[:, :, :n] = k_prefill
-            v[:, :, :n] = v_prefill
+            for src, dst in ((k_prefill, k), (v_prefill, v)):
+                f = np.ascontiguousarray(src).view(np.float16).astype(np.float32)
+                dst[:, :, :n] = q8_0_quantize_f32(f).reshape(s.n_layers, s.n_kv_heads, n, nb, 34)
         return k, v
 
     def layer_step(self, layer: int, pos: int, cache, cap: int, x: np.ndarray) -> np.ndarray:
         """One layer of one session: x (fp64 [hidden]) updated in place; cache = (k, v)."""
         k, v = cache
         s = self.shape
-        off = layer * s.n_kv_heads * cap * s.head_dim
-        kp = C.cast(k.ctypes.data + 2 * off, _u16p)
-        vp = C.cast(v.ctypes.data + 2 * off, _u16p)
+        row = (s.head_dim // 32) * 34 if self.kv_q8_0 else 2 * s.head_dim
+        off = layer * s.n_kv_heads * cap * row
+        kp = C.c_void_p(k.ctypes.data + off)
+        vp = C.c_void_p(v.ctypes.data + off)
         rc = lib().kdo_layer_step(C.byref(self.cfg), C.byref(self.cw), layer, pos, kp, vp, cap,
                                   _p(x, _f64p))
         if rc != 0:
@@ -250,8 +288,8 @@ class OracleModel:
         B = len(tokens)
         tok = np.ascontiguousarray(tokens, dtype=np.int32)
         pos = np.ascontiguousarray(positions, dtype=np.int32)
-        kp = (_u16p * B)(*[_p(c[0], _u16p) for c in caches])
-        vp = (_u16p * B)(*[_p(c[1], _u16p) for c in caches])
+        kp = (C.c_void_p * B)(*[c[0].ctypes.data for c in caches])
+        vp = (C.c_void_p * B)(*[c[1].ctypes.data for c in caches])
         logits = np.empty((B, s.vocab), dtype=np.float32)
         am = np.empty(B, dtype=np.int32)
         hidden = np.empty((B, s.n_layers + 1, s.hidden), dtype=np.float32) if want_hidden else None

@@ -174,6 +174,67 @@ KDO_EXPORT void kdo_attention_head(const double* q, const uint16_t* K, const uin
     free(s);
 }
 
+/* ---------------------------------------------------------------------------
+ * Q8_0 KV cache (the long-context option: memra appends quantized K/V,
+ * `decode_batch_layers` phase A; hf2q ADR-040 measures against llama.cpp with
+ * q8_0 K/V).  A cached head row of hd values is hd/32 canonical blocks.
+ * Quantisation, in fp32 (the precision the kernel takes the integer decision
+ * in): per block d = max|x| / 127, stored as fp16(d); q_j = x_j / d rounded to
+ * the nearest integer, halves away from zero, within [-127, 127]; an all-zero
+ * block gives d = 0, q = 0.  Inputs are finite.  Dequantised value = q * fp16(d).
+ * ------------------------------------------------------------------------- */
+KDO_EXPORT void kdo_q8_0_quantize_f32(const float* x, int32_t n, uint8_t* out) {
+    for (int b = 0; b < n / QK; ++b) {
+        const float* xb = x + (size_t)b * QK;
+        uint8_t* ob = out + (size_t)b * QB;
+        float amax = 0.0f;
+        for (int j = 0; j < QK; ++j) {
+            const float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        const float d = amax / 127.0f;
+        const uint16_t dh = kdo_double_to_half((double)d);
+        ob[0] = (uint8_t)(dh & 0xff);
+        ob[1] = (uint8_t)(dh >> 8);
+        for (int j = 0; j < QK; ++j) {
+            int q = 0;
+            if (d > 0.0f) {
+                q = (int)roundf(xb[j] / d);
+                if (q > 127) q = 127;
+                if (q < -127) q = -127;
+            }
+            ob[2 + j] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
+/* Element i of a cached Q8_0 row. */
+static double q8_row_value(const uint8_t* row, int i) {
+    const uint8_t* blk = row + (size_t)(i / QK) * QB;
+    return (double)(int8_t)blk[2 + i % QK] * q8_scale(blk);
+}
+
+/* kdo_attention_head over a Q8_0 cache: rows of row_bytes, values dequantised. */
+KDO_EXPORT void kdo_attention_head_q8(const double* q, const uint8_t* K, const uint8_t* V, int32_t t_kv,
+                                      int32_t hd, int64_t row_bytes, double scale, double* out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(t_kv > 0 ? t_kv : 1));
+    double m = -INFINITY;
+    for (int t = 0; t < t_kv; ++t) {
+        double dot = 0.0;
+        for (int i = 0; i < hd; ++i) dot += q[i] * q8_row_value(K + (size_t)t * row_bytes, i);
+        s[t] = dot * scale;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int t = 0; t < t_kv; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+    double* acc = (double*)calloc((size_t)hd, sizeof(double));
+    for (int t = 0; t < t_kv; ++t)
+        for (int i = 0; i < hd; ++i) acc[i] += s[t] * q8_row_value(V + (size_t)t * row_bytes, i);
+    for (int i = 0; i < hd; ++i) out[i] = acc[i] / l;
+    free(acc);
+    free(s);
+}
+
 /* silu(y) = y / (1 + e^-y). (`silu_mul(g, u, act, n)` computes silu(g) * u.) */
 KDO_EXPORT double kdo_silu(double y) { return y / (1.0 + exp(-y)); }
 
@@ -261,7 +322,13 @@ KDO_EXPORT int32_t kdo_sample_f32(const float* logits, int32_t n, float temperat
 typedef struct {
     int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
     double rope_theta, rms_eps;
+    int32_t kv_q8_0;  /* 0: fp16 KV caches; 1: Q8_0 KV caches */
 } kdo_config;
+
+/* Bytes of one cached head row. */
+static size_t kv_row_bytes(const kdo_config* c) {
+    return c->kv_q8_0 ? (size_t)(c->head_dim / QK) * QB : (size_t)c->head_dim * 2;
+}
 
 typedef struct {
     const uint8_t* tok_embd;          /* Q8_0 [vocab][hidden/32] */
@@ -280,10 +347,16 @@ typedef struct {
 
 /* One layer of one session (the body of `decode_batch_layers` for one row):
  * x is the fp32-valued residual stream [hidden], updated in place.  The layer's
- * fp16 caches are [n_kv][cap][hd]; row `pos` is written, rows 0..pos are read. */
+ * caches are [n_kv][cap] rows (fp16 [hd], or Q8_0 blocks with kv_q8_0); row
+ * `pos` is written, rows 0..pos are read. */
 KDO_EXPORT int32_t kdo_layer_step(const kdo_config* c, const kdo_weights* w, int32_t l,
-                                  int32_t pos, uint16_t* Kl, uint16_t* Vl, int32_t cap,
+                                  int32_t pos, void* Kv, void* Vv, int32_t cap,
                                   double* x) {
+    uint16_t* Kl = (uint16_t*)Kv;
+    uint16_t* Vl = (uint16_t*)Vv;
+    uint8_t* Kq = (uint8_t*)Kv;
+    uint8_t* Vq = (uint8_t*)Vv;
+    const size_t rb = kv_row_bytes(c);
     const int H = c->hidden, nh = c->n_heads, nkv = c->n_kv_heads, hd = c->head_dim;
     const int F = c->ffn;
     if (l < 0 || l >= c->n_layers || pos < 0 || pos >= cap || nh % nkv || hd % 2) return -1;
@@ -307,18 +380,34 @@ KDO_EXPORT int32_t kdo_layer_step(const kdo_config* c, const kdo_weights* w, int
     /* RoPE of q and k at this session's own position. */
     for (int h = 0; h < nh; ++h) kdo_rope_neox(q + h * hd, hd, pos, c->rope_theta);
     for (int h = 0; h < nkv; ++h) kdo_rope_neox(k + h * hd, hd, pos, c->rope_theta);
-    /* KV append: row `pos` of this session's cache, stored as fp16. */
-    for (int h = 0; h < nkv; ++h)
-        for (int i = 0; i < hd; ++i) {
-            Kl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(k[h * hd + i]);
-            Vl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(v[h * hd + i]);
+    /* KV append: row `pos` of this session's cache, stored as fp16, or (Q8_0
+     * cache) the row as fp32, quantised. */
+    if (!c->kv_q8_0) {
+        for (int h = 0; h < nkv; ++h)
+            for (int i = 0; i < hd; ++i) {
+                Kl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(k[h * hd + i]);
+                Vl[((size_t)h * cap + pos) * hd + i] = kdo_double_to_half(v[h * hd + i]);
+            }
+    } else {
+        float* rowf = malloc(sizeof(float) * hd);
+        for (int h = 0; h < nkv; ++h) {
+            for (int i = 0; i < hd; ++i) rowf[i] = (float)k[h * hd + i];
+            kdo_q8_0_quantize_f32(rowf, hd, Kq + ((size_t)h * cap + pos) * rb);
+            for (int i = 0; i < hd; ++i) rowf[i] = (float)v[h * hd + i];
+            kdo_q8_0_quantize_f32(rowf, hd, Vq + ((size_t)h * cap + pos) * rb);
         }
+        free(rowf);
+    }
     /* Attention over keys 0..pos (t_kv = pos + 1), GQA head mapping h -> h / group. */
 #pragma omp parallel for schedule(static)
     for (int h = 0; h < nh; ++h) {
         int kh = h / group;
-        kdo_attention_head(q + h * hd, Kl + (size_t)kh * cap * hd, Vl + (size_t)kh * cap * hd,
-                           pos + 1, hd, hd, scale, att + h * hd);
+        if (!c->kv_q8_0)
+            kdo_attention_head(q + h * hd, Kl + (size_t)kh * cap * hd, Vl + (size_t)kh * cap * hd,
+                               pos + 1, hd, hd, scale, att + h * hd);
+        else
+            kdo_attention_head_q8(q + h * hd, Kq + (size_t)kh * cap * rb, Vq + (size_t)kh * cap * rb,
+                                  pos + 1, hd, (int64_t)rb, scale, att + h * hd);
     }
     for (int i = 0; i < nh * hd; ++i) att[i] = round_half(att[i]);
     /* o-projection and residual add (fp32 residual). */
@@ -336,16 +425,18 @@ KDO_EXPORT int32_t kdo_layer_step(const kdo_config* c, const kdo_weights* w, int
     return 0;
 }
 
-/* One session, one step.  k_cache / v_cache are the session's fp16 caches,
- * [n_layers][n_kv][cap][hd]; rows 0..pos-1 hold its history, row `pos` is
- * overwritten with this step's key/value, rows beyond pos are never read.
+/* One session, one step.  k_cache / v_cache are the session's caches,
+ * [n_layers][n_kv][cap] rows (fp16 [hd], or Q8_0 blocks); rows 0..pos-1 hold its
+ * history, row `pos` is overwritten with this step's key/value, rows beyond pos
+ * are never read.
  * logits: [vocab] fp32.  hidden: NULL or [n_layers+1][hidden] fp32, the residual
  * after the embedding and after every layer. */
 KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
                                     int32_t token, int32_t pos,
-                                    uint16_t* k_cache, uint16_t* v_cache, int32_t cap,
+                                    void* k_cache, void* v_cache, int32_t cap,
                                     float* logits, float* hidden) {
-    const int H = c->hidden, nkv = c->n_kv_heads, hd = c->head_dim;
+    const int H = c->hidden, nkv = c->n_kv_heads;
+    const size_t layer_bytes = (size_t)nkv * cap * kv_row_bytes(c);
     const int V = c->vocab, L = c->n_layers;
     if (token < 0 || token >= V || pos < 0 || pos >= cap) return -1;
     double* x = malloc(sizeof(double) * H);
@@ -359,8 +450,8 @@ KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
 
     int32_t rc = 0;
     for (int l = 0; l < L && rc == 0; ++l) {
-        rc = kdo_layer_step(c, w, l, pos, k_cache + (size_t)l * nkv * cap * hd,
-                            v_cache + (size_t)l * nkv * cap * hd, cap, x);
+        rc = kdo_layer_step(c, w, l, pos, (uint8_t*)k_cache + (size_t)l * layer_bytes,
+                            (uint8_t*)v_cache + (size_t)l * layer_bytes, cap, x);
         if (hidden) for (int i = 0; i < H; ++i) hidden[(size_t)(l + 1) * H + i] = (float)x[i];
     }
     if (rc == 0) {
@@ -378,7 +469,7 @@ KDO_EXPORT int32_t kdo_session_step(const kdo_config* c, const kdo_weights* w,
  * logits [B][vocab]; hidden NULL or [B][n_layers+1][hidden]; argmax [B]. */
 KDO_EXPORT int32_t kdo_decode_step(const kdo_config* c, const kdo_weights* w, int32_t B,
                                    const int32_t* tokens, const int32_t* positions,
-                                   uint16_t* const* k_caches, uint16_t* const* v_caches,
+                                   void* const* k_caches, void* const* v_caches,
                                    int32_t cap, float* logits, float* hidden, int32_t* argmax) {
     for (int b = 0; b < B; ++b) {
         float* lg = logits + (size_t)b * c->vocab;
