@@ -41,15 +41,18 @@ METRIC = "aggregate decode tok/s (8B-shaped Q8_0, B sessions, 1 GB300)"
 FALLBACK_HBM_GBS = 6800.0
 
 
-def kv_bytes_per_pos(s):
-    return 2 * s.n_layers * s.n_kv_heads * s.head_dim * 2  # K and V, fp16
+def kv_bytes_per_pos(s, kv_q8=False):
+    """K and V bytes of one position over all layers and KV heads: fp16 rows, or
+    Q8_0 rows (a quant byte per value and an fp16 scale per 32 values)."""
+    row = s.head_dim + s.head_dim // 32 * 2 if kv_q8 else s.head_dim * 2
+    return 2 * s.n_layers * s.n_kv_heads * row
 
 
-def step_bytes(s, positions):
+def step_bytes(s, positions, kv_q8=False):
     """Algorithmic HBM bytes of one step: every weight once, the embedding rows,
     the KV rows attended (incl. the new one) and the new rows written."""
     B = len(positions)
-    kvb = kv_bytes_per_pos(s)
+    kvb = kv_bytes_per_pos(s, kv_q8)
     return (s.weight_bytes() + B * (s.hidden // 32) * 34 + sum(int(p) + 1 for p in positions) * kvb
             + B * kvb)
 
@@ -373,9 +376,10 @@ def run_op_mmvq(args):
     return dict(op="mmvq", **time_mmvq(args.rows, args.cols, args.m, args.steps, args.warmup))
 
 
-def time_attn(B, cap, steps, warmup):
+def time_attn(B, cap, steps, warmup, kv_q8=False):
     """Isolated KV append + ragged split-K flash-decode: 32/8 heads of 128, B sessions with
-    attended lengths uniform in [1, cap] (seeded), fp16 KV ~N(0,1)."""
+    attended lengths uniform in [1, cap] (seeded), KV ~N(0,1) in fp16 (or, kv_q8, those
+    values quantised to Q8_0)."""
     import torch
 
     import session_decode_step_gb300 as kd
@@ -384,8 +388,19 @@ def time_attn(B, cap, steps, warmup):
     lens = synth.ragged_lengths(0, "attn-config", B, 1, cap)
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
-    kc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
-    vc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
+    if kv_q8:
+        planes = []
+        for _ in range(2):
+            x = torch.randn(B, nkv, cap, hd, device="cuda", generator=g)
+            qs = torch.empty(B, nkv, cap, hd, dtype=torch.uint8, device="cuda")
+            sc = torch.empty(B, nkv, cap, hd // 32, dtype=torch.int16, device="cuda")
+            kd.kd_kv_q8_quantize(x, qs, sc)
+            planes += [qs, sc]
+            del x
+        kc = vc = None
+    else:
+        kc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
+        vc = torch.randn(B, nkv, cap, hd, device="cuda", generator=g).to(torch.float16)
     q = torch.randn(B, nh, hd, device="cuda", generator=g)
     kn = torch.randn(B, nkv, hd, device="cuda", generator=g)
     vn = torch.randn(B, nkv, hd, device="cuda", generator=g)
@@ -394,20 +409,27 @@ def time_attn(B, cap, steps, warmup):
     slots = np.arange(B, dtype=np.int32)
     pos = (lens - 1).astype(np.int32)
     st = torch.cuda.current_stream()
+
+    def call():
+        if kv_q8:
+            kd.kd_attn_append_decode_q8(q, kn, vn, *planes, slots, pos, nh, nkv, B, cap, out, ws, st)
+        else:
+            kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
     for _ in range(max(3, warmup)):
-        kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
+        call()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     for _ in range(steps):
-        kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws, st)
+        call()
     e1.record(st)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / steps
-    alg = int(lens.sum()) * nkv * hd * 2 * 2 + B * nkv * hd * 2 * 2
+    row = hd + hd // 32 * 2 if kv_q8 else hd * 2  # K or V bytes of one head row
+    alg = int(lens.sum()) * nkv * row * 2 + B * nkv * row * 2
     peak, kind = read_peaks()
     status = kd.kd_attn_device_status(ws, st)
-    return {"B": B, "cap": cap, "sum_t_kv": int(lens.sum()), "launches": steps,
+    return {"B": B, "cap": cap, "kv": "q8_0" if kv_q8 else "fp16", "sum_t_kv": int(lens.sum()), "launches": steps,
             "avg_us": round(us, 3), "alg_bytes": alg, "gbs": round(alg / us / 1e3, 1), "peak": peak,
             "peak_source": kind, "frac": round(alg / us / 1e3 / peak, 4), "device_status": status,
             "note": "per call: host-staged descriptor copy, append, split kernel, combine"}
@@ -419,12 +441,13 @@ def run_op_attn(args):
     from session_decode_step_gb300 import build as kbuild
     kbuild.build()
     torch.cuda.set_device(0)
-    return dict(op="attn_append_decode", **time_attn(args.m, args.cap, args.steps, args.warmup))
+    return dict(op="attn_append_decode", **time_attn(args.m, args.cap, args.steps, args.warmup, args.kv_q8))
 
 
-def time_long(steps, warmup, w=None):
+def time_long(steps, warmup, w=None, kv_q8=False):
     """The long-context multi-tenant workload: 8 sessions in 32768-position slots, pre-filled to
-    25704 + 1000 i (i = 0..7) fp16 positions, each step at its own position (64 positions cycling)."""
+    25704 + 1000 i (i = 0..7) fp16 positions, each step at its own position (64 positions cycling);
+    kv_q8: the cache held as Q8_0 (KD_FLAG_KV_Q8_0)."""
     import torch
 
     import session_decode_step_gb300 as kd
@@ -433,7 +456,8 @@ def time_long(steps, warmup, w=None):
     lens = [c["prefill_base"] + c["prefill_stagger"] * i for i in range(S)]
     if w is None:
         w = synth.model_weights(shape, seed=c["seed"])
-    m = kd.kd_model_load(kd.make_config(shape, max_sessions=S, max_ctx=cap), w)
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=S, max_ctx=cap,
+                                        flags=kd.KD_FLAG_KV_Q8_0 if kv_q8 else 0), w)
     ids = []
     for i, n in enumerate(lens):
         k, v = synth.kv_prefill(shape, c["seed"], 1000 + i, n)
@@ -458,14 +482,14 @@ def time_long(steps, warmup, w=None):
     for i in range(steps):
         p = pos(i)
         kd.kd_decode_step(m, ids, tok, p, None, am, st)
-        byts += step_bytes(shape, p)
+        byts += step_bytes(shape, p, kv_q8)
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     peak, kind = read_peaks()
     status = kd.kd_device_status(m)
     kd.kd_model_free(m)
-    return {"B": S, "capacity": cap, "positions": f"{lens[0]}..{lens[-1] + win - 1}",
+    return {"B": S, "capacity": cap, "kv": "q8_0" if kv_q8 else "fp16", "positions": f"{lens[0]}..{lens[-1] + win - 1}",
             "steps": steps, "ms_per_step": round(ms, 4), "tok_s": round(S / (ms / 1e3), 1),
             "alg_bytes_per_step": int(byts / steps), "gbs": round(byts / steps / (ms / 1e3) / 1e9, 1),
             "peak": peak, "peak_source": kind, "frac": round(byts / steps / (ms / 1e3) / 1e9 / peak, 4),
@@ -478,7 +502,7 @@ def run_op_long(args):
     from session_decode_step_gb300 import build as kbuild
     kbuild.build()
     torch.cuda.set_device(0)
-    return dict(op="long_context_step", **time_long(args.steps, args.warmup))
+    return dict(op="long_context_step", **time_long(args.steps, args.warmup, kv_q8=args.kv_q8))
 
 
 def run_op_step(args):
@@ -592,10 +616,13 @@ def other_workloads(steps, warmup, w):
     """The workloads other than the headline one, measured in the same run: the
     long-context step, the isolated mmvq at every m, the isolated ragged attention."""
     c2, c3 = synth.MMVQ_CASE, synth.RAGGED_ATTN_CASE
-    out = {"long_context": time_long(max(16, min(steps, synth.LONG_CTX_8B_CASE["steps"])), warmup, w)}
+    nl = max(16, min(steps, synth.LONG_CTX_8B_CASE["steps"]))
+    out = {"long_context": time_long(nl, warmup, w), "long_context_kv_q8": time_long(nl, warmup, w, kv_q8=True)}
     out["isolated_mmvq"] = [time_mmvq(R, K, m, max(50, min(steps, 200)), warmup)
                             for R, K in c2["matrices"] for m in c2["rows_m"]]
     out["isolated_attention"] = time_attn(c3["sessions"], c3["max_ctx"], max(50, min(steps, 200)), warmup)
+    out["isolated_attention_kv_q8"] = time_attn(c3["sessions"], c3["max_ctx"], max(50, min(steps, 200)), warmup,
+                                                kv_q8=True)
     return out
 
 
@@ -659,6 +686,7 @@ def main():
     ap.add_argument("--cols", type=int, default=14336)
     ap.add_argument("--m", type=int, default=8)
     ap.add_argument("--cap", type=int, default=32768)
+    ap.add_argument("--kv-q8", action="store_true", help="--op attn / long: the Q8_0 KV cache")
     args = ap.parse_args()
     if args.op:
         r = {"mmvq": run_op_mmvq, "attn": run_op_attn, "long": run_op_long, "step": run_op_step,

@@ -90,6 +90,15 @@ typedef struct {
  * as kernels of their own.  Bit-identical to the fused epilogues; for testing
  * and measurement. */
 #define KD_FLAG_UNFUSED 64
+/* The KV cache in Q8_0 (the long-context option; memra appends quantised K/V in
+ * `decode_batch_layers` phase A, hf2q ADR-040 measures llama.cpp with q8_0
+ * K/V): each cached head row is 128 quants and 4 fp16 block scales (136 bytes
+ * instead of 256).  Per 32-value block d = max|x| / 127 in fp32, stored as
+ * fp16(d); q = x / d rounded half away from zero within [-127, 127]; value =
+ * q * fp16(d).  New rows are quantised from the step's fp32 k (after RoPE) and
+ * v; kd_session_load_kv quantises its fp16 input the same way.  Needs
+ * head_dim 128 and an even max_ctx (else KD_ERR_UNSUPPORTED). */
+#define KD_FLAG_KV_Q8_0 128
 
 /* Host weights.  Matrices are canonical Q8_0: row-major [rows][cols/32] blocks
  * of {fp16 scale d (little-endian); int8 q[32]} (34 bytes), value = q * d, the
@@ -390,6 +399,25 @@ kd_status kd_attn_append_decode(const float* q, const float* k_new, const float*
  * when no bounded wait ran out; otherwise KD_ERR_DEVICE (that call's output is
  * not valid).  Each call clears its word when it starts. */
 kd_status kd_attn_device_status(const void* workspace, int32_t* flags_out, kd_stream stream);
+
+/* The Q8_0 KV row format (KD_FLAG_KV_Q8_0), for the isolated workloads: rows of
+ * 128 values as 128 quant bytes u = q + 128 (uint8 [rows][128]) and 4 fp16 block
+ * scales (uint16 bits [rows][4]), quantised as KD_FLAG_KV_Q8_0 states.
+ * kd_kv_q8_quantize: src device fp32 [rows][128] -> quants, scales (device). */
+kd_status kd_kv_q8_quantize(const float* src, int64_t rows, uint8_t* quants, uint16_t* scales, kd_stream stream);
+
+/* kd_attn_append_decode over a Q8_0 cache of head_dim 128: the new rows (fp32,
+ * k_new / v_new as for kd_attn_append_decode) are quantised into row pos_b of
+ * slot_b, then every session attends keys 0..pos_b.  Caches:
+ * [n_slots][n_kv_heads][cap] rows of quants ([..][128] uint8) and scales
+ * ([..][4] fp16 bits); cap even.  Workspace: kd_attn_workspace_bytes(B, n_heads,
+ * 128, cap).  All device buffers 16-byte aligned.  Other arguments and errors
+ * as for kd_attn_append_decode. */
+kd_status kd_attn_append_decode_q8(const float* q, const float* k_new, const float* v_new, uint8_t* k_quants,
+                                   uint16_t* k_scales, uint8_t* v_quants, uint16_t* v_scales,
+                                   const int32_t* slots, const int32_t* positions, int32_t B, int32_t n_heads,
+                                   int32_t n_kv_heads, int32_t n_slots, int32_t cap, uint16_t* out,
+                                   void* workspace, size_t workspace_bytes, kd_stream stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free variant (no counterpart on the batched-decode pages: it

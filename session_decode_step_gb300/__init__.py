@@ -19,6 +19,11 @@ LIB_PATH = _PKG / "libkd.so"
 KD_MAX_BATCH = 16
 KD_ATTN_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 KD_FLAG_NO_GRAPH = 1
+KD_FLAG_SCHEDULE_STREAM = 2
+KD_FLAG_SCHEDULE_GROUP = 4
+KD_FLAG_FUSED_NORM = 32
+KD_FLAG_UNFUSED = 64
+KD_FLAG_KV_Q8_0 = 128
 STATUS = {0: "KD_OK", -1: "KD_ERR_INVALID_ARG", -2: "KD_ERR_OOM", -3: "KD_ERR_CUDA",
           -4: "KD_ERR_NO_FREE_SLOT", -5: "KD_ERR_BAD_SESSION", -6: "KD_ERR_POSITION",
           -7: "KD_ERR_BATCH", -8: "KD_ERR_UNSUPPORTED", -9: "KD_ERR_DEVICE"}
@@ -103,6 +108,9 @@ def lib():
                                       i32, _vp, _vp, C.c_size_t, _vp],
             "kd_attn_append_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                               i32, _vp, _vp],
+            "kd_kv_q8_quantize": [_vp, C.c_int64, _vp, _vp, _vp],
+            "kd_attn_append_decode_q8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
+                                         _vp, _vp, C.c_size_t, _vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -366,6 +374,27 @@ def kd_attn_append_decode(q, k_new, v_new, k_cache, v_cache, slots, positions, n
                                        sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p), B, n_heads,
                                        n_kv_heads, head_dim, n_slots, cap, _ptr(out), _ptr(workspace),
                                        nbytes, _stream(stream)))
+
+
+def kd_kv_q8_quantize(src, quants, scales, stream=None):
+    """Rows of 128 fp32 values (device [rows][128]) into Q8_0 quants (uint8
+    [rows][128], q + 128) and fp16 block scales ([rows][4], as int16/uint16 bits)."""
+    rows = src.numel() // 128
+    _check(lib().kd_kv_q8_quantize(_ptr(src), rows, _ptr(quants), _ptr(scales), _stream(stream)))
+
+
+def kd_attn_append_decode_q8(q, k_new, v_new, k_quants, k_scales, v_quants, v_scales, slots, positions, n_heads,
+                             n_kv_heads, n_slots, cap, out, workspace, stream=None):
+    """kd_attn_append_decode over a Q8_0 cache of head_dim 128 (see include/kd.h)."""
+    sl = _i32(slots)
+    B = sl.size
+    ps = _i32(positions, B)
+    i32p = C.POINTER(C.c_int32)
+    nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else workspace.nbytes
+    _check(lib().kd_attn_append_decode_q8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_quants), _ptr(k_scales),
+                                          _ptr(v_quants), _ptr(v_scales), sl.ctypes.data_as(i32p),
+                                          ps.ctypes.data_as(i32p), B, n_heads, n_kv_heads, n_slots, cap, _ptr(out),
+                                          _ptr(workspace), nbytes, _stream(stream)))
 
 
 def kd_attn_device_status(workspace=None, stream=None) -> int:

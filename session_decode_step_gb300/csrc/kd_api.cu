@@ -61,6 +61,7 @@ cudaError_t init_device_attributes(int dev) {
     std::call_once(g_attr_once[dev], [dev] {
         cudaError_t e = kd::mmvq_init_attributes();
         if (e == cudaSuccess) e = kd::attn_init_attributes();
+        if (e == cudaSuccess) e = kd::attn_q8_init_attributes();
         if (e == cudaSuccess) e = kd::rowops_init_attributes();
         g_attr_err[dev] = e;
     });
@@ -136,8 +137,15 @@ struct kd_model {
     PackedQ8 head;
     float* norms = nullptr;   // [2L+1][H]: attn_norm l, ffn_norm l, then output_norm
     float2* rope = nullptr;   // [max_ctx][hd/2]
-    __half* kc = nullptr;     // [L][slots][nkv][cap][hd]
+    __half* kc = nullptr;     // [L][slots][nkv][cap][hd] (fp16 KV)
     __half* vc = nullptr;
+    bool kvq8 = false;        // Q8_0 KV cache (KD_FLAG_KV_Q8_0)
+    uint8_t* kq = nullptr;    // [L][slots][nkv][cap][128] quants u = q + 128
+    uint8_t* vq = nullptr;
+    __half* ks = nullptr;     // [L][slots][nkv][cap][4] block scales
+    __half* vs = nullptr;
+    float* knew = nullptr;    // [16][nkv][hd] the step's rotated k rows before quantisation
+    float* vnew = nullptr;
     size_t layer_kv = 0;      // elements per layer of one arena
     kd::AttnMaps kmaps{};     // tensor maps over the K and V arenas
     CUtensorMap map_xn{}, map_attn{}, map_act{};  // activation maps the projections read through
@@ -216,6 +224,9 @@ static kd_status check_config(const kd_config* c) {
         return fail(KD_ERR_UNSUPPORTED,
                     "kd_config: need hidden, ffn, n_heads*head_dim multiples of 128, vocab a multiple "
                     "of 32, head_dim in {64,128}, n_heads/n_kv_heads in {1,2,4,8}");
+    if ((c->flags & KD_FLAG_KV_Q8_0) && (!kd::attn_q8_supported(c->head_dim, c->n_heads / c->n_kv_heads) ||
+                                         c->max_ctx % 2))
+        return fail(KD_ERR_UNSUPPORTED, "kd_config: the Q8_0 KV cache needs head_dim 128 and an even max_ctx");
     return KD_OK;
 }
 
@@ -290,13 +301,26 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     }
 
     // ---- KV arena and workspaces
-    m->layer_kv = (size_t)S * nkv * cap * hd;
-    KD_CK(m->alloc(&m->kc, (size_t)L * m->layer_kv * sizeof(__half)));
-    KD_CK(m->alloc(&m->vc, (size_t)L * m->layer_kv * sizeof(__half)));
-    KD_CK(cudaMemset(m->kc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
-    KD_CK(cudaMemset(m->vc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
-    KD_CK(kd::make_attn_maps(m->kc, m->vc, (long)L * S * nkv * cap, hd, &m->kmaps));
     const int MB = KD_MAX_BATCH;
+    m->layer_kv = (size_t)S * nkv * cap * hd;
+    if (!m->kvq8) {
+        KD_CK(m->alloc(&m->kc, (size_t)L * m->layer_kv * sizeof(__half)));
+        KD_CK(m->alloc(&m->vc, (size_t)L * m->layer_kv * sizeof(__half)));
+        KD_CK(cudaMemset(m->kc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
+        KD_CK(cudaMemset(m->vc, 0, (size_t)L * m->layer_kv * sizeof(__half)));
+        KD_CK(kd::make_attn_maps(m->kc, m->vc, (long)L * S * nkv * cap, hd, &m->kmaps));
+    } else {
+        const size_t rows = (size_t)L * S * nkv * cap;
+        KD_CK(m->alloc(&m->kq, rows * 128));
+        KD_CK(m->alloc(&m->vq, rows * 128));
+        KD_CK(m->alloc(&m->ks, rows * 4 * sizeof(__half) + 16));  // + a 16-byte tail for rounded scale copies
+        KD_CK(m->alloc(&m->vs, rows * 4 * sizeof(__half) + 16));
+        for (void* p : {(void*)m->kq, (void*)m->vq}) KD_CK(cudaMemset(p, 0x80, rows * 128));  // q = 0
+        for (void* p : {(void*)m->ks, (void*)m->vs}) KD_CK(cudaMemset(p, 0, rows * 4 * sizeof(__half) + 16));
+        KD_CK(kd::make_attn_q8_maps(m->kq, m->vq, (long)rows, &m->kmaps));
+        KD_CK(m->alloc(&m->knew, (size_t)MB * nkv * hd * sizeof(float)));
+        KD_CK(m->alloc(&m->vnew, (size_t)MB * nkv * hd * sizeof(float)));
+    }
     KD_CK(m->alloc(&m->x, (size_t)MB * H * sizeof(float)));
     KD_CK(m->alloc(&m->xn, (size_t)MB * H * sizeof(__half)));
     KD_CK(m->alloc(&m->ssq, (size_t)(H / kd::GROUP_ROWS) * kd::MAX_NORM_SLOTS * sizeof(float)));
@@ -461,6 +485,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
         if (fq) norm_in(a, attn_w);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
+        if (m->kvq8) { a.k_out = m->knew; a.v_out = m->vnew; }
         a.nh = nh; a.nkv = nkv; a.hd = hd; a.cap = c.max_ctx;
         a.inject_tx = inject(KD_K_QKV);
         a.tl = tl_next();
@@ -472,7 +497,15 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         t.max_splits = m->max_splits; t.out = m->attn; t.err = m->err;
         t.inject_tx = inject(KD_K_ATTN_SPLIT);
         t.tl = tl_next();
-        KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->kmaps, m->attn_grid, pdl, s));
+        if (!m->kvq8) {
+            KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split(t, m->kmaps, m->attn_grid, pdl, s));
+        } else {  // quantised append of the new rows, then the attention over the Q8_0 cache
+            t.ks = m->ks;
+            t.vs = m->vs;
+            KD_RUN(KD_K_ATTN_SPLIT, kd::launch_kvq8_append(m->knew, m->vnew, m->kq, m->ks, m->vq, m->vs, slot, pos, B,
+                                                           nkv, c.max_ctx, t.row0, pdl, s));
+            KD_RUN(KD_K_ATTN_SPLIT, kd::launch_attn_split_q8(t, m->kmaps, m->num_sms, pdl, s));
+        }
         t.tl = tl_next();
         KD_RUN(KD_K_ATTN_COMBINE, kd::launch_attn_combine(t, pdl, s));
         a = mm(m->wo[l], m->attn);
@@ -560,6 +593,7 @@ kd_status kd_model_load(const kd_config* cfg, const kd_weights* w, kd_model** ou
     kd_model* m = new (std::nothrow) kd_model();
     if (!m) return fail(KD_ERR_OOM, "kd_model_load: host allocation failed");
     m->cfg = *cfg;
+    m->kvq8 = (cfg->flags & KD_FLAG_KV_Q8_0) != 0;
     st = load_impl(m, w);
     if (st != KD_OK) {
         m->release();
@@ -630,6 +664,26 @@ kd_status kd_session_load_kv(kd_model* m, int32_t id, const void* k, const void*
     cudaStream_t s = (cudaStream_t)stream;
     KD_CK(cudaStreamWaitEvent(s, m->last_step, 0));
     const kd_config& c = m->cfg;
+    if (m->kvq8 && len > 0) {
+        // Q8_0 cache: the fp16 rows to a stream-ordered temporary, quantised into the slot's rows.
+        const size_t n_rows = (size_t)c.n_layers * c.n_kv_heads * len, bytes = n_rows * c.head_dim * sizeof(__half);
+        void* tmp = nullptr;
+        KD_CK(cudaMallocAsync(&tmp, bytes, s));
+        const long layer_rows = (long)c.max_sessions * c.n_kv_heads * c.max_ctx, base = (long)id * c.n_kv_heads * c.max_ctx;
+        cudaError_t e = cudaSuccess;
+        for (int part = 0; part < 2 && e == cudaSuccess; ++part) {
+            e = cudaMemcpyAsync(tmp, part ? v : k, bytes, cudaMemcpyDefault, s);
+            if (e == cudaSuccess)
+                e = kd::launch_kvq8_rows(tmp, true, (long)n_rows, c.n_kv_heads, len, c.max_ctx, layer_rows, base,
+                                         part ? m->vq : m->kq, part ? m->vs : m->ks, s);
+        }
+        const cudaError_t e2 = cudaFreeAsync(tmp, s);
+        KD_CK(e);
+        KD_CK(e2);
+        KD_CK(cudaEventRecord(m->last_step, s));
+        m->len[id] = len;
+        return KD_OK;
+    }
     const size_t row = (size_t)c.head_dim * sizeof(__half);
     for (int l = 0; l < c.n_layers && len > 0; ++l) {
         const size_t dst = (size_t)l * m->layer_kv + (size_t)id * c.n_kv_heads * c.max_ctx * c.head_dim;
@@ -1036,6 +1090,76 @@ kd_status kd_attn_device_status(const void* workspace, int32_t* flags_out, kd_st
     KD_CK(cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost));
     *flags_out = v;
     if (v) return fail(KD_ERR_DEVICE, "attention: a kernel gave up a bounded wait (flags 0x%x)", v);
+    return KD_OK;
+}
+
+kd_status kd_kv_q8_quantize(const float* src, int64_t rows, uint8_t* quants, uint16_t* scales, kd_stream stream) {
+    if (!src || !quants || !scales) return fail(KD_ERR_INVALID_ARG, "kd_kv_q8_quantize: null argument");
+    if (rows < 1 || rows > 0x7fffffff) return fail(KD_ERR_INVALID_ARG, "kd_kv_q8_quantize: rows=%lld", (long long)rows);
+    int dev = 0;
+    KD_CK(cudaGetDevice(&dev));
+    KD_CK(init_device_attributes(dev));
+    KD_CK(kd::launch_kvq8_rows(src, false, (long)rows, 1, (int)rows, (int)rows, 0, 0, quants,
+                               reinterpret_cast<__half*>(scales), (cudaStream_t)stream));
+    return KD_OK;
+}
+
+kd_status kd_attn_append_decode_q8(const float* q, const float* k_new, const float* v_new, uint8_t* k_quants,
+                                   uint16_t* k_scales, uint8_t* v_quants, uint16_t* v_scales, const int32_t* slots,
+                                   const int32_t* positions, int32_t B, int32_t n_heads, int32_t n_kv_heads,
+                                   int32_t n_slots, int32_t cap, uint16_t* out, void* workspace,
+                                   size_t workspace_bytes, kd_stream stream) {
+    if (!q || !k_new || !v_new || !k_quants || !k_scales || !v_quants || !v_scales || !slots || !positions || !out ||
+        !workspace)
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_q8: null argument");
+    if (B < 1 || B > KD_MAX_BATCH) return fail(KD_ERR_BATCH, "kd_attn_append_decode_q8: B=%d", B);
+    if (n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads || !kd::attn_q8_supported(128, n_heads / n_kv_heads))
+        return fail(KD_ERR_UNSUPPORTED, "kd_attn_append_decode_q8: group %d", n_kv_heads > 0 ? n_heads / n_kv_heads : 0);
+    if (n_slots < 1 || cap < 2 || cap % 2) return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_q8: n_slots/cap");
+    if ((cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK > kd::ATT_MAX_SPLITS)
+        return fail(KD_ERR_UNSUPPORTED, "kd_attn_append_decode_q8: cap %d exceeds %d", cap,
+                    kd::ATT_MAX_SPLITS * kd::ATT_CHUNK);
+    if (workspace_bytes < kd_attn_workspace_bytes(B, n_heads, 128, cap))
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_q8: workspace too small");
+    if ((((uintptr_t)workspace | (uintptr_t)k_quants | (uintptr_t)v_quants | (uintptr_t)k_scales |
+          (uintptr_t)v_scales | (uintptr_t)q) & 15))
+        return fail(KD_ERR_INVALID_ARG, "kd_attn_append_decode_q8: buffers must be 16-byte aligned");
+    int32_t desc[2 * KD_MAX_BATCH] = {};
+    for (int b = 0; b < B; ++b) {
+        if (slots[b] < 0 || slots[b] >= n_slots) return fail(KD_ERR_BAD_SESSION, "slot %d", slots[b]);
+        for (int j = 0; j < b; ++j)
+            if (slots[j] == slots[b]) return fail(KD_ERR_BAD_SESSION, "slot %d repeated", slots[b]);
+        if (positions[b] < 0 || positions[b] >= cap)
+            return fail(KD_ERR_POSITION, "position %d outside [0, %d)", positions[b], cap);
+        desc[b] = slots[b];
+        desc[KD_MAX_BATCH + b] = positions[b];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0, sms = 0;
+    KD_CK(cudaGetDevice(&dev));
+    KD_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    KD_CK(init_device_attributes(dev));
+    int* d_desc = (int*)workspace;
+    int* d_err = d_desc + 2 * KD_MAX_BATCH;
+    KD_CK(cudaMemcpyAsync(d_desc, desc, sizeof desc, cudaMemcpyHostToDevice, s));
+    KD_CK(cudaMemsetAsync(d_err, 0, sizeof(int), s));
+    __half* ksc = reinterpret_cast<__half*>(k_scales);
+    __half* vsc = reinterpret_cast<__half*>(v_scales);
+    KD_CK(kd::launch_kvq8_append(k_new, v_new, k_quants, ksc, v_quants, vsc, d_desc, d_desc + KD_MAX_BATCH, B,
+                                 n_kv_heads, cap, 0, false, s));
+    kd::AttnMaps maps;
+    KD_CK(kd::make_attn_q8_maps(k_quants, v_quants, (long)n_slots * n_kv_heads * cap, &maps));
+    kd::AttnArgs t{};
+    t.q = q; t.row0 = 0; t.slot = d_desc; t.pos = d_desc + KD_MAX_BATCH; t.B = B; t.nh = n_heads; t.nkv = n_kv_heads;
+    t.hd = 128; t.cap = cap; t.scale = 1.0f / std::sqrt(128.0f);
+    t.part = (float*)((char*)workspace + 256);
+    t.max_splits = (cap + kd::ATT_CHUNK - 1) / kd::ATT_CHUNK;
+    t.out = (__half*)out;
+    t.err = d_err;
+    t.ks = ksc;
+    t.vs = vsc;
+    KD_CK(kd::launch_attn_split_q8(t, maps, sms, false, s));
+    KD_CK(kd::launch_attn_combine(t, false, s));
     return KD_OK;
 }
 

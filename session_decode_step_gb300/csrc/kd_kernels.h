@@ -122,6 +122,11 @@ struct MmvqArgs {
     const int* pos;      // [B]
     const float2* rope;  // [max_ctx][hd/2] (cos, sin)
     int nh, nkv, hd, cap;
+    // Q8_0 KV cache: the epilogue leaves the rotated k and v rows in fp32
+    // [B][nkv][hd] here (quantised into the arena by launch_kvq8_append) instead
+    // of writing fp16 rows into kc / vc.
+    float* k_out;
+    float* v_out;
 };
 
 // xmap: make_x_map of a.x with at least B rows.
@@ -156,6 +161,10 @@ struct AttnArgs {
     int* err;
     int inject_tx;        // debug fault hook (0 in normal use): extra bytes item 0's K tile waits for
     unsigned long long* tl;  // timeline records of this launch (split or combine), or nullptr
+    // Q8_0 KV cache: this layer's block-scale planes [rows][hd/32] fp16 (the
+    // quants are read through the tensor maps); unused with fp16 KV.
+    const __half* ks;
+    const __half* vs;
 };
 
 // Tensor maps over the K and V arenas, each viewed as [rows][hd] fp16: 64-row
@@ -170,6 +179,23 @@ cudaError_t launch_attn_split(const AttnArgs& a, const AttnMaps& maps, int grid,
 cudaError_t launch_attn_combine(const AttnArgs& a, bool pdl, cudaStream_t s);
 int attn_split_grid(int num_sms, int hd, int group);
 cudaError_t attn_init_attributes();
+
+// ---- Q8_0 KV cache (head_dim 128) -----------------------------------------------
+// Arena rows are 128 quant bytes u = q + 128 ([rows][128] uint8) and 4 fp16
+// block scales ([rows][4]); per 32-value block d = max|x| / 127 (fp32) stored as
+// fp16, q = x / d rounded half away from zero within [-127, 127].
+bool attn_q8_supported(int hd, int group);
+cudaError_t attn_q8_init_attributes();
+cudaError_t make_attn_q8_maps(const uint8_t* kq, const uint8_t* vq, long rows, AttnMaps* out);
+cudaError_t launch_attn_split_q8(const AttnArgs& a, const AttnMaps& maps, int grid, bool pdl, cudaStream_t s);
+// The step's new rows (fp32 [B][nkv][128]) into the arenas at row0 + (slot*nkv + h)*cap + pos.
+cudaError_t launch_kvq8_append(const float* knew, const float* vnew, uint8_t* kq, __half* ks, uint8_t* vq, __half* vs,
+                               const int* slot, const int* pos, int B, int nkv, int cap, long row0, bool pdl,
+                               cudaStream_t s);
+// n_rows source rows [n_rows][128] (fp16 or fp32, device) of a [layers][nkv][len]
+// block into arena rows l * layer_rows + base + h * cap + t.
+cudaError_t launch_kvq8_rows(const void* src, bool src_fp16, long n_rows, int nkv, int len, int cap, long layer_rows,
+                             long base, uint8_t* q, __half* sc, cudaStream_t s);
 
 // Append fp32 k/v rows [B][nkv][hd] to the fp16 arenas at (slot[b], pos[b]).
 cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half* vc, const int* slot,

@@ -248,11 +248,19 @@ __device__ __forceinline__ void epi_qkv_in(const MmvqArgs& a, int g, int r, int 
             float* q = a.q_out + ((size_t)n * a.nh + head) * a.hd;
             q[dim] = y0;
             q[dim + half] = y1;
+        } else if (a.k_out) {  // Q8_0 cache: the fp32 row, quantised by the append kernel
+            float* k = a.k_out + ((size_t)n * a.nkv + (head - a.nh)) * a.hd;
+            k[dim] = y0;
+            k[dim + half] = y1;
         } else {
             __half* k = a.kc + (((size_t)in.slot * a.nkv + (head - a.nh)) * a.cap + p) * a.hd;
             k[dim] = __float2half_rn(y0);
             k[dim + half] = __float2half_rn(y1);
         }
+    } else if (a.v_out) {
+        float* vv = a.v_out + ((size_t)n * a.nkv + (head - a.nh - a.nkv)) * a.hd;
+        vv[dim] = x0;
+        vv[dim + half] = x1;
     } else {
         __half* vv = a.vc + (((size_t)in.slot * a.nkv + (head - a.nh - a.nkv)) * a.cap + p) * a.hd;
         vv[dim] = __float2half_rn(x0);

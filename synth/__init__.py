@@ -74,6 +74,8 @@ class ModelShape:
 
 
 TINY = ModelShape("tiny-1L-h256", 1, 256, 4, 2, 64, 768, 512, 10000.0, 1e-5)
+# 128-wide heads (the Q8_0 KV cache's head size), 2 layers, 4 query heads per KV head.
+TINY_HD128 = ModelShape("tiny-2L-h256-hd128", 2, 256, 4, 1, 128, 768, 512, 10000.0, 1e-5)
 LLAMA3_8B = ModelShape("llama3-8b-shaped", 32, 4096, 32, 8, 128, 14336, 128256, 500000.0, 1e-5)
 
 
@@ -213,6 +215,7 @@ def f32_normal(seed: int, name: str, shape) -> np.ndarray:
 # ---------------------------------------------------------------------------
 TINY_CASE = dict(shape=TINY, sessions=2, prefill=(17, 40), steps=4, seed=0)
 MMVQ_CASE = dict(matrices=((4096, 4096), (14336, 4096)), rows_m=(1, 2, 4, 8, 16), seed=0)
+TINY_KV_Q8_CASE = dict(shape=TINY_HD128, sessions=3, prefill=(17, 64, 70), steps=6, seed=0)
 RAGGED_ATTN_CASE = dict(n_heads=32, n_kv_heads=8, head_dim=128, sessions=8, max_ctx=32768, seed=0)
 DENSE_8B_CASE = dict(shape=LLAMA3_8B, batch=(1, 2, 4, 8, 16), prefill=1238, capacity=2048,
                      steps=128, seed=0)

@@ -67,6 +67,10 @@ def test_unsupported_model_shapes_fail_before_cuda(lib):
         cfg = kd.make_config(synth.TINY, 2, 64)
         setattr(cfg, field, 0)
         assert lib.kd_model_load(C.byref(cfg), C.byref(w), C.byref(h)) == -1
+    # the Q8_0 KV cache needs 128-wide heads and an even slot capacity
+    for shape, cap in ((synth.TINY, 64), (synth.TINY_HD128, 63)):
+        cfg = kd.make_config(shape, 2, cap, kd.KD_FLAG_KV_Q8_0)
+        assert lib.kd_model_load(C.byref(cfg), C.byref(w), C.byref(h)) == -8, (shape.name, cap)
     # a valid config with null weights is rejected on the host too
     assert lib.kd_model_load(C.byref(good), C.byref(w), C.byref(h)) == -1
     assert not h.value
@@ -106,6 +110,29 @@ def test_op_level_argument_checks(lib):
                                    pos.ctypes.data_as(i32p), 2, 32, 8, 128, 4, 64, dummy, dummy, 1 << 30,
                                    None)
     assert st == -5  # slot 0 repeated
+
+
+def test_kv_q8_argument_checks(lib):
+    i32p = C.POINTER(C.c_int32)
+    slots = np.array([0, 1], np.int32)
+    pos = np.zeros(2, np.int32)
+    d = 1 << 20
+    big = 1 << 30
+
+    def call(B=2, nh=32, nkv=8, n_slots=4, cap=64, ws=big, sl=slots, ps=pos, q=d):
+        return lib.kd_attn_append_decode_q8(q, d, d, d, d, d, d, sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p),
+                                            B, nh, nkv, n_slots, cap, d, d, ws, None)
+    assert call(B=17) == -7
+    assert call(nh=24, nkv=8) == -8        # group 3
+    assert call(nh=32, nkv=2) == -8        # group 16
+    assert call(cap=63) == -1              # odd capacity
+    assert call(ws=16) == -1               # workspace too small
+    assert call(q=d + 4) == -1             # not 16-byte aligned
+    assert call(sl=np.array([0, 0], np.int32)) == -5
+    assert call(sl=np.array([0, 4], np.int32)) == -5
+    assert call(ps=np.array([0, 64], np.int32)) == -6
+    assert lib.kd_kv_q8_quantize(None, 4, d, d, None) == -1
+    assert lib.kd_kv_q8_quantize(d, 0, d, d, None) == -1
 
 
 def test_attention_workspace_size():

@@ -45,3 +45,12 @@ def test_ragged_positions_count_each_session():
     s = synth.TINY
     pos = [0, 16, 39]
     assert bench.step_bytes(s, pos) == by_hand(s, pos)
+
+
+def test_q8_0_kv_rows():
+    # a Q8_0 head row: 128 quant bytes + 4 fp16 scales = 136 bytes (fp16: 256)
+    s = synth.LLAMA3_8B
+    assert bench.kv_bytes_per_pos(s, kv_q8=True) == 2 * 32 * 8 * 136 == 69_632
+    pos = [25704, 32767]
+    want = s.weight_bytes() + 2 * 4352 + (25705 + 32768) * 69_632 + 2 * 69_632
+    assert bench.step_bytes(s, pos, kv_q8=True) == want
