@@ -549,9 +549,11 @@ def run_op_step(args):
 def run_op_timeline(args):
     """Where the graph-replayed step's time goes: per-CTA global-timer stamps of every
     launch (kd_profile_timeline) of the 8B-shaped step at B = --batch (1238 positions),
-    summarised per kernel class over the middle layers (medians): `run` = the first
-    CTA's dependency release to the last CTA's end, `gap` = that end to the next
-    kernel's first release, `early` = the first CTA's entry to the release."""
+    or with --long the long-context case (8 sessions at 25704 + 1000 i positions, KV in
+    fp16 or with --kv-q8 in Q8_0), summarised per kernel class over the middle layers
+    (medians): `run` = the first CTA's dependency release to the last CTA's end, `gap`
+    = that end to the next kernel's first release, `early` = the first CTA's entry to
+    the release."""
     import torch
 
     import session_decode_step_gb300 as kd
@@ -559,15 +561,25 @@ def run_op_timeline(args):
     kbuild.build()
     torch.cuda.set_device(0)
     shape = synth.LLAMA3_8B
-    B = args.batch
+    if args.long:
+        c = synth.LONG_CTX_8B_CASE
+        cap, win = c["capacity"], c["steps"]
+        lens = [c["prefill_base"] + c["prefill_stagger"] * i for i in range(c["sessions"])]
+    else:
+        cap, win = CAPACITY, WINDOW
+        lens = [PREFILL] * args.batch
+    B = len(lens)
     w = synth.model_weights(shape, seed=0)
-    m = kd.kd_model_load(kd.make_config(shape, max_sessions=B, max_ctx=CAPACITY), w)
+    flags = kd.KD_FLAG_KV_Q8_0 if args.kv_q8 else 0
+    m = kd.kd_model_load(kd.make_config(shape, max_sessions=B, max_ctx=cap, flags=flags), w)
     ids = []
     for i in range(B):
-        k, v = synth.kv_prefill(shape, 0, i, PREFILL)
+        k, v = synth.kv_prefill(shape, 0, i, lens[i])
         sid = kd.kd_session_bind(m)
-        kd.kd_session_load_kv(m, sid, k, v, PREFILL)
+        kd.kd_session_load_kv(m, sid, k, v, lens[i])
+        torch.cuda.synchronize()
         ids.append(sid)
+        del k, v
     tok = synth.tokens(0, "bench", B, shape.vocab)
     am = torch.empty(B, dtype=torch.int32, device="cuda")
     st = torch.cuda.current_stream()
@@ -579,7 +591,7 @@ def run_op_timeline(args):
     stats, steps_ns = {}, []
     for i in range(max(3, args.warmup) + args.steps):
         buf.zero_()
-        kd.kd_decode_step(m, ids, tok, np.full(B, PREFILL + i % WINDOW, np.int32), None, am, st)
+        kd.kd_decode_step(m, ids, tok, np.array(lens, np.int32) + i % win, None, am, st)
         torch.cuda.synchronize()
         if i < max(3, args.warmup):
             continue
@@ -608,7 +620,8 @@ def run_op_timeline(args):
                 "early_us": round(statistics.median(v["early"]), 2), "ctas": v["ctas"]} for k, v in stats.items()}
     layer_us = sum(v["run_us"] + v["gap_us"] for k, v in summ.items()
                    if k not in ("embed", "rmsnorm_out", "lm_head", "argmax"))
-    return {"op": "timeline", "B": B, "steps": args.steps, "step_us": round(statistics.median(steps_ns) / 1e3, 1),
+    return {"op": "timeline", "B": B, "positions": f"{lens[0]}..{lens[-1] + win - 1}", "kv": "q8_0" if args.kv_q8 else "fp16",
+            "steps": args.steps, "step_us": round(statistics.median(steps_ns) / 1e3, 1),
             "launches_per_step": n_launch, "layer_us": round(layer_us, 2), "classes": summ}
 
 
@@ -686,7 +699,8 @@ def main():
     ap.add_argument("--cols", type=int, default=14336)
     ap.add_argument("--m", type=int, default=8)
     ap.add_argument("--cap", type=int, default=32768)
-    ap.add_argument("--kv-q8", action="store_true", help="--op attn / long: the Q8_0 KV cache")
+    ap.add_argument("--kv-q8", action="store_true", help="--op attn / long / timeline: the Q8_0 KV cache")
+    ap.add_argument("--long", action="store_true", help="--op timeline: the long-context case")
     args = ap.parse_args()
     if args.op:
         r = {"mmvq": run_op_mmvq, "attn": run_op_attn, "long": run_op_long, "step": run_op_step,

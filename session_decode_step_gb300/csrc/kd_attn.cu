@@ -15,6 +15,8 @@
 // softmax (max m, sum l) in between, written as (o, m, l).  A second kernel merges a session-head's
 // splits in split order (online-softmax combine).
 #include <cuda.h>
+
+#include <type_traits>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -366,23 +368,35 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
     tl_exit(a.tl);
 }
 
-// Merge a (session, head)'s splits in split order:
+// Merge a (session, head)'s splits (flash-decoding's reduction):
 //   M = max_s m_s,  out = fp16( sum_s e^{m_s - M} o_s / sum_s e^{m_s - M} l_s ).
-// Thread d owns output dimension d and splits d, d + HD, ...: the loads of the
-// splits' (m, l) and of the first COMB_BATCH splits' o[d] go out together; the
-// denominator is a fixed tree over the threads (each summing its own splits in
-// order), the numerator a sum over the splits in order.  Both orders depend on
-// the split count only.
+// NW warps.  The numerator is split into NW contiguous ranges of splits, one per
+// warp, whose lanes read whole records (HD/32 dims each, 16- or 8-byte loads)
+// and sum their range in split order, COMB_UNROLL records in flight; the first
+// COMB_UNROLL records of every range are requested before anything else, so that
+// a short session's merge waits for one round of loads.  Each thread reads the
+// (m, l) of splits t, t + 32 NW, ... into shared memory; M is a block max, the
+// weights e^{m_s - M} are formed once per split and the denominator is a fixed
+// tree (each thread summing its splits in order, then the warps' sums in warp
+// order); the warps' numerators are added in warp order.  Every order depends on
+// the session's split count and NW (fixed by the split capacity) only.
 constexpr int COMB_MAX_SPLITS = ATT_MAX_SPLITS;
-constexpr int COMB_BATCH = 32;
+constexpr int COMB_UNROLL = 8;
+// warps of the merge: 4 up to 64 splits (4096 positions) of capacity, 16 beyond
+__host__ __device__ constexpr int comb_warps(int max_splits) { return max_splits <= 64 ? 4 : 16; }
 
-template <int HD>
-__global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
+template <int HD, int NW>
+__global__ void __launch_bounds__(NW * 32) attn_combine_kernel(const AttnArgs a) {
+    constexpr int DPL = HD / 32;  // dims per lane
+    constexpr int NT = NW * 32;
+    static_assert(DPL == 2 || DPL == 4, "head_dim 64 or 128");
+    using VecT = typename std::conditional<DPL == 4, float4, float2>::type;
     __shared__ float wts[COMB_MAX_SPLITS], ls[COMB_MAX_SPLITS];
-    __shared__ float red_m[HD / 32], red_l[HD / 32];
+    __shared__ float red_m[NW], red_l[NW];
+    __shared__ __align__(16) float part[NW][HD];
     tl_entry(a.tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
-    const int b = blockIdx.y, h = blockIdx.x, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int b = blockIdx.y, h = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     // The step's positions were staged before its first kernel: read while the
     // split kernel finishes.
     const int pos_b = b < a.B ? a.pos[b] : 0;
@@ -394,16 +408,18 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     }
     const float* p = a.part + ((size_t)b * a.nh + h) * a.max_splits * ATT_REC(HD);
     // Only the session's own split records are read: records past its split count
-    // may be cold (never written), and the first round waits for its slowest load.
+    // may be cold (never written).
     const int ns = (pos_b + ATT_CHUNK) / ATT_CHUNK;
-    float o[COMB_BATCH];
+    // the warp's range of splits, and its first records
+    const int s0 = (int)(((long)ns * warp) / NW), s1 = (int)(((long)ns * (warp + 1)) / NW);
+    const float* pl = p + lane * DPL;
+    VecT o[COMB_UNROLL];
 #pragma unroll
-    for (int s = 0; s < COMB_BATCH; ++s) o[s] = s < ns ? __ldcg(p + (size_t)s * ATT_REC(HD) + d) : 0.0f;
-    const float2 ml0 = d < ns ? __ldcg(reinterpret_cast<const float2*>(p + (size_t)d * ATT_REC(HD) + HD))
-                              : make_float2(0.0f, 0.0f);
+    for (int u = 0; u < COMB_UNROLL; ++u)
+        if (s0 + u < s1) o[u] = __ldcg(reinterpret_cast<const VecT*>(pl + (size_t)(s0 + u) * ATT_REC(HD)));
     float mloc = -INFINITY;
-    for (int s = d; s < ns; s += HD) {
-        const float2 ml = s == d ? ml0 : __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
+    for (int s = t; s < ns; s += NT) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + (size_t)s * ATT_REC(HD) + HD));
         wts[s] = ml.x;
         ls[s] = ml.y;
         mloc = fmaxf(mloc, ml.x);
@@ -414,9 +430,9 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __syncthreads();
     float M = red_m[0];
 #pragma unroll
-    for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, red_m[w]);
+    for (int w = 1; w < NW; ++w) M = fmaxf(M, red_m[w]);
     float den = 0.0f;
-    for (int s = d; s < ns; s += HD) {
+    for (int s = t; s < ns; s += NT) {
         const float e = expf(__fsub_rn(wts[s], M));
         wts[s] = e;
         den = __fmaf_rn(e, ls[s], den);
@@ -427,20 +443,34 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnArgs a) {
     __syncthreads();
     float L = red_l[0];
 #pragma unroll
-    for (int w = 1; w < HD / 32; ++w) L = __fadd_rn(L, red_l[w]);
-    float num = 0.0f;
+    for (int w = 1; w < NW; ++w) L = __fadd_rn(L, red_l[w]);
+    float num[DPL];
 #pragma unroll
-    for (int s = 0; s < COMB_BATCH; ++s)
-        if (s < ns) num = __fmaf_rn(wts[s], o[s], num);
-    for (int s0 = COMB_BATCH; s0 < ns; s0 += COMB_BATCH) {
+    for (int i = 0; i < DPL; ++i) num[i] = 0.0f;
+    for (int sb = s0; sb < s1; sb += COMB_UNROLL) {
+        if (sb != s0) {
 #pragma unroll
-        for (int s = 0; s < COMB_BATCH; ++s)
-            o[s] = s0 + s < ns ? __ldcg(p + (size_t)(s0 + s) * ATT_REC(HD) + d) : 0.0f;
+            for (int u = 0; u < COMB_UNROLL; ++u)
+                if (sb + u < s1) o[u] = __ldcg(reinterpret_cast<const VecT*>(pl + (size_t)(sb + u) * ATT_REC(HD)));
+        }
 #pragma unroll
-        for (int s = 0; s < COMB_BATCH; ++s)
-            if (s0 + s < ns) num = __fmaf_rn(wts[s0 + s], o[s], num);
+        for (int u = 0; u < COMB_UNROLL; ++u)
+            if (sb + u < s1) {
+                const float e = wts[sb + u];
+                const float* ov = reinterpret_cast<const float*>(&o[u]);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) num[i] = __fmaf_rn(e, ov[i], num[i]);
+            }
     }
-    a.out[(size_t)b * a.nh * HD + (size_t)h * HD + d] = __float2half_rn(__fdiv_rn(num, L));
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) part[warp][lane * DPL + i] = num[i];
+    __syncthreads();
+    for (int d = t; d < HD; d += NT) {
+        float n = part[0][d];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) n = __fadd_rn(n, part[w][d]);
+        a.out[(size_t)b * a.nh * HD + (size_t)h * HD + d] = __float2half_rn(__fdiv_rn(n, L));
+    }
     tl_exit(a.tl);
 }
 
@@ -484,7 +514,8 @@ cudaError_t attn_init_attributes() {
         KD_ATT_DISPATCH(128, KD_SET)
     }
 #undef KD_SET
-    for (const void* f : {(const void*)attn_combine_kernel<64>, (const void*)attn_combine_kernel<128>,
+    for (const void* f : {(const void*)attn_combine_kernel<64, 4>, (const void*)attn_combine_kernel<128, 4>,
+                          (const void*)attn_combine_kernel<64, 16>, (const void*)attn_combine_kernel<128, 16>,
                           (const void*)kv_append_kernel})
         if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
@@ -572,11 +603,16 @@ cudaError_t launch_attn_combine(const AttnArgs& a, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     launch_cfg(cfg, attr, pdl);
+    const int nw = comb_warps(a.max_splits);
     cfg.gridDim = dim3(a.nh, a.B);
-    cfg.blockDim = dim3(a.hd);
+    cfg.blockDim = dim3(nw * 32);
     cfg.stream = s;
-    if (a.hd == 64) return cudaLaunchKernelEx(&cfg, attn_combine_kernel<64>, a);
-    if (a.hd == 128) return cudaLaunchKernelEx(&cfg, attn_combine_kernel<128>, a);
+    if (a.hd == 64)
+        return nw == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 4>, a)
+                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 16>, a);
+    if (a.hd == 128)
+        return nw == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 4>, a)
+                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 16>, a);
     return cudaErrorInvalidValue;
 }
 
