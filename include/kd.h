@@ -230,6 +230,17 @@ kd_status kd_decode_step_sampled(kd_model* m, const int32_t* session_ids, const 
                                  const int32_t* positions, int32_t B, const kd_sample_params* params,
                                  float* logits_out, int32_t* token_out, kd_stream stream);
 
+/* Allocation failure, for checking that a load fails closed (hf2q ADR-040:
+ * allocation overruns are refused with an error, never a crash or a half-built
+ * object).  With nth >= 1, the nth device or pinned-host allocation of the next
+ * kd_model_load fails as if memory had run out: that load returns KD_ERR_OOM
+ * with everything it had allocated freed; the switch then disarms itself.
+ * nth = 0 disarms it.  *allocs_out (nullable) receives the number of
+ * allocations the most recent kd_model_load made, so that a caller can arm each
+ * of them in turn.  No other thread may load a model while it is armed.
+ * Errors: KD_ERR_INVALID_ARG for nth < 0. */
+kd_status kd_debug_fail_alloc(int32_t nth, int32_t* allocs_out);
+
 /* Debug: when dev_buf is not NULL, later steps also write the residual stream
  * after the embedding and after every layer to dev_buf, device fp32
  * [n_layers+1][B][hidden] (steps then launch kernel by kernel).  NULL turns it off.

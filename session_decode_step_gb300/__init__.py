@@ -109,6 +109,7 @@ def lib():
             "kd_attn_append_decode_noalloc": [_vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                               i32, _vp, _vp],
             "kd_kv_q8_quantize": [_vp, C.c_int64, _vp, _vp, _vp],
+            "kd_debug_fail_alloc": [i32, i32p],
             "kd_attn_append_decode_q8": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, i32p, i32p, i32, i32, i32, i32, i32,
                                          _vp, _vp, C.c_size_t, _vp],
         }
@@ -374,6 +375,14 @@ def kd_attn_append_decode(q, k_new, v_new, k_cache, v_cache, slots, positions, n
                                        sl.ctypes.data_as(i32p), ps.ctypes.data_as(i32p), B, n_heads,
                                        n_kv_heads, head_dim, n_slots, cap, _ptr(out), _ptr(workspace),
                                        nbytes, _stream(stream)))
+
+
+def kd_debug_fail_alloc(nth: int) -> int:
+    """Arm (nth >= 1) or disarm (0) the allocation-failure switch of the next
+    kd_model_load; returns the number of allocations the last load made."""
+    out = C.c_int32()
+    _check(lib().kd_debug_fail_alloc(int(nth), C.byref(out)))
+    return out.value
 
 
 def kd_kv_q8_quantize(src, quants, scales, stream=None):

@@ -98,6 +98,22 @@ std::vector<int> tiles_qkv(int heads, int hd) {  // group = (dims 16j.., dims hd
 
 size_t q8_row_bytes(int K) { return (size_t)(K / 32) * 34; }
 
+// ---- the allocation-failure switch (kd_debug_fail_alloc) ------------------------
+// Every device or pinned-host allocation a model load makes goes through
+// load_malloc, which counts them; an armed count fails as out of memory.
+int g_fail_at = 0;          // armed for the next load: its allocation number that fails (1-based)
+int g_load_fail_at = 0;     // the current load's copy
+int g_load_count = -1;      // allocations counted in the current load (-1: no load running)
+int g_last_load_allocs = 0; // allocations the last completed load made
+
+cudaError_t load_malloc(void** p, size_t bytes, bool host = false) {
+    if (g_load_count >= 0 && ++g_load_count == g_load_fail_at) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return host ? cudaMallocHost(p, bytes) : cudaMalloc(p, bytes);
+}
+
 // Upload canonical Q8_0 parts (stacked by rows) through `staging`, then repack.
 kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, int K,
                         const std::vector<int>& tile_src, uint8_t* staging, int* d_tiles, int num_sms,
@@ -116,7 +132,7 @@ kd_status upload_packed(const std::vector<std::pair<const void*, int>>& parts, i
     out.G = (int)tile_src.size() / kd::MT;
     out.KG = K / kd::KGROUP;
     kd::plan_split(out, num_sms, force_mode);
-    KD_CK(cudaMalloc(&out.w, out.bytes()));
+    KD_CK(load_malloc((void**)&out.w, out.bytes()));
     KD_CK(cudaMemcpy(d_tiles, tile_src.data(), tile_src.size() * sizeof(int), cudaMemcpyHostToDevice));
     KD_CK(kd::launch_repack(staging, K, d_tiles, out.G, out.w, 0));
     KD_CK(cudaDeviceSynchronize());
@@ -186,7 +202,7 @@ struct kd_model {
 
     template <class T>
     cudaError_t alloc(T** p, size_t bytes) {
-        cudaError_t e = cudaMalloc((void**)p, std::max<size_t>(bytes, 16));
+        cudaError_t e = load_malloc((void**)p, std::max<size_t>(bytes, 16));
         if (e == cudaSuccess) allocs.push_back((void*)*p);
         return e;
     }
@@ -246,9 +262,9 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
                                          (size_t)H * q8_row_bytes(F), (size_t)H * q8_row_bytes(nh * hd)});
     uint8_t* staging = nullptr;
     int* d_tiles = nullptr;
-    KD_CK(cudaMalloc(&staging, stage_bytes));
+    KD_CK(load_malloc((void**)&staging, stage_bytes));
     const size_t max_tiles = std::max({(size_t)V, (size_t)2 * F, (size_t)(nh + 2 * nkv) * hd}) / kd::TILE_ROWS;
-    if (cudaMalloc(&d_tiles, max_tiles * sizeof(int)) != cudaSuccess) {
+    if (load_malloc((void**)&d_tiles, max_tiles * sizeof(int)) != cudaSuccess) {
         cudaFree(staging);
         return fail(KD_ERR_OOM, "tile map allocation failed");
     }
@@ -357,7 +373,7 @@ static kd_status load_impl(kd_model* m, const kd_weights* w) {
     KD_CK(cudaMemset(m->err, 0, sizeof(int)));
     KD_CK(m->alloc(&m->desc, DESC_INTS * sizeof(int)));
     KD_CK(cudaMemset(m->desc, 0, DESC_INTS * sizeof(int)));
-    KD_CK(cudaMallocHost(&m->pinned, (size_t)RING * DESC_INTS * sizeof(int32_t)));
+    KD_CK(load_malloc((void**)&m->pinned, (size_t)RING * DESC_INTS * sizeof(int32_t), true));
     for (auto& e : m->ring_ev) KD_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     KD_CK(cudaEventCreateWithFlags(&m->last_step, cudaEventDisableTiming));
     KD_CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
@@ -594,7 +610,12 @@ kd_status kd_model_load(const kd_config* cfg, const kd_weights* w, kd_model** ou
     if (!m) return fail(KD_ERR_OOM, "kd_model_load: host allocation failed");
     m->cfg = *cfg;
     m->kvq8 = (cfg->flags & KD_FLAG_KV_Q8_0) != 0;
+    g_load_fail_at = g_fail_at;  // an armed failure applies to this load only
+    g_fail_at = 0;
+    g_load_count = 0;
     st = load_impl(m, w);
+    g_last_load_allocs = g_load_count;
+    g_load_count = -1;
     if (st != KD_OK) {
         m->release();
         delete m;
@@ -816,6 +837,13 @@ kd_status kd_debug_layer(kd_model* m, int32_t layer, const int32_t* ids, const i
     KD_CK(e);
     KD_CK(cudaMemcpyAsync(x_out, m->x, bytes, cudaMemcpyDefault, s));
     KD_CK(cudaEventRecord(m->last_step, s));
+    return KD_OK;
+}
+
+kd_status kd_debug_fail_alloc(int32_t nth, int32_t* allocs_out) {
+    if (nth < 0) return fail(KD_ERR_INVALID_ARG, "kd_debug_fail_alloc: nth=%d", nth);
+    g_fail_at = nth;
+    if (allocs_out) *allocs_out = g_last_load_allocs;
     return KD_OK;
 }
 

@@ -112,6 +112,18 @@ def test_op_level_argument_checks(lib):
     assert st == -5  # slot 0 repeated
 
 
+def test_fail_alloc_switch_host_side(lib):
+    out = C.c_int32(-7)
+    assert lib.kd_debug_fail_alloc(-1, C.byref(out)) == -1
+    assert lib.kd_debug_fail_alloc(3, C.byref(out)) == 0 and out.value >= 0
+    # a load refused before it allocates anything leaves the switch armed; disarm it
+    cfg = kd.make_config(synth.TINY, 2, 64)
+    cfg.head_dim = 96
+    h = C.c_void_p()
+    assert lib.kd_model_load(C.byref(cfg), C.byref(kd.KdWeights()), C.byref(h)) in (-8, -1)
+    assert lib.kd_debug_fail_alloc(0, None) == 0
+
+
 def test_kv_q8_argument_checks(lib):
     i32p = C.POINTER(C.c_int32)
     slots = np.array([0, 1], np.int32)

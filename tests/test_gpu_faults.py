@@ -11,7 +11,11 @@ Checked for every kernel class with bounded waits, on both projection
 schedules: the faulted step is reported, and the next step (rewound to the same
 positions) matches the oracle before the host has cleared anything -- so a
 kernel that gave up left no state (arrival counters, ring barriers) that spoils
-later launches -- and again after the status call."""
+later launches -- and again after the status call.
+
+Also the host side of failure: a model load that runs out of memory at any one
+of its allocations (kd_debug_fail_alloc) fails closed with KD_ERR_OOM, returns
+the device memory it took, and leaves the next load and step working."""
 import numpy as np
 import pytest
 
@@ -115,3 +119,41 @@ def test_op_level_fault_words_read_clean(kdlib):
     slots, pos = np.arange(B, dtype=np.int32), np.array([0, 5], np.int32)
     kd.kd_attn_append_decode(q, kn, vn, kc, vc, slots, pos, nh, nkv, hd, B, cap, out, ws)
     assert kd.kd_attn_device_status(ws) == 0
+
+
+def test_model_load_fails_closed_at_every_allocation(kdlib, tiny):
+    kd = kdlib
+    shape, w = tiny
+    cfg = kd.make_config(shape, 2, CAP)
+    m = kd.kd_model_load(cfg, w)  # a complete load first: its kernels' modules are resident after it
+    kd.kd_model_free(m)
+    n = kd.kd_debug_fail_alloc(0)
+    assert n >= 20, n
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for k in range(1, n + 1):
+        kd.kd_debug_fail_alloc(k)
+        with pytest.raises(kd.KdError) as e:
+            kd.kd_model_load(cfg, w)
+        assert e.value.name == "KD_ERR_OOM", (k, e.value)
+        assert abs(torch.cuda.mem_get_info()[0] - free0) <= (2 << 20), k  # nothing left allocated
+    # disarmed (one-shot): the next load and a step work and match the oracle
+    m = kd.kd_model_load(cfg, w)
+    try:
+        assert kd.kd_debug_fail_alloc(0) == n
+        ids = []
+        for i, L0 in enumerate(LENS):
+            k_, v_ = synth.kv_prefill(shape, 0, i, L0)
+            sid = kd.kd_session_bind(m)
+            kd.kd_session_load_kv(m, sid, k_, v_, L0)
+            ids.append(sid)
+        torch.cuda.synchronize()
+        om = oracle.OracleModel(shape, w)
+        caches = [om.new_cache(CAP, *synth.kv_prefill(shape, 0, i, L0)) for i, L0 in enumerate(LENS)]
+        tok = synth.tokens(0, "fail-alloc", len(LENS), shape.vocab)
+        got = run_step(kd, m, ids, tok, list(LENS), shape.vocab)
+        ref, _, _ = om.step(tok, list(LENS), caches, CAP)
+        assert np.abs(got - ref).max() <= LOGIT_TOL
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
