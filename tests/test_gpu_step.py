@@ -334,3 +334,39 @@ def test_tiny_fused_epilogues_bitwise_equal_unfused_train(kdlib, tiny):
     for step, ((l0, h0), (l1, h1)) in enumerate(zip(*runs)):
         assert np.array_equal(h0, h1), step
         assert np.array_equal(l0, l1), step
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_tiny_measured_steps(kdlib, tiny, flags):
+    """kd_profile_enable: measured steps (every kernel launched from the host and
+    bracketed by two events) give the same bits as unmeasured ones, graph-replayed
+    or not, and kd_profile_read counts every launch of every class with a
+    positive device time, then resets."""
+    kd = kdlib
+    shape, w = tiny
+    cap, lens, steps = 64, [17, 40], 3
+    m = load(kd, shape, w, 4, cap, flags)
+    try:
+        ids = bind_prefilled(kd, m, shape, lens)
+        tok = synth.tokens(0, "tiny-prof", len(lens), shape.vocab)
+        ref = [gpu_step(kd, m, ids, tok, [n + s for n in lens], shape.vocab)[0] for s in range(steps)]
+        kd.kd_profile_enable(m, True)
+        kd.kd_profile_read(m)
+        got = [gpu_step(kd, m, ids, tok, [n + s for n in lens], shape.vocab)[0] for s in range(steps)]
+        prof = kd.kd_profile_read(m)
+        kd.kd_profile_enable(m, False)
+        after = gpu_step(kd, m, ids, tok, lens, shape.vocab)[0]
+        for a, b in zip(ref, got):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(after.view(np.uint32), ref[0].view(np.uint32))
+        L = shape.n_layers
+        want = {"embed": 1, "rmsnorm": 2 * L + 1, "qkv": L, "attn_split": L, "attn_combine": L, "wo": L,
+                "gate_up": L, "down": L, "lm_head": 1, "argmax": 1}
+        for k, per_step in want.items():
+            n, ms = prof[k]
+            assert n == per_step * steps, (k, n)
+            assert ms > 0.0, k
+        assert all(v == (0, 0.0) for v in kd.kd_profile_read(m).values())
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
