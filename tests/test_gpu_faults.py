@@ -84,6 +84,37 @@ def test_bounded_wait_runs_out_is_reported_and_recovered(kdlib, tiny, flags, cls
         kd.kd_model_free(m)
 
 
+# 10 sessions: every projection runs its two-tile kernel (two 8-session MMA
+# column tiles per warp), whose give-up path differs from the one-tile kernel's.
+@pytest.mark.parametrize("cls", ["qkv", "wo", "gate_up", "down", "lm_head"])
+def test_bounded_wait_runs_out_in_the_two_tile_kernels(kdlib, tiny, cls):
+    kd = kdlib
+    shape, w = tiny
+    lens = [17 + 3 * i for i in range(10)]
+    m = kd.kd_model_load(kd.make_config(shape, 12, CAP), w)
+    try:
+        ids = []
+        for i, n in enumerate(lens):
+            k, v = synth.kv_prefill(shape, 0, i, n)
+            sid = kd.kd_session_bind(m)
+            kd.kd_session_load_kv(m, sid, k, v, n)
+            ids.append(sid)
+        om = oracle.OracleModel(shape, w)
+        caches = [om.new_cache(CAP, *synth.kv_prefill(shape, 0, i, n)) for i, n in enumerate(lens)]
+        tok = synth.tokens(0, "faults-10", len(lens), shape.vocab)
+        ref, _, _ = om.step(tok, lens, caches, CAP)
+        kd.kd_debug_inject_wait_timeout(m, cls)
+        run_step(kd, m, ids, tok, lens, shape.vocab)  # the faulted step
+        got = run_step(kd, m, ids, tok, lens, shape.vocab)
+        assert np.abs(got - ref).max() <= LOGIT_TOL, (cls, float(np.abs(got - ref).max()))
+        with pytest.raises(kd.KdError) as e:
+            kd.kd_device_status(m)
+        assert e.value.name == "KD_ERR_DEVICE"
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
 def test_inject_refuses_classes_without_waits(kdlib, tiny):
     kd = kdlib
     shape, w = tiny
