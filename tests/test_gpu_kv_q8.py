@@ -204,7 +204,10 @@ def load_bound(kd, shape, w, case, cap, flags):
     return m, ids
 
 
-@pytest.mark.parametrize("flags", [0, 1])
+# 0: schedules as chosen; 1: direct launches instead of the graph; 2 / 4: every
+# projection forced onto the stream / group schedule (both write the fp32 k, v rows
+# the append quantises).
+@pytest.mark.parametrize("flags", [0, 1, 2, 4])
 def test_tiny_kv_q8_teacher_forced_against_oracle(kdlib, tiny128, flags):
     kd = kdlib
     shape, w, case = tiny128
@@ -264,6 +267,103 @@ def test_tiny_kv_q8_batch_invariance(kdlib, tiny128):
             t1, l1 = stream([i])
             assert np.array_equal(t1[:, 0], toks[:, i]), i
             assert np.array_equal(l1[:, 0], lgs[:, i]), i
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
+def greedy_streams(kd, m, ids, starts, tok0, steps, V, params=None):
+    B = len(ids)
+    tok = np.array(tok0, np.int32)
+    toks, lgs = [], []
+    lg = torch.empty(B, V, device="cuda", dtype=torch.float32)
+    am = torch.empty(B, device="cuda", dtype=torch.int32)
+    for s_ in range(steps):
+        pos = [p + s_ for p in starts]
+        if params is None:
+            kd.kd_decode_step(m, ids, tok, pos, lg, am)
+        else:
+            sp = kd.sample_params([p["temperature"] for p in params], [p["seed"] for p in params], [s_] * B)
+            kd.kd_decode_step_sampled(m, ids, tok, pos, sp, lg, am)
+        tok = am.cpu().numpy()
+        toks.append(tok.copy())
+        lgs.append(lg.cpu().numpy().view(np.uint32).copy())
+    return np.array(toks), np.array(lgs)
+
+
+def test_tiny_kv_q8_fused_bitwise_equal_unfused_train(kdlib, tiny128):
+    """The q|k|v epilogue's fp32 k, v rows and the append kernel: the fused step
+    and the unfused train (plain projections, epilogues as kernels of their own)
+    give the same logits, through later steps' attention over the appended rows."""
+    kd = kdlib
+    shape, w, case = tiny128
+    lens = list(case["prefill"])
+    runs = []
+    for flags in (0, kd.KD_FLAG_UNFUSED):
+        m, ids = load_bound(kd, shape, w, case, 128, flags)
+        try:
+            runs.append(greedy_streams(kd, m, ids, lens, synth.tokens(0, "q8-unfused", len(lens), shape.vocab),
+                                       case["steps"], shape.vocab))
+            assert kd.kd_device_status(m) == 0
+        finally:
+            kd.kd_model_free(m)
+    assert np.array_equal(runs[0][0], runs[1][0])
+    assert np.array_equal(runs[0][1], runs[1][1])
+
+
+def test_tiny_kv_q8_many_sessions_and_sampling(kdlib, tiny128):
+    """20 sessions (groups of 16 and 4 rows) with the Q8_0 cache, greedy and
+    sampled: every session's tokens and logit bits equal its run alone."""
+    kd = kdlib
+    shape, w, case = tiny128
+    n = 20
+    lens = [5 + 5 * i for i in range(n)]
+    m = kd.kd_model_load(kd.make_config(shape, n, 128, kd.KD_FLAG_KV_Q8_0), w)
+    try:
+        ids = []
+        for i, L0 in enumerate(lens):
+            k, v = synth.kv_prefill(shape, case["seed"], 100 + i, L0)
+            sid = kd.kd_session_bind(m)
+            kd.kd_session_load_kv(m, sid, k, v, L0)
+            ids.append(sid)
+        torch.cuda.synchronize()
+        tok0 = synth.tokens(0, "q8-many", n, shape.vocab)
+        params = [dict(temperature=0.7 + 0.1 * (i % 4), seed=1000 + i) for i in range(n)]
+        for p in (None, params):
+            toks, lgs = greedy_streams(kd, m, ids, lens, tok0, 3, shape.vocab, p)
+            for i in (0, 7, 15, 16, 19):
+                t1, l1 = greedy_streams(kd, m, [ids[i]], [lens[i]], tok0[i:i + 1], 3, shape.vocab,
+                                        None if p is None else p[i:i + 1])
+                assert np.array_equal(t1[:, 0], toks[:, i]), (p is None, i)
+                assert np.array_equal(l1[:, 0], lgs[:, i]), (p is None, i)
+        assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
+def test_tiny_kv_q8_attention_wait_runs_out_and_recovers(kdlib, tiny128):
+    """One bounded wait of the Q8_0 attention kernel made to run out: the step
+    reports KD_ERR_DEVICE, and the next step (rewound) matches the oracle."""
+    kd = kdlib
+    shape, w, case = tiny128
+    cap = 128
+    lens = list(case["prefill"])
+    m, ids = load_bound(kd, shape, w, case, cap, 0)
+    try:
+        om = oracle.OracleModel(shape, w, kv_q8_0=True)
+        caches = [om.new_cache(cap, *synth.kv_prefill(shape, case["seed"], i, L0)) for i, L0 in enumerate(lens)]
+        tok = synth.tokens(case["seed"], "q8-fault", len(lens), shape.vocab)
+        ref, _, _ = om.step(tok, lens, caches, cap)
+        lg = torch.empty(len(ids), shape.vocab, device="cuda", dtype=torch.float32)
+        kd.kd_debug_inject_wait_timeout(m, "attn_split")
+        kd.kd_decode_step(m, ids, tok, lens, lg, None)
+        torch.cuda.synchronize()
+        kd.kd_decode_step(m, ids, tok, lens, lg, None)
+        torch.cuda.synchronize()
+        assert float(np.abs(lg.cpu().numpy() - ref).max()) <= LOGIT_TOL
+        with pytest.raises(kd.KdError) as e:
+            kd.kd_device_status(m)
+        assert e.value.name == "KD_ERR_DEVICE"
         assert kd.kd_device_status(m) == 0
     finally:
         kd.kd_model_free(m)
