@@ -382,8 +382,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
 // the session's split count and NW (fixed by the split capacity) only.
 constexpr int COMB_MAX_SPLITS = ATT_MAX_SPLITS;
 constexpr int COMB_UNROLL = 8;
-// warps of the merge: 4 up to 64 splits (4096 positions) of capacity, 16 beyond
-__host__ __device__ constexpr int comb_warps(int max_splits) { return max_splits <= 64 ? 4 : 16; }
+// warps of the merge: 4 up to 64 splits (4096 positions) of capacity, 32 beyond
+__host__ __device__ constexpr int comb_warps(int max_splits) { return max_splits <= 64 ? 4 : 32; }
 
 template <int HD, int NW>
 __global__ void __launch_bounds__(NW * 32) attn_combine_kernel(const AttnArgs a) {
@@ -515,7 +515,7 @@ cudaError_t attn_init_attributes() {
     }
 #undef KD_SET
     for (const void* f : {(const void*)attn_combine_kernel<64, 4>, (const void*)attn_combine_kernel<128, 4>,
-                          (const void*)attn_combine_kernel<64, 16>, (const void*)attn_combine_kernel<128, 16>,
+                          (const void*)attn_combine_kernel<64, 32>, (const void*)attn_combine_kernel<128, 32>,
                           (const void*)kv_append_kernel})
         if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
@@ -609,10 +609,10 @@ cudaError_t launch_attn_combine(const AttnArgs& a, bool pdl, cudaStream_t s) {
     cfg.stream = s;
     if (a.hd == 64)
         return nw == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 4>, a)
-                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 16>, a);
+                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<64, 32>, a);
     if (a.hd == 128)
         return nw == 4 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 4>, a)
-                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 16>, a);
+                       : cudaLaunchKernelEx(&cfg, attn_combine_kernel<128, 32>, a);
     return cudaErrorInvalidValue;
 }
 
