@@ -14,11 +14,13 @@
 namespace kd {
 
 constexpr int EMBED_THREADS = 256;
+constexpr int EMBED_COLS = 1024;  // columns per CTA: 4 per thread, their loads issued together
 
 // x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), and the
 // per-group sums of squares ssq[g][b] of the row, as a residual writer leaves
-// them for the next RMSNorm: warp w holds elements 256u + 32w + lane, i.e.
-// group 8u + w with lane = row, added by the same shuffle tree.
+// them for the next RMSNorm.  Block (c, b) covers columns [1024c, 1024c + 1024)
+// of row b: warp w holds elements 1024c + 256u + 32w + lane, i.e. group
+// 32c + 8u + w with lane = row, added by the residual writers' shuffle tree.
 __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __restrict__ emb,
                                                               const int* __restrict__ token, int H,
                                                               float* __restrict__ x, float* __restrict__ ssq,
@@ -27,11 +29,12 @@ __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __r
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(tl);
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float* xr = x + (size_t)b * H;
     const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
-    constexpr int U = 16;  // elements per thread whose loads are issued together
-    for (int i0 = 0; i0 < H; i0 += EMBED_THREADS * U) {
+    constexpr int U = EMBED_COLS / EMBED_THREADS;
+    {
+        const int i0 = blockIdx.x * EMBED_COLS;
         int8_t q[U];
         unsigned short dbits[U];
 #pragma unroll
@@ -270,7 +273,7 @@ cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
-    cfg.gridDim = dim3(B);
+    cfg.gridDim = dim3((H + EMBED_COLS - 1) / EMBED_COLS, B);
     cfg.blockDim = dim3(EMBED_THREADS);
     cfg.stream = s;
     return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, ssq, tl);
