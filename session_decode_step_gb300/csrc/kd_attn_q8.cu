@@ -8,8 +8,9 @@
 // (memra appends quantised K/V in `decode_batch_layers` phase A; hf2q ADR-040
 // measures against llama.cpp's q8_0 K/V).
 //
-// The attention keeps the fp16 kernel's work items, ring, bounded waits and
-// combine (kd_attn.cu); only the tiles and the two products differ:
+// The attention keeps the fp16 kernel's work items, bounded waits and merge
+// (kd_attn.cu), with separate rings for the K and the V parts of the items; the
+// tiles and the two products differ:
 //   scores Sᵀ = K Qᵀ per 32-dim block: the quants, read with ldmatrix as pairs
 //   of bytes and converted to fp16 exactly, are the A operand of the block's two
 //   m16n8k16 MMAs, whose k index runs over the block's dims in the fixed order
@@ -37,18 +38,22 @@ struct AttnQ8Smem {
     static constexpr int TILE = AT_C * QROW;             // 8 KB of quants per tile
     static constexpr int SROW = NBLK * 2;                // 8 bytes of scales per row
     static constexpr int STILE = AT_C * SROW;            // 512 B of scales per tile
-    static constexpr int KQ = 0, VQ = TILE, KS = 2 * TILE, VS = 2 * TILE + STILE;
-    static constexpr int STAGE = 2 * TILE + 2 * STILE;   // 17 KB
+    // Separate rings for the items' K parts (SK slots) and V parts (SV slots): a V
+    // part is re-issued only when its slot's previous item has finished its value
+    // phase, so V needs the deeper ring (K 8 / V 18 measured best of the 26 slots'
+    // splits; 13 / 13 was 1.4% slower on the long-context step, 6 / 20 2.4%).
+    static constexpr int SK = 8, SV = 18;
+    static constexpr int KQ_OFF = 0, VQ_OFF = SK * TILE, KS_OFF = (SK + SV) * TILE, VS_OFF = KS_OFF + SK * STILE;
     // Consumer warps per CTA (one CTA per SM): as many as the kernel's registers
     // allow without spilling -- 16 (128 registers a lane) for a group of 4, 12 for
     // groups of 1 and 2, 8 for a group of 8.
     static constexpr __host__ __device__ int warps(int group) { return group == 8 ? 8 : group == 4 ? 16 : 12; }
     // as many 17 KB stages as the opt-in shared memory holds (with barriers, item words, slack)
-    static constexpr int STAGES = (227 * 1024 - 1024 - 16) / (2 * TILE + 2 * STILE + 2 * 8 + 2 * 4);
-    static constexpr int BAR_OFF = STAGES * STAGE;
-    static constexpr int ITEM_OFF = BAR_OFF + 2 * STAGES * 8;
-    static constexpr int TOTAL = ITEM_OFF + 2 * STAGES * 4 + 16 + 1024;
-    static_assert(STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static constexpr int BAR_OFF = VS_OFF + SV * STILE;
+    static constexpr int ITEM_OFF = BAR_OFF + (SK + SV) * 8;
+    static constexpr int TOTAL = ITEM_OFF + (SK + SV) * 4 + 16 + 1024;
+    static_assert(TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(TOTAL <= 227 * 1024, "opt-in shared memory");
     // quants: row r's 16-byte chunk c at chunk c ^ (r & 7) (128-byte swizzle)
     static __device__ __forceinline__ uint32_t qoff(int row, int chunk) {
         return (uint32_t)(row * QROW + ((chunk ^ (row & 7)) << 4));
@@ -92,7 +97,7 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
                          const __grid_constant__ CUtensorMap tmk8, const __grid_constant__ CUtensorMap tmv,
                          const __grid_constant__ CUtensorMap tmv8) {
     using L = AttnQ8Smem;
-    constexpr int S = L::STAGES;
+    constexpr int SK = L::SK, SV = L::SV, SMAX = SK > SV ? SK : SV;
     constexpr int HD = L::HD;
     constexpr int NU = HD / 8;  // 8-dim output tiles of P V
     constexpr int W = L::warps(GQ);
@@ -104,10 +109,10 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
     const int g = lane >> 2, c = lane & 3;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     volatile int* stage_item = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
-    volatile int* cta_failed = stage_item + 2 * S;
+    volatile int* cta_failed = stage_item + SK + SV;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2 * S; ++i) {
+        for (int i = 0; i < SK + SV; ++i) {
             mbar_init(&bar[i], 1);
             stage_item[i] = -1;
         }
@@ -122,14 +127,12 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
     const int n_items = tab.n_items;
     const int nk = (int)blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto gitem = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
-    // Issue the copies of the CTA's item k into stage k % S (lane 0): its K part
-    // (parts & 1: quants and scales) and/or its V part (parts & 2), each on its
-    // own barrier.  Quants by tensor map (64-row box, or 8-row boxes for a ragged
+    // Issue the copies of the CTA's item k (lane 0): its K part (parts & 1: quants
+    // and scales) into K slot k % SK and/or its V part (parts & 2) into V slot
+    // k % SV, each on its slot's barrier.  Quants by tensor map (64-row box, or 8-row boxes for a ragged
     // tail); scales by one bulk copy (8 bytes a row, rounded up to 16).
     const uint64_t kv_policy = l2_policy_evict_first();
     auto issue = [&](const AttnItem& it, int k, int parts) {
-        const int st = k % S;
-        uint8_t* stg = smem + st * L::STAGE;
         const long row = a.row0 + ((long)it.slot * a.nkv + it.kvh) * a.cap + (long)it.s * AT_C;
         const bool full = it.n == AT_C;
         const int qrows = full ? AT_C : (it.n + 7) / 8 * 8;
@@ -137,18 +140,20 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             if (!((parts >> part) & 1)) continue;
-            uint64_t* b = &bar[part * S + st];
+            const int st = part ? k % SV : k % SK;
+            uint64_t* b = &bar[part * SK + st];
             const CUtensorMap* tm = part ? &tmv : &tmk;
             const CUtensorMap* tm8 = part ? &tmv8 : &tmk8;
             const __half* sc = part ? a.vs : a.ks;
-            stage_item[part * S + st] = k;
+            stage_item[part * SK + st] = k;
             mbar_arrive_expect_tx(b, (uint32_t)(qrows * L::QROW) + sbytes);
-            uint8_t* dq = stg + (part ? L::VQ : L::KQ);
+            uint8_t* dq = smem + (part ? L::VQ_OFF : L::KQ_OFF) + st * L::TILE;
             if (full)
                 tma_load_2d_hint(dq, tm, 0, (int)row, b, kv_policy);
             else
                 for (int k8 = 0; k8 < qrows; k8 += 8) tma_load_2d_hint(dq + k8 * L::QROW, tm8, 0, (int)row + k8, b, kv_policy);
-            bulk_g2s_hint(stg + (part ? L::VS : L::KS), sc + row * L::NBLK, sbytes, b, kv_policy);
+            bulk_g2s_hint(smem + (part ? L::VS_OFF : L::KS_OFF) + st * L::STILE, sc + row * L::NBLK, sbytes, b,
+                          kv_policy);
         }
     };
 
@@ -160,20 +165,21 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
     }
     // History items (not holding this step's new row) are fetched before the wait.
     unsigned early = 0;
-    for (int i = 0, k = warp; k < S && k < nk; ++i, k += W) {
+    auto first_parts = [&](int k) { return (k < SK ? 1 : 0) | (k < SV ? 2 : 0); };
+    for (int i = 0, k = warp; k < SMAX && k < nk; ++i, k += W) {
         const AttnItem it = tab.item(a, lane, gitem(k));
         if (it.s != it.ns - 1) {
-            if (lane == 0) issue(it, k, 3);
+            if (lane == 0) issue(it, k, first_parts(k));
             early |= 1u << i;
         }
     }
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(a.tl);
-    for (int i = 0, k = warp; k < S && k < nk; ++i, k += W)
+    for (int i = 0, k = warp; k < SMAX && k < nk; ++i, k += W)
         if (!((early >> i) & 1u)) {
             const AttnItem it = tab.item(a, lane, gitem(k));
-            if (lane == 0) issue(it, k, 3);
+            if (lane == 0) issue(it, k, first_parts(k));
         }
 
     // MMA columns as in the fp16 kernel: column 2h + part of N-tile j is head 4j + h,
@@ -224,16 +230,14 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
 
     for (int k = warp; k < nk; k += W) {
         const AttnItem it = it_next;
-        const int st = k % S;
-        uint8_t* stg = smem + st * L::STAGE;
-        const uint32_t kq = smem_u32(stg + L::KQ);
-        const uint8_t* kscale = stg + L::KS;
-        const uint32_t vq = smem_u32(stg + L::VQ);
-        const uint8_t* vscale = stg + L::VS;
+        const int kst = k % SK, vst = k % SV;
+        const uint32_t kq = smem_u32(smem + L::KQ_OFF + kst * L::TILE);
+        const uint8_t* kscale = smem + L::KS_OFF + kst * L::STILE;
+        const uint32_t vq = smem_u32(smem + L::VQ_OFF + vst * L::TILE);
+        const uint8_t* vscale = smem + L::VS_OFF + vst * L::STILE;
 
-        const uint32_t par = (uint32_t)(k / S) & 1u;
-        bool ok = wait_value(stage_item + st, k);
-        ok = ok && mbar_wait_bounded(&bar[st], par);  // the K part
+        bool ok = wait_value(stage_item + kst, k);
+        ok = ok && mbar_wait_bounded(&bar[kst], (uint32_t)(k / SK) & 1u);  // the K part
         if (__any_sync(FULL_MASK, !ok)) {
             if (lane == 0) {
                 atomicOr(a.err, ERR_WAIT_TIMEOUT);
@@ -242,9 +246,6 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
             break;
         }
         const int n = it.n;
-        const bool refill = k + S < nk;
-        AttnItem nx{};
-        if (refill) nx = tab.item(a, lane, gitem(k + S));
 
         // ---- scores: per 16-key tile m and 32-dim block, two MMAs, then the keys' block scales
         float sacc[AT_KT][NQ][4];
@@ -284,9 +285,12 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
         }
         // The K part is read: refill it with item k + S's.
         __syncwarp();
-        if (refill && lane == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(nx, k + S, 1);
+        if (k + SK < nk) {
+            const AttnItem nx = tab.item(a, lane, gitem(k + SK));
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(nx, k + SK, 1);
+            }
         }
         if (k + W < nk) {
             it_next = tab.item(a, lane, gitem(k + W));
@@ -323,8 +327,8 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
         }
 
         // The V part.
-        ok = wait_value(stage_item + S + st, k);
-        ok = ok && mbar_wait_bounded(&bar[S + st], par);
+        ok = wait_value(stage_item + SK + vst, k);
+        ok = ok && mbar_wait_bounded(&bar[SK + vst], (uint32_t)(k / SV) & 1u);
         if (__any_sync(FULL_MASK, !ok)) {
             if (lane == 0) {
                 atomicOr(a.err, ERR_WAIT_TIMEOUT);
@@ -435,18 +439,21 @@ __global__ void __launch_bounds__(AttnQ8Smem::warps(GQ) * 32, 1)
             }
         }
         __syncwarp();  // the V part is read: refill it
-        if (refill && lane == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(nx, k + S, 2);
+        if (k + SV < nk) {
+            const AttnItem nx = tab.item(a, lane, gitem(k + SV));
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(nx, k + SV, 2);
+            }
         }
     }
     // After a wait gave up, copies may still be in flight: before the CTA's shared
     // memory is released, wait (bounded) for the last item issued into each part.
     __syncthreads();
     if (threadIdx.x == 0 && *cta_failed)
-        for (int i = 0; i < 2 * S; ++i) {
+        for (int i = 0; i < SK + SV; ++i) {
             const int k = stage_item[i];
-            if (k >= 0) (void)mbar_wait_bounded(&bar[i], (uint32_t)(k / S) & 1u);
+            if (k >= 0) (void)mbar_wait_bounded(&bar[i], (uint32_t)(k / (i < SK ? SK : SV)) & 1u);
         }
     tl_exit(a.tl);
 }
