@@ -587,7 +587,13 @@ def run_op_timeline(args):
     buf = torch.zeros(nmax, kd.KD_TIMELINE_CTAS, 4, dtype=torch.int64, device="cuda")
     classes = kd.kd_profile_timeline(m, buf, nmax)
     n_launch = sum(c is not None for c in classes)
-    per_layer = (n_launch - 4) // shape.n_layers  # embed, then layers, then output norm, lm_head, argmax
+    # embed, the layers (layer 0's attention norm is formed by the embedding
+    # kernel), the output norm, lm_head (and argmax, unless lm_head made the pick)
+    qkv_at = [j for j in range(n_launch) if classes[j] == "qkv"]
+    head_at = classes.index("lm_head")
+    tail = [(0, "embed"), (head_at - 1, "rmsnorm_out"), (head_at, "lm_head")]
+    if head_at + 1 < n_launch:
+        tail.append((head_at + 1, "argmax"))
     stats, steps_ns = {}, []
     for i in range(max(3, args.warmup) + args.steps):
         buf.zero_()
@@ -601,7 +607,7 @@ def run_op_timeline(args):
             r = t[j][t[j][:, 0] > 0]
             rows.append((int(r[:, 0].min()), int(r[:, 1].min()), int(r[:, 2].max()), len(r)))
         steps_ns.append(rows[-1][2] - rows[0][0])
-        for j in range(1 + 2 * per_layer, 1 + (shape.n_layers - 2) * per_layer):
+        for j in range(qkv_at[2] - 1, qkv_at[shape.n_layers - 2] - 1):  # layers 2 .. L - 3, from their norm
             name = classes[j]
             if name == "rmsnorm":
                 name += "_ffn" if classes[j + 1] == "gate_up" else "_attn"
@@ -609,7 +615,7 @@ def run_op_timeline(args):
             d["run"].append((rows[j][2] - rows[j][1]) / 1e3)
             d["gap"].append((rows[j + 1][1] - rows[j][2]) / 1e3)
             d["early"].append((rows[j][1] - rows[j][0]) / 1e3)
-        for j, name in ((0, "embed"), (n_launch - 3, "rmsnorm_out"), (n_launch - 2, "lm_head"), (n_launch - 1, "argmax")):
+        for j, name in tail:
             d = stats.setdefault(name, {"run": [], "gap": [], "early": [], "ctas": rows[j][3]})
             d["run"].append((rows[j][2] - rows[j][1]) / 1e3)
             d["gap"].append((rows[j + 1][1] - rows[j][2]) / 1e3 if j + 1 < n_launch else 0.0)

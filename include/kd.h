@@ -58,7 +58,8 @@ typedef void* kd_stream;          /* cudaStream_t */
 typedef struct kd_model kd_model; /* opaque, library-owned */
 
 /* Model shape.  Requirements (else KD_ERR_UNSUPPORTED): hidden, ffn and
- * n_heads*head_dim are multiples of 128; head_dim is 64 or 128; n_heads is
+ * n_heads*head_dim are multiples of 128; hidden is at most 131072 (the
+ * embedding kernel stages a whole row on chip); head_dim is 64 or 128; n_heads is
  * 1, 2, 4 or 8 times n_kv_heads; vocab is a multiple of 32; max_ctx is at
  * most 65536.  All sizes and max_sessions, max_ctx are >= 1 (else
  * KD_ERR_INVALID_ARG).

@@ -235,11 +235,12 @@ static kd_status check_config(const kd_config* c) {
                     c->head_dim, c->ffn, c->vocab, c->max_sessions, c->max_ctx);
     if (!(c->rms_eps >= 0.0f) || !(c->rope_theta > 0.0f))
         return fail(KD_ERR_INVALID_ARG, "kd_config: rms_eps must be >= 0 and rope_theta > 0");
-    if (c->hidden % 128 || c->ffn % 128 || c->vocab % 32 || (c->n_heads * c->head_dim) % 128 ||
-        c->n_heads % c->n_kv_heads || !kd::attn_supported(c->head_dim, c->n_heads / c->n_kv_heads))
+    if (c->hidden % 128 || c->hidden > 131072 || c->ffn % 128 || c->vocab % 32 ||
+        (c->n_heads * c->head_dim) % 128 || c->n_heads % c->n_kv_heads ||
+        !kd::attn_supported(c->head_dim, c->n_heads / c->n_kv_heads))
         return fail(KD_ERR_UNSUPPORTED,
-                    "kd_config: need hidden, ffn, n_heads*head_dim multiples of 128, vocab a multiple "
-                    "of 32, head_dim in {64,128}, n_heads/n_kv_heads in {1,2,4,8}");
+                    "kd_config: need hidden, ffn, n_heads*head_dim multiples of 128, hidden <= 131072, vocab "
+                    "a multiple of 32, head_dim in {64,128}, n_heads/n_kv_heads in {1,2,4,8}");
     if ((c->flags & KD_FLAG_KV_Q8_0) && (!kd::attn_q8_supported(c->head_dim, c->n_heads / c->n_kv_heads) ||
                                          c->max_ctx % 2))
         return fail(KD_ERR_UNSUPPORTED, "kd_config: the Q8_0 KV cache needs head_dim 128 and an even max_ctx");
@@ -390,6 +391,16 @@ static bool fused_norm(const kd_model* m, const PackedQ8& p) {
            p.KG <= kd::MMVQ_WARPS * kd::NORM_IN_MAX_KG;
 }
 
+// The embedding kernel forms layer 0's attention-norm input itself (unless the
+// unfused train runs, or q|k|v forms its normed input in its own load).
+static bool embed_norm(const kd_model* m) {
+    return !(m->cfg.flags & KD_FLAG_UNFUSED) && !fused_norm(m, m->qkv[0]);
+}
+// The lm_head launch makes each row's pick itself (stream schedule, fused train).
+static bool head_pick(const kd_model* m) {
+    return !(m->cfg.flags & KD_FLAG_UNFUSED) && m->head.mode == kd::MMVQ_STREAM;
+}
+
 // The launch train of one step; `lg` receives the logits, `am` (nullable) the argmax.
 // With only_layer >= 0: that layer alone, on residual rows already in m->x and
 // their per-group sums of squares in m->ssq; no embedding, no head.
@@ -486,8 +497,10 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     };
     const int l0 = only_layer >= 0 ? only_layer : 0, l1 = only_layer >= 0 ? only_layer + 1 : L;
     const bool whole = only_layer < 0;
+    const bool en = whole && embed_norm(m);
     if (whole)
-        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->ssq, pdl, s, tl_next()));
+        KD_RUN(KD_K_EMBED, kd::launch_embed(m->tok_embd, tok, B, H, m->x, m->ssq, en ? m->norms : nullptr,
+                                            c.rms_eps, m->xn, pdl, s, tl_next()));
     if (whole && m->hidden_dbg &&
         (e = cudaMemcpyAsync(m->hidden_dbg + (size_t)hrow0 * H, m->x, (size_t)B * H * 4, cudaMemcpyDeviceToDevice,
                              s)) != cudaSuccess)
@@ -497,7 +510,7 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
         __half* vc = m->vc + (size_t)l * m->layer_kv;
         const float* attn_w = m->norms + (size_t)(2 * l) * H;
         const bool fq = fused_norm(m, m->qkv[l]);
-        if (!fq) KD_RUN(KD_K_RMSNORM, norm(attn_w));
+        if (!fq && !(en && l == 0)) KD_RUN(KD_K_RMSNORM, norm(attn_w));
         kd::MmvqArgs a = mm(m->qkv[l], m->xn);
         if (fq) norm_in(a, attn_w);
         a.q_out = m->q; a.kc = kc; a.vc = vc; a.slot = slot; a.pos = pos; a.rope = m->rope;
@@ -554,11 +567,20 @@ static cudaError_t enqueue_step(kd_model* m, int B, float* lg, int* am, cudaStre
     a.y = lg; a.ld = V;
     a.inject_tx = inject(KD_K_LM_HEAD);
     a.tl = tl_next();
-    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->map_xn, m->head.mode, kd::EPI_STORE, m->num_sms, pdl, s));
-    if (am)
+    const int* samp = sampled ? m->desc + 3 * KD_MAX_BATCH : nullptr;
+    const bool pick = am && head_pick(m);
+    if (pick) {
+        a.pick_keys = m->amax_keys;
+        a.pick_done = reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH);
+        a.pick_out = am;
+        a.samp = samp;
+    }
+    KD_RUN(KD_K_LM_HEAD, kd::launch_mmvq(a, m->map_xn, m->head.mode, pick ? kd::EPI_PICK : kd::EPI_STORE,
+                                         m->num_sms, pdl, s));
+    if (am && !pick)
         KD_RUN(KD_K_ARGMAX, kd::launch_argmax(lg, B, V, am, m->amax_keys,
                                               reinterpret_cast<unsigned*>(m->amax_keys + KD_MAX_BATCH), pdl, s,
-                                              tl_next(), sampled ? m->desc + 3 * KD_MAX_BATCH : nullptr));
+                                              tl_next(), samp));
 #undef KD_RUN
     return cudaSuccess;
 }
@@ -869,14 +891,14 @@ kd_status kd_profile_timeline(kd_model* m, uint64_t* dev_buf, int32_t max_launch
         std::vector<int32_t> cls;
         cls.push_back(KD_K_EMBED);
         for (int l = 0; l < L; ++l) {
-            if (!fused_norm(m, m->qkv[l])) cls.push_back(KD_K_RMSNORM);
+            if (!fused_norm(m, m->qkv[l]) && !(l == 0 && embed_norm(m))) cls.push_back(KD_K_RMSNORM);
             for (int k : {KD_K_QKV, KD_K_ATTN_SPLIT, KD_K_ATTN_COMBINE, KD_K_WO}) cls.push_back(k);
             if (!fused_norm(m, m->gu[l])) cls.push_back(KD_K_RMSNORM);
             for (int k : {KD_K_GATE_UP, KD_K_DOWN}) cls.push_back(k);
         }
         cls.push_back(KD_K_RMSNORM);
         cls.push_back(KD_K_LM_HEAD);
-        cls.push_back(KD_K_ARGMAX);
+        if (!head_pick(m)) cls.push_back(KD_K_ARGMAX);
         for (int i = 0; i < max_launches; ++i) classes_out[i] = i < (int)cls.size() ? cls[i] : -1;
     }
     return KD_OK;

@@ -187,7 +187,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 // ---- RMSNorm from per-group sums of squares -----------------------------------
 // r = 1 / sqrt(sum_g ssq[g][b] / H + eps) for the H/32 groups a residual writer
-// left: lane l adds groups l, l + 32, ... in order (the first add is exact),
+// left: lane l adds groups l, l + 32, ... in order (the first add is exact;
+// the loads are issued four at a time),
 // then a fixed shuffle tree; every lane returns the same value.  The RMSNorm
 // kernel (rms_factor_from_ssq) and the fused activation load
 // (rms_factor_from_parts, with the lane's values loaded ahead: groups
@@ -209,13 +210,98 @@ __device__ __forceinline__ void rms_parts_load(const float* ssq, int b, int lane
         pre[i] = lane + 32 * i < ng ? __ldcg(ssq + (size_t)(lane + 32 * i) * MAX_NORM_SLOTS + b) : 0.0f;
 }
 
-__device__ __forceinline__ float rms_factor_from_ssq(const float* ssq, int b, int lane, int H, float eps) {
+// The sums read through `get(g)`: from global memory (the norm kernel) or from
+// the shared-memory copy the embedding kernel keeps of the sums it wrote.
+template <class Get>
+__device__ __forceinline__ float rms_factor_of(Get get, int lane, int H, float eps) {
     const int ng = H / 32;
     float s = 0.0f;
-    for (int g = lane; g < ng; g += 32) s = __fadd_rn(s, __ldcg(ssq + (size_t)g * MAX_NORM_SLOTS + b));
+    constexpr int PRE = 4;  // loads issued together, then added in order
+    for (int g0 = lane; g0 < ng; g0 += 32 * PRE) {
+        float pre[PRE];
+#pragma unroll
+        for (int i = 0; i < PRE; ++i) pre[i] = g0 + 32 * i < ng ? get(g0 + 32 * i) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < PRE; ++i)
+            if (g0 + 32 * i < ng) s = __fadd_rn(s, pre[i]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));
+}
+__device__ __forceinline__ float rms_factor_from_ssq(const float* ssq, int b, int lane, int H, float eps) {
+    return rms_factor_of([&](int g) { return __ldcg(ssq + (size_t)g * MAX_NORM_SLOTS + b); }, lane, H, eps);
+}
+
+// Device-scope atomic add with acquire-release semantics: the writes this CTA
+// ordered before it (through a barrier) are visible to a CTA that reads the
+// counter afterwards, and that CTA's later accesses see every write released
+// into the counter before.
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// ---- the pick: greedy argmax and Gumbel-max sampling ---------------------------
+// Each (value, index) maps to a 64-bit key whose unsigned order is the pick
+// order -- larger value first, then lower index; -0 counts as +0; NaN maps to 0
+// and never wins -- so partial picks merge with a maximum, in any order, with
+// one result.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
+    if (v != v) return 0ull;
+    if (v == 0.0f) v = 0.0f;
+    const unsigned u = __float_as_uint(v);
+    const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(~(unsigned)i);
+}
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 64 x 64
+// -> 128 multiplies mixing the four counter words with the key, the key bumped
+// by the two Weyl constants between rounds.  Returns the block's four words.
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
+                                              uint64_t k1, uint64_t (&w)[4]) {
+    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0, hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    w[0] = c0; w[1] = c1; w[2] = c2; w[3] = c3;
+}
+
+// logit / T - log(-log u), u = (top 24 bits of w + 1/2) / 2^24 (exact, in (0, 1)).
+__device__ __forceinline__ float gumbel_perturb(float logit, float T, uint64_t w) {
+    const float u = __fmul_rn(__fadd_rn((float)(unsigned)(w >> 40), 0.5f), 0x1p-24f);
+    const float g = -logf(-logf(u));
+    return __fadd_rn(__fdiv_rn(logit, T), g);
+}
+
+// A row's sampling parameters in the staged descriptor block `samp`: the
+// temperature's bits at [b], the seed at [16 + 2b] (low word first), the
+// counter at [48 + 2b]; T <= 0 picks greedily.  Entry v of the row is perturbed
+// by word v mod 4 of the Philox block at counter (v / 4, counter, 0, 0) under
+// key (seed, 0).
+struct PickParams {
+    float T;
+    uint64_t seed, ctr;
+};
+__device__ __forceinline__ PickParams pick_params(const int* samp, int b) {
+    PickParams p{0.0f, 0, 0};
+    if (!samp) return p;
+    p.T = __int_as_float(samp[b]);
+    p.seed = ((uint64_t)(unsigned)samp[17 + 2 * b] << 32) | (unsigned)samp[16 + 2 * b];
+    p.ctr = ((uint64_t)(unsigned)samp[49 + 2 * b] << 32) | (unsigned)samp[48 + 2 * b];
+    return p;
 }
 
 // ---- exact int8 -> fp16 ----------------------------------------------------

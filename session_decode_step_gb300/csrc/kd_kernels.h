@@ -38,6 +38,7 @@ enum Epilogue : int {
     EPI_RESID = 1,   // x[n][row] += v (fp32 residual stream)
     EPI_SWIGLU = 2,  // act[n][i] = fp16(silu(gate_i) * up_i)
     EPI_QKV = 3,     // RoPE q and k at each row's position, q to fp32, k/v appended as fp16
+    EPI_PICK = 4,    // EPI_STORE, and the rows' pick from the stored values (stream schedule only)
 };
 
 // Timeline records (kd_profile_timeline): per launch [TL_CTAS][TL_WORDS] u64.
@@ -127,6 +128,12 @@ struct MmvqArgs {
     // of writing fp16 rows into kc / vc.
     float* k_out;
     float* v_out;
+    // EPI_PICK: each row's pick (launch_argmax's result, from the stored values)
+    // fused into the store; keys, done and samp as launch_argmax takes them.
+    unsigned long long* pick_keys;
+    unsigned* pick_done;
+    int* pick_out;
+    const int* samp;
 };
 
 // xmap: make_x_map of a.x with at least B rows.
@@ -203,9 +210,12 @@ cudaError_t launch_kv_append(const float* k, const float* v, __half* kc, __half*
 
 // ---- row ops -----------------------------------------------------------------
 // x[b][:] = dequant(tok_embd[token[b]])  (canonical Q8_0 rows) and, as a residual
-// writer leaves them, the per-group sums of squares ssq[g][b] of those rows
-cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq, bool pdl,
-                         cudaStream_t s, unsigned long long* tl = nullptr);
+// writer leaves them, the per-group sums of squares ssq[g][b] of those rows;
+// with w (nullable), also xn[b][:] = the RMSNorm of x[b] with weight w, bit for
+// bit what launch_norm_from_ssq would then form
+cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq,
+                         const float* w, float eps, __half* xn, bool pdl, cudaStream_t s,
+                         unsigned long long* tl = nullptr);
 // ssq[g][b] = sum of x[b][32g .. 32g+31]^2 for rows supplied from outside, in
 // the residual writers' group layout and summation order
 cudaError_t launch_ssq_rows(const float* x, int B, int H, float* ssq, cudaStream_t s);

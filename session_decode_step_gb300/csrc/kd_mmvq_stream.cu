@@ -18,9 +18,60 @@ namespace kd {
 
 __device__ __forceinline__ int stage_owner(long t, long T, long W) { return (int)(((t + 1) * W - 1) / T); }
 
+// EPI_PICK state of a lane: for each of its two session columns per tile, the
+// best pick key so far.
+template <int NT>
+struct PickLane {
+    unsigned long long best[NT][2];
+};
+
+// The Gumbel words of this lane's four rows (gq + 8k, k < 4) of row group g in
+// column (nt, j) -- entry e takes word e mod 4 of Philox block e / 4.  The four
+// lanes gq = 4h + t (t < 4) of one cq need blocks 8g + 2k + h, k < 4, and word t
+// of each: lane t computes block k = t, and four shuffle rounds transpose the
+// words (in round s lane t reads block (t + s) mod 4 from the lane that made it,
+// which sends its word (k - s) mod 4).  Every lane takes part.
+__device__ __forceinline__ void pick_words(const PickParams& p, int g, int gq, int lane, uint64_t (&out)[4]) {
+    const int t = gq & 3, h = gq >> 2;
+    uint64_t w[4];
+    philox4x64_10((uint64_t)(8 * g + 2 * t + h), p.ctr, 0, 0, p.seed, 0, w);
+#pragma unroll
+    for (int sft = 0; sft < 4; ++sft) {
+        const int q = (t - sft) & 3;  // the word this lane sends in this round
+        const uint64_t send = q == 0 ? w[0] : q == 1 ? w[1] : q == 2 ? w[2] : w[3];
+        const int k = (t + sft) & 3;  // the block this lane receives
+        const int src = ((h * 4 + k) << 2) | (lane & 3);
+        const uint64_t got = __shfl_sync(FULL_MASK, send, src);
+        if (k == 0) out[0] = got;
+        else if (k == 1) out[1] = got;
+        else if (k == 2) out[2] = got;
+        else out[3] = got;
+    }
+}
+
 // Epilogue over this lane's fragment of a finished row group.
 template <int NT, int EPI>
-__device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, int cq, float (&v)[MT][NT][4]) {
+__device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, int cq, float (&v)[MT][NT][4],
+                                              PickLane<NT>& pk) {
+    if constexpr (EPI == EPI_PICK) {
+        // keys of the lane's entries: rows gq + 8k (k = 2 mt + (i >> 1)) of columns (nt, i & 1)
+        const int lane = (gq << 2) | cq;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const PickParams p = pick_params(a.samp, nt * 8 + col_session(2 * cq + j));
+                uint64_t gw[4] = {0, 0, 0, 0};
+                if (a.samp) pick_words(p, g, gq, lane, gw);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int row = gq + 8 * k;
+                    float x = v[k >> 1][nt][((k & 1) << 1) | j];
+                    if (p.T > 0.0f) x = gumbel_perturb(x, p.T, gw[k]);
+                    pk.best[nt][j] = max(pk.best[nt][j], argmax_key(x, g * GROUP_ROWS + row));
+                }
+            }
+    }
     float ss[NT][2];  // RESID: this lane's share of sum(x_new^2) per column
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) ss[nt][0] = ss[nt][1] = 0.0f;
@@ -31,7 +82,7 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
             const int n = nt * 8 + col_session(2 * cq + (i & 1));
             if (n >= a.B) continue;
             const int r = gq + ((i >> 1) << 3);  // row within a 16-row tile
-            if constexpr (EPI == EPI_STORE) {
+            if constexpr (EPI == EPI_STORE || EPI == EPI_PICK) {
                 epi_store(a, g, r, n, v[0][nt][i]);
                 epi_store(a, g, r + TILE_ROWS, n, v[1][nt][i]);
             } else if constexpr (EPI == EPI_RESID) {
@@ -57,6 +108,45 @@ __device__ __forceinline__ void frag_epilogue(const MmvqArgs& a, int g, int gq, 
                 const int n = nt * 8 + col_session(2 * cq + j);
                 if (gq == 0 && n < a.B) a.ssq_out[(size_t)g * NORM_SLOTS + n] = s;
             }
+    }
+}
+
+// The end of an EPI_PICK launch: a session's best key over the CTA's lanes
+// (the 8 row lanes, then the warps) goes into pick_keys with one atomic
+// maximum; the last CTA to arrive turns the keys into indices (-1 if nothing
+// but NaN) and leaves the keys and the counter zero for the next launch --
+// launch_argmax's merge, over keys made from the same stored values.
+template <int NT>
+__device__ __forceinline__ void pick_finish(const MmvqArgs& a, PickLane<NT>& pk, int warp, int lane) {
+    __shared__ unsigned long long tab[MMVQ_WARPS][16];
+    __shared__ bool last;
+    const int gq = lane >> 2, cq = lane & 3, tid = threadIdx.x;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            unsigned long long k = pk.best[nt][j];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) k = max(k, __shfl_xor_sync(FULL_MASK, k, o));
+            if (gq == 0) tab[warp][nt * 8 + col_session(2 * cq + j)] = k;
+        }
+    __syncthreads();
+    if (warp == 0) {  // B <= 16: the merging threads are lanes of warp 0
+        if (lane < a.B) {
+            unsigned long long k = tab[0][lane];
+#pragma unroll
+            for (int w = 1; w < MMVQ_WARPS; ++w) k = max(k, tab[w][lane]);
+            if (k) atomicMax(&a.pick_keys[lane], k);
+        }
+        __threadfence();  // the warp's maxima are visible before its arrival
+        __syncwarp();
+        if (lane == 0) last = atomic_add_acq_rel(a.pick_done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (last && tid < a.B) {  // after the acquiring arrival: every CTA's maxima are in
+        const unsigned long long k = atomicExch(&a.pick_keys[tid], 0ull);
+        a.pick_out[tid] = k ? (int)(~(unsigned)(k & 0xffffffffull)) : -1;
+        if (tid == 0) *a.pick_done = 0u;
     }
 }
 
@@ -114,6 +204,14 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(a.tl);
+
+    PickLane<NT> pk;
+    if constexpr (EPI == EPI_PICK) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) pk.best[nt][j] = 0ull;
+    }
 
     int g = (int)(s_begin / a.KG), kg = (int)(s_begin - (long)g * a.KG);
     int xkg = kg;  // k-group of the next stage whose activations are requested (lane 0)
@@ -176,7 +274,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
         const long gfirst = (long)g * a.KG;
         const int w0 = stage_owner(gfirst, T, a.W), w1 = stage_owner(gfirst + a.KG - 1, T, a.W);
         if (w0 == w1) {
-            frag_epilogue<NT, EPI>(a, g, gq, cq, acc);  // the whole group was this warp's
+            frag_epilogue<NT, EPI>(a, g, gq, cq, acc, pk);  // the whole group was this warp's
         } else {
             const int ncontrib = w1 - w0 + 1;
             float* pt = a.part + ((size_t)g * a.maxc + (w - w0)) * (GROUP_ROWS * 16);
@@ -236,7 +334,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
                             }
                     }
                 }
-                frag_epilogue<NT, EPI>(a, g, gq, cq, v);
+                frag_epilogue<NT, EPI>(a, g, gq, cq, v, pk);
                 if (lane == 0) a.cnt[g] = 0;  // ready for the next launch
             }
         }
@@ -249,6 +347,7 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
         ++g;
         kg = 0;
     }
+    if constexpr (EPI == EPI_PICK) pick_finish<NT>(a, pk, warp, lane);
     tl_exit(a.tl);
 }
 
@@ -276,7 +375,8 @@ static cudaError_t stream_launch(const MmvqArgs& a, const CUtensorMap& xm, bool 
     return cudaLaunchKernelEx(&cfg, mmvq_stream_kernel<NT, EPI>, a, xm);
 }
 
-#define KD_STREAM_CASES(X, NT_) X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID)
+#define KD_STREAM_CASES(X, NT_) \
+    X(NT_, EPI_STORE) X(NT_, EPI_SWIGLU) X(NT_, EPI_QKV) X(NT_, EPI_RESID) X(NT_, EPI_PICK)
 
 cudaError_t mmvq_stream_init_attributes() {
     cudaError_t e;

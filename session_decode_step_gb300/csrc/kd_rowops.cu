@@ -13,50 +13,94 @@
 
 namespace kd {
 
-constexpr int EMBED_THREADS = 256;
-constexpr int EMBED_COLS = 1024;  // columns per CTA: 4 per thread, their loads issued together
+constexpr int EMBED_THREADS = 1024;
+constexpr int EMBED_U = 4;  // columns per thread and pass (4096 per pass)
 
-// x[b][i] = q * d of the token's canonical Q8_0 row (exact in fp32), and the
+// x[b] = q * d of the token's canonical Q8_0 row (exact in fp32), and the
 // per-group sums of squares ssq[g][b] of the row, as a residual writer leaves
-// them for the next RMSNorm.  Block (c, b) covers columns [1024c, 1024c + 1024)
-// of row b: warp w holds elements 1024c + 256u + 32w + lane, i.e. group
-// 32c + 8u + w with lane = row, added by the residual writers' shuffle tree.
+// them for the next RMSNorm.  With w: also the first RMSNorm of the row,
+// xn[b] = fp16(x * r_b * w), r_b formed from those sums in the RMSNorm kernel's
+// order and roundings (the same bits as the norm kernel run after this one).
+// Block b covers row b.  The row's bytes are first copied to shared memory in
+// 8-byte words (a row is 136 (H / 128) bytes, so 8-byte aligned); in pass p warp
+// w then holds elements 4096p + 1024u + 32w + lane, i.e. group 128p + 32u + w
+// with lane = row, added by the residual writers' shuffle tree.
 __global__ void __launch_bounds__(EMBED_THREADS) embed_kernel(const uint8_t* __restrict__ emb,
                                                               const int* __restrict__ token, int H,
                                                               float* __restrict__ x, float* __restrict__ ssq,
-                                                              unsigned long long* tl) {
+                                                              const float* __restrict__ w, float eps,
+                                                              __half* __restrict__ xn, unsigned long long* tl) {
+    extern __shared__ uint2 rowsh[];  // [H / 32 * 34 / 8] the row's bytes, then [H / 32] the group sums
+    __shared__ float rsh;
     tl_entry(tl);
     pdl_launch_dependents();  // dependents may become resident now; they still wait for this grid
     pdl_wait();
     tl_waited(tl);
-    const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = H / 32 * 34 / 8;  // 8-byte words of the row
+    float* gsq = reinterpret_cast<float*>(rowsh + nw);
     float* xr = x + (size_t)b * H;
-    const uint8_t* row = emb + (size_t)token[b] * (H / 32) * 34;
-    constexpr int U = EMBED_COLS / EMBED_THREADS;
     {
-        const int i0 = blockIdx.x * EMBED_COLS;
-        int8_t q[U];
-        unsigned short dbits[U];
+        const uint2* src = reinterpret_cast<const uint2*>(emb + (size_t)token[b] * (H / 32) * 34);
+        for (int i = tid; i < nw; i += EMBED_THREADS) rowsh[i] = __ldcs(src + i);
+    }
+    float w0[EMBED_U];  // the first pass's norm weights, loaded while the row arrives
+    if (w) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + tid + EMBED_THREADS * u;
-            const uint8_t* blk = row + (i >> 5) * 34;
-            q[u] = i < H ? (int8_t)blk[2 + (i & 31)] : (int8_t)0;
-            dbits[u] = i < H ? (unsigned short)(blk[0] | (blk[1] << 8)) : (unsigned short)0;
+        for (int u = 0; u < EMBED_U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            w0[u] = i < H ? w[i] : 0.0f;
         }
+    }
+    __syncthreads();
+    const uint8_t* row = reinterpret_cast<const uint8_t*>(rowsh);
+    auto elem = [&](int i) {
+        const uint8_t* blk = row + (i >> 5) * 34;
+        const __half_raw hr{(unsigned short)(blk[0] | (blk[1] << 8))};
+        return __fmul_rn((float)(int8_t)blk[2 + (i & 31)], __half2float(__half(hr)));
+    };
+    constexpr int PASS = EMBED_THREADS * EMBED_U;
+    float v0[EMBED_U];  // the first pass, kept for the norm
+    for (int p0 = 0; p0 < H; p0 += PASS) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + tid + EMBED_THREADS * u;
-            if (i0 + EMBED_THREADS * u + 32 * warp < H) {  // the warp's 32 elements: one whole group
-                const __half_raw hr{dbits[u]};
-                const float v = __fmul_rn((float)q[u], __half2float(__half(hr)));
+        for (int u = 0; u < EMBED_U; ++u) {
+            const int i = p0 + tid + EMBED_THREADS * u;
+            if (p0 + EMBED_THREADS * u + 32 * warp < H) {  // the warp's 32 elements: one whole group
+                const float v = elem(i);
+                if (p0 == 0) v0[u] = v;
                 xr[i] = v;
                 float s = __fmul_rn(v, v);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
-                if (lane == 0) ssq[(size_t)(i >> 5) * MAX_NORM_SLOTS + b] = s;
+                if (lane == 0) {
+                    ssq[(size_t)(i >> 5) * MAX_NORM_SLOTS + b] = s;
+                    gsq[i >> 5] = s;
+                }
+            } else if (p0 == 0) {
+                v0[u] = 0.0f;
             }
         }
+    }
+    if (w) {
+        __syncthreads();  // every group sum is in gsq
+        if (warp == 0) {
+            const float r = rms_factor_of([&](int g) { return gsq[g]; }, lane, H, eps);
+            if (lane == 0) rsh = r;
+        }
+        __syncthreads();
+        const float r = rsh;
+        __half* o = xn + (size_t)b * H;
+#pragma unroll
+        for (int u = 0; u < EMBED_U; ++u) {
+            const int i = tid + EMBED_THREADS * u;
+            if (i < H) o[i] = __float2half_rn(__fmul_rn(__fmul_rn(v0[u], r), w0[u]));
+        }
+        for (int p0 = PASS; p0 < H; p0 += PASS)
+#pragma unroll
+            for (int u = 0; u < EMBED_U; ++u) {
+                const int i = p0 + tid + EMBED_THREADS * u;
+                if (i < H) o[i] = __float2half_rn(__fmul_rn(__fmul_rn(elem(i), r), w[i]));
+            }
     }
     tl_exit(tl);
 }
@@ -143,44 +187,6 @@ cudaError_t launch_norm_from_ssq(const float* x, const float* ssq, int B, int H,
 constexpr int ARGMAX_THREADS = 256;
 constexpr int ARGMAX_CHUNK = ARGMAX_THREADS * 8;  // logits per CTA: two float4 per thread
 
-__device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
-    if (v != v) return 0ull;
-    if (v == 0.0f) v = 0.0f;
-    const unsigned u = __float_as_uint(v);
-    const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)ord << 32) | (unsigned long long)(~(unsigned)i);
-}
-
-// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 64 x 64
-// -> 128 multiplies mixing the four counter words with the key, the key bumped
-// by the two Weyl constants between rounds.  Returns the block's four words.
-__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
-                                              uint64_t k1, uint64_t (&w)[4]) {
-    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k0 += W0;
-            k1 += W1;
-        }
-        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0, hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
-        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
-    }
-    w[0] = c0; w[1] = c1; w[2] = c2; w[3] = c3;
-}
-
-// logit / T - log(-log u), u = (top 24 bits of w + 1/2) / 2^24 (exact, in (0, 1)).
-__device__ __forceinline__ float gumbel_perturb(float logit, float T, uint64_t w) {
-    const float u = __fmul_rn(__fadd_rn((float)(unsigned)(w >> 40), 0.5f), 0x1p-24f);
-    const float g = -logf(-logf(u));
-    return __fadd_rn(__fdiv_rn(logit, T), g);
-}
-
 __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __restrict__ logits, int V,
                                                                 unsigned long long* keys, unsigned* done,
                                                                 int* __restrict__ out, unsigned long long* tl,
@@ -203,20 +209,18 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_kernel(const float* __r
     // Temperature sampling: the row's entries get their Gumbel perturbation
     // (entry v: word v mod 4 of the Philox block at counter (v / 4, counter, 0, 0)
     // under key (seed, 0)); the pick is then the same argmax.
-    const float T = samp ? __int_as_float(samp[b]) : 0.0f;
-    if (T > 0.0f) {
-        const uint64_t seed = ((uint64_t)(unsigned)samp[17 + 2 * b] << 32) | (unsigned)samp[16 + 2 * b];
-        const uint64_t ctr = ((uint64_t)(unsigned)samp[49 + 2 * b] << 32) | (unsigned)samp[48 + 2 * b];
+    const PickParams pp = pick_params(samp, b);
+    if (pp.T > 0.0f) {  // one Philox block serves the four entries of a float4
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = i0 + h * ARGMAX_THREADS * 4;
             if (i < V) {
                 uint64_t w[4];
-                philox4x64_10((uint64_t)(i >> 2), ctr, 0, 0, seed, 0, w);
-                v[h].x = gumbel_perturb(v[h].x, T, w[0]);
-                v[h].y = gumbel_perturb(v[h].y, T, w[1]);
-                v[h].z = gumbel_perturb(v[h].z, T, w[2]);
-                v[h].w = gumbel_perturb(v[h].w, T, w[3]);
+                philox4x64_10((uint64_t)(i >> 2), pp.ctr, 0, 0, pp.seed, 0, w);
+                v[h].x = gumbel_perturb(v[h].x, pp.T, w[0]);
+                v[h].y = gumbel_perturb(v[h].y, pp.T, w[1]);
+                v[h].z = gumbel_perturb(v[h].z, pp.T, w[2]);
+                v[h].w = gumbel_perturb(v[h].w, pp.T, w[3]);
             }
         }
     }
@@ -258,7 +262,8 @@ cudaError_t rowops_init_attributes() {
                                              cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    // the embedding stages a whole row (and its group sums) in shared memory
+    return cudaFuncSetAttribute(embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
 }
 
 static void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pdl) {
@@ -268,15 +273,16 @@ static void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, bool pd
     cfg.numAttrs = pdl ? 1 : 0;
 }
 
-cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq, bool pdl,
-                         cudaStream_t s, unsigned long long* tl) {
+cudaError_t launch_embed(const uint8_t* tok_embd, const int* token, int B, int H, float* x, float* ssq,
+                         const float* w, float eps, __half* xn, bool pdl, cudaStream_t s, unsigned long long* tl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_attr(cfg, attr, pdl);
-    cfg.gridDim = dim3((H + EMBED_COLS - 1) / EMBED_COLS, B);
+    cfg.gridDim = dim3(B);
     cfg.blockDim = dim3(EMBED_THREADS);
+    cfg.dynamicSmemBytes = (size_t)(H / 32) * 34 + (size_t)(H / 32) * sizeof(float);  // the row, its group sums
     cfg.stream = s;
-    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, ssq, tl);
+    return cudaLaunchKernelEx(&cfg, embed_kernel, tok_embd, token, H, x, ssq, w, eps, xn, tl);
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int* out, unsigned long long* keys, unsigned* done,

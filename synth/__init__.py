@@ -76,6 +76,10 @@ class ModelShape:
 TINY = ModelShape("tiny-1L-h256", 1, 256, 4, 2, 64, 768, 512, 10000.0, 1e-5)
 # 128-wide heads (the Q8_0 KV cache's head size), 2 layers, 4 query heads per KV head.
 TINY_HD128 = ModelShape("tiny-2L-h256-hd128", 2, 256, 4, 1, 128, 768, 512, 10000.0, 1e-5)
+# A vocabulary of 32000 (1000 row groups of the lm_head, which no whole number of
+# groups per SM covers evenly), so the head runs on the stream schedule, as at
+# the 8B shape, while the rest of the model stays tiny.
+TINY_WIDE_VOCAB = ModelShape("tiny-1L-h256-v32000", 1, 256, 4, 2, 64, 768, 32000, 10000.0, 1e-5)
 LLAMA3_8B = ModelShape("llama3-8b-shaped", 32, 4096, 32, 8, 128, 14336, 128256, 500000.0, 1e-5)
 
 

@@ -57,8 +57,8 @@ def test_unsupported_model_shapes_fail_before_cuda(lib):
     good = kd.make_config(synth.TINY, 2, 64)
     w = kd.KdWeights()
     h = C.c_void_p()
-    for field, value in [("hidden", 200), ("head_dim", 96), ("n_kv_heads", 3), ("ffn", 100),
-                         ("vocab", 500)]:
+    for field, value in [("hidden", 200), ("hidden", 131072 + 128), ("head_dim", 96), ("n_kv_heads", 3),
+                         ("ffn", 100), ("vocab", 500)]:
         cfg = kd.make_config(synth.TINY, 2, 64)
         setattr(cfg, field, value)
         st = lib.kd_model_load(C.byref(cfg), C.byref(w), C.byref(h))

@@ -11,8 +11,10 @@ the oracle's input to that layer (the layer's attention norm goes through the
 step's own sums-of-squares RMSNorm kernel, its FFN norm through the residual
 writer's sums); one B = 8 step end to end: logits within 5e-2 and hidden states
 within the end-to-end bound for 4 sessions; and the fused step bit-identical to
-the unfused train (every epilogue as a kernel of its own; the RMSNorm folded
-into the projections' activation load) over two B = 8 steps."""
+the unfused train (every epilogue as a kernel of its own, the first norm after
+the embedding and the pick after the lm_head; the RMSNorm folded into the
+projections' activation load) over two B = 8 steps, logits, hidden states and
+picked tokens."""
 import numpy as np
 import pytest
 
@@ -126,8 +128,9 @@ def test_8b_fused_step_bitwise_equal_unfused_and_folded_norm(model_norms):
         try:
             for step in range(2):
                 kd.kd_decode_step(model, ids, tok, [PREFILL + step] * B, lg, am)
-                out.append((lg.cpu().numpy().view(np.uint32).copy(), hid.cpu().numpy().view(np.uint32).copy()))
                 tok = am.cpu().numpy()
+                out.append((lg.cpu().numpy().view(np.uint32).copy(), hid.cpu().numpy().view(np.uint32).copy(),
+                            tok.copy()))
         finally:
             kd.kd_debug_capture_hidden(model, None)
             for sid in ids:
@@ -142,6 +145,7 @@ def test_8b_fused_step_bitwise_equal_unfused_and_folded_norm(model_norms):
             assert kd.kd_device_status(other) == 0
         finally:
             kd.kd_model_free(other)
-        for step, ((l0, h0), (l1, h1)) in enumerate(zip(ref, got)):
+        for step, ((l0, h0, t0), (l1, h1, t1)) in enumerate(zip(ref, got)):
             assert np.array_equal(h0, h1), (flags, step)
             assert np.array_equal(l0, l1), (flags, step)
+            assert np.array_equal(t0, t1), (flags, step)  # the pick fused into lm_head vs the pick kernel

@@ -305,7 +305,8 @@ def test_tiny_fused_epilogues_bitwise_equal_unfused_train(kdlib, tiny):
     """Each fusion of the step against its unfused sequence, bit for bit: RoPE and
     the KV append in the q|k|v epilogue, SwiGLU in the gate|up epilogue, the
     residual add and the next norm's sums of squares in the o-proj and down
-    epilogues (KD_FLAG_UNFUSED runs them as kernels of their own after plain
+    epilogues, and layer 0's attention norm in the embedding kernel
+    (KD_FLAG_UNFUSED runs them as kernels of their own after plain
     projections, with the group schedule's summation order).  Logits, every
     hidden state and the appended cache rows (through later steps' attention),
     several steps, seeded norm weights."""
@@ -360,7 +361,9 @@ def test_tiny_measured_steps(kdlib, tiny, flags):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
         assert np.array_equal(after.view(np.uint32), ref[0].view(np.uint32))
         L = shape.n_layers
-        want = {"embed": 1, "rmsnorm": 2 * L + 1, "qkv": L, "attn_split": L, "attn_combine": L, "wo": L,
+        # the embedding kernel forms layer 0's attention norm (2L norm launches:
+        # L - 1 attention norms, L FFN norms, the output norm)
+        want = {"embed": 1, "rmsnorm": 2 * L, "qkv": L, "attn_split": L, "attn_combine": L, "wo": L,
                 "gate_up": L, "down": L, "lm_head": 1, "argmax": 1}
         for k, per_step in want.items():
             n, ms = prof[k]
