@@ -187,8 +187,7 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 // ---- RMSNorm from per-group sums of squares -----------------------------------
 // r = 1 / sqrt(sum_g ssq[g][b] / H + eps) for the H/32 groups a residual writer
-// left: lane l adds groups l, l + 32, ... in order (the first add is exact;
-// the loads are issued four at a time),
+// left: lane l adds groups l, l + 32, ... in order (the first add is exact),
 // then a fixed shuffle tree; every lane returns the same value.  The RMSNorm
 // kernel (rms_factor_from_ssq) and the fused activation load
 // (rms_factor_from_parts, with the lane's values loaded ahead: groups
@@ -216,15 +215,7 @@ template <class Get>
 __device__ __forceinline__ float rms_factor_of(Get get, int lane, int H, float eps) {
     const int ng = H / 32;
     float s = 0.0f;
-    constexpr int PRE = 4;  // loads issued together, then added in order
-    for (int g0 = lane; g0 < ng; g0 += 32 * PRE) {
-        float pre[PRE];
-#pragma unroll
-        for (int i = 0; i < PRE; ++i) pre[i] = g0 + 32 * i < ng ? get(g0 + 32 * i) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < PRE; ++i)
-            if (g0 + 32 * i < ng) s = __fadd_rn(s, pre[i]);
-    }
+    for (int g = lane; g < ng; g += 32) s = __fadd_rn(s, get(g));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL_MASK, s, o));
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)H), eps)));

@@ -30,8 +30,9 @@ struct PickLane {
 // lanes gq = 4h + t (t < 4) of one cq need blocks 8g + 2k + h, k < 4, and word t
 // of each: lane t computes block k = t, and four shuffle rounds transpose the
 // words (in round s lane t reads block (t + s) mod 4 from the lane that made it,
-// which sends its word (k - s) mod 4).  Every lane takes part.
-__device__ __forceinline__ void pick_words(const PickParams& p, int g, int gq, int lane, uint64_t (&out)[4]) {
+// which sends its word (k - s) mod 4).  Every lane takes part.  Out of line:
+// only sampled steps call it, and its code stays out of the streaming loop.
+__device__ __noinline__ void pick_words(const PickParams& p, int g, int gq, int lane, uint64_t (&out)[4]) {
     const int t = gq & 3, h = gq >> 2;
     uint64_t w[4];
     philox4x64_10((uint64_t)(8 * g + 2 * t + h), p.ctr, 0, 0, p.seed, 0, w);
@@ -273,8 +274,18 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
         // ---- this warp's part of row group g is done ----
         const long gfirst = (long)g * a.KG;
         const int w0 = stage_owner(gfirst, T, a.W), w1 = stage_owner(gfirst + a.KG - 1, T, a.W);
+        // The group's finished values: the warp's own (the whole group was its),
+        // or, for the last of several contributors, the sum of their partials.
+        float v[MT][NT][4];
+        bool finish = false;
         if (w0 == w1) {
-            frag_epilogue<NT, EPI>(a, g, gq, cq, acc, pk);  // the whole group was this warp's
+            finish = true;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) v[mt][nt][i2] = acc[mt][nt][i2];
         } else {
             const int ncontrib = w1 - w0 + 1;
             float* pt = a.part + ((size_t)g * a.maxc + (w - w0)) * (GROUP_ROWS * 16);
@@ -296,7 +307,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
                 // Sum the slots in contributor order; loads are issued CH slots at a
                 // time so their latencies overlap.
                 constexpr int CH = NT == 1 ? 4 : 4;
-                float v[MT][NT][4];
                 const float* p0 = a.part + (size_t)g * a.maxc * (GROUP_ROWS * 16);
                 for (int s0 = 0; s0 < ncontrib; s0 += CH) {
                     float2 lo[CH][MT][NT], hi[CH][MT][NT];
@@ -334,10 +344,11 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, 1)
                             }
                     }
                 }
-                frag_epilogue<NT, EPI>(a, g, gq, cq, v, pk);
+                finish = true;
                 if (lane == 0) a.cnt[g] = 0;  // ready for the next launch
             }
         }
+        if (finish) frag_epilogue<NT, EPI>(a, g, gq, cq, v, pk);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
