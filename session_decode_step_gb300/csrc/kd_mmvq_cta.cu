@@ -13,9 +13,11 @@
 
 namespace kd {
 
-// PAIR: a launch with one CTA per group for SMs < G <= 2 * SMs (B <= 8): a
-// shallower ring and the partial buffer laid over it let two CTAs share an SM,
-// so no CTA waits for a second group while others idle.
+// PAIR: a launch of two CTAs per SM for G > SMs (B <= 8): one CTA per group up
+// to 2 * SMs groups, else 2 * SMs CTAs taking groups c, c + grid, ...  A
+// shallower ring lets two CTAs share an SM: twice the warps to hide the stage
+// pipeline's latency, and for G <= 2 * SMs no CTA waits for a second group
+// while others idle.
 // NIN: the RMSNorm fused into the activation load (MmvqArgs::nx): each warp
 // forms its whole k-range of normed tiles once, after the dependency wait, and
 // keeps them for all its groups; the ring then carries weights only.
@@ -33,10 +35,9 @@ struct CtaSmem {
     static constexpr size_t RING_BYTES = (size_t)MMVQ_WARPS * RD * STAGE_BYTES;
     static constexpr size_t BAR_OFF = W_OFF + RING_BYTES;
     static constexpr size_t RED_BYTES = (size_t)MMVQ_WARPS * GROUP_ROWS * RS * sizeof(float);
-    static constexpr size_t RED_OFF = PAIR ? W_OFF : BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
-    static constexpr size_t TOTAL =
-        (PAIR ? BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t) : RED_OFF + RED_BYTES) + 1024;  // + alignment slack
-    static_assert(!PAIR || RED_BYTES <= RING_BYTES, "the partial buffer lies over the ring");
+    static constexpr size_t RED_OFF = BAR_OFF + MMVQ_WARPS * RD * sizeof(uint64_t);
+    static constexpr size_t TOTAL = RED_OFF + RED_BYTES + 1024;  // + alignment slack
+    static_assert(!PAIR || 2 * (TOTAL + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 template <int NT, int EPI, bool PAIR, bool NIN>
@@ -149,7 +150,6 @@ __global__ void __launch_bounds__(MMVQ_WARPS * 32, NT == 1 && !NIN ? 2 : 1)
             if (++slot == RD) { slot = 0; phase ^= 1u; }
         }
         // ---- the group's partials meet in shared memory (every warp takes part) ----
-        if constexpr (PAIR) __syncthreads();  // every warp is done with the ring the partials lie over
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -245,8 +245,9 @@ cudaError_t mmvq_cta_init_attributes() {
 // one-tile kernel is used (two CTAs fit an SM); otherwise min(G, SMs) CTAs that
 // each take groups c, c + grid, ...
 int mmvq_cta_grid(int G, int B, int num_sms, bool fused_norm, bool* pair) {
-    *pair = !fused_norm && B <= 8 && G > num_sms && G <= 2 * num_sms;
-    return *pair ? G : (G < num_sms ? G : num_sms);
+    *pair = !fused_norm && B <= 8 && G > num_sms;
+    if (*pair) return G < 2 * num_sms ? G : 2 * num_sms;
+    return G < num_sms ? G : num_sms;
 }
 
 cudaError_t launch_mmvq_cta(const MmvqArgs& a, const CUtensorMap& xm, int epi, int num_sms, bool pdl, cudaStream_t s) {
