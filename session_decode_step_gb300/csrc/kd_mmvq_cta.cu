@@ -241,11 +241,13 @@ cudaError_t mmvq_cta_init_attributes() {
     return cudaSuccess;
 }
 
-// One CTA per group when the groups outnumber the SMs by at most 2x and the
-// one-tile kernel is used (two CTAs fit an SM); otherwise min(G, SMs) CTAs that
-// each take groups c, c + grid, ...
+// The one-tile kernel (B <= 8) runs two CTAs per SM when the groups outnumber
+// the SMs and the pair of CTAs on an SM takes no more groups than one CTA per SM
+// would: one CTA per group up to 2 x SMs groups, else 2 x SMs CTAs.  Otherwise
+// min(G, SMs) CTAs.  A CTA takes groups c, c + grid, ...
 int mmvq_cta_grid(int G, int B, int num_sms, bool fused_norm, bool* pair) {
-    *pair = !fused_norm && B <= 8 && G > num_sms;
+    const int per_sm = (G + num_sms - 1) / num_sms, per_pair = 2 * ((G + 2 * num_sms - 1) / (2 * num_sms));
+    *pair = !fused_norm && B <= 8 && G > num_sms && per_pair <= per_sm;
     if (*pair) return G < 2 * num_sms ? G : 2 * num_sms;
     return G < num_sms ? G : num_sms;
 }

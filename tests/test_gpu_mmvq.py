@@ -1,8 +1,9 @@
 """Q8_0 mmvq on the GPU against the CPU oracle and against itself across m.
 
 Workload: the isolated-mmvq configuration (4096x4096 and 14336x4096 Q8_0 weights
-times fp16 activations ~N(0,1) at m = 1, 2, 4, 8, 16), plus small shapes that
-span several row groups and k-groups with ragged m."""
+times fp16 activations ~N(0,1) at m = 1, 2, 4, 8, 16), the step's interleaved
+gate|up shape (28672x4096), plus small shapes that span several row groups and
+k-groups with ragged m."""
 import numpy as np
 import pytest
 
@@ -42,7 +43,9 @@ def check_vs_oracle(W, x16, y):
         assert np.all(err <= bound), (r, float((err / bound).max()))
 
 
-@pytest.mark.parametrize("rows,cols", [(4096, 4096), (14336, 4096)])
+# 28672 x 4096 (the interleaved gate|up shape, 896 row groups): at m <= 8 two CTAs
+# per SM walking several groups each, at m = 16 one CTA per SM.
+@pytest.mark.parametrize("rows,cols", [(4096, 4096), (14336, 4096), (28672, 4096)])
 def test_mmvq_config_shapes_row_identity_and_oracle(kdlib, rows, cols):
     kd = kdlib
     W = synth.q8_0_matrix(0, f"mmvq-{rows}x{cols}", rows, cols)
