@@ -13,11 +13,11 @@
 
 namespace kd {
 
-// PAIR: a launch of two CTAs per SM for G > SMs (B <= 8): one CTA per group up
-// to 2 * SMs groups, else 2 * SMs CTAs taking groups c, c + grid, ...  A
-// shallower ring lets two CTAs share an SM: twice the warps to hide the stage
-// pipeline's latency, and for G <= 2 * SMs no CTA waits for a second group
-// while others idle.
+// PAIR: a launch of two CTAs per SM for G > SMs (B <= 8, where it gives no SM
+// more groups than one CTA per SM would): one CTA per group up to 2 * SMs
+// groups, else 2 * SMs CTAs taking groups c, c + grid, ...  A shallower ring
+// lets two CTAs share an SM: twice the warps and more weight bytes in flight
+// per SM for the stage pipeline, which (not HBM) bounds the one-CTA launch.
 // NIN: the RMSNorm fused into the activation load (MmvqArgs::nx): each warp
 // forms its whole k-range of normed tiles once, after the dependency wait, and
 // keeps them for all its groups; the ring then carries weights only.
