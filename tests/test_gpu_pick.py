@@ -12,7 +12,8 @@ Workload: a tiny model with a 32000-entry vocabulary (1000 row groups: the
 stream schedule, as at the 8B shape), B = 1, 5, 8, 12, 16 sessions with
 pre-filled fp16 positions, three fed-back steps each.  Ties: the same model
 with the lm_head's second half a copy of its first, so every logit appears
-twice, 16000 rows apart (in other CTAs); the lower index must win."""
+twice, 16000 rows apart (in other CTAs); the lower index must win.  NaN: a NaN
+in the output norm makes every logit NaN; every pick must be -1."""
 import numpy as np
 import pytest
 
@@ -134,5 +135,34 @@ def test_fused_pick_ties_take_the_lower_index(kdlib, weights):
         for B in (1, 8, 16):
             got = run_and_compare(kd, m, B, sampled=False)
             assert (got < half).all(), got
+    finally:
+        kd.kd_model_free(m)
+
+
+def test_fused_pick_all_nan_rows_give_minus_one(kdlib, weights):
+    """A NaN in the output norm makes every logit NaN: the fused pick, greedy and
+    sampled, returns -1 for every row, as the pick kernels do."""
+    kd = kdlib
+    w = dict(weights)
+    on = w["output_norm"].copy()
+    on[7] = np.float32(np.nan)
+    w["output_norm"] = on
+    B = 5
+    lens = [3 + (7 * b) % 40 for b in range(B)]
+    tok = synth.tokens(0, "pick-nan", B, SHAPE.vocab)
+    m = kd.kd_model_load(kd.make_config(SHAPE, 16, CAP), w)
+    try:
+        ids = bind(kd, m, lens)
+        lg = torch.empty(B, SHAPE.vocab, device="cuda", dtype=torch.float32)
+        out = torch.empty(B, device="cuda", dtype=torch.int32)
+        kd.kd_decode_step(m, ids, tok, lens, lg, out)
+        assert torch.isnan(lg).all()
+        assert (out.cpu().numpy() == -1).all()
+        assert (picks_of(kd, lg, B) == -1).all()
+        params = kd.sample_params([0.7] * B, list(range(B)), [0] * B)
+        kd.kd_decode_step_sampled(m, ids, tok, lens, params, lg, out)
+        assert (out.cpu().numpy() == -1).all()
+        assert (picks_of(kd, lg, B, params) == -1).all()
+        assert kd.kd_device_status(m) == 0
     finally:
         kd.kd_model_free(m)
