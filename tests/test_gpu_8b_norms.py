@@ -149,3 +149,38 @@ def test_8b_fused_step_bitwise_equal_unfused_and_folded_norm(model_norms):
             assert np.array_equal(h0, h1), (flags, step)
             assert np.array_equal(l0, l1), (flags, step)
             assert np.array_equal(t0, t1), (flags, step)  # the pick fused into lm_head vs the pick kernel
+
+
+@pytest.mark.parametrize("cls", ["qkv", "gate_up", "lm_head"])
+def test_8b_bounded_wait_runs_out_and_the_step_recovers(model_norms, cls):
+    """At the 8B shape, B = 8: one bounded wait run out in q|k|v or gate|up (two
+    CTAs per SM; gate|up's CTAs walk several row groups) or in the lm_head with
+    the pick (stream schedule).  The fault is reported once, and the same step
+    run again gives the logit bits and tokens of a clean run."""
+    kd, m, w, prefill = model_norms
+    B, V = 8, SHAPE.vocab
+    tok = synth.tokens(0, "8b-fault", B, V)
+    ids = bind(kd, m, prefill, range(B))
+    lg = torch.empty(B, V, device="cuda", dtype=torch.float32)
+    am = torch.empty(B, device="cuda", dtype=torch.int32)
+
+    def step():
+        kd.kd_decode_step(m, ids, tok, [PREFILL] * B, lg, am)
+        return lg.cpu().numpy().view(np.uint32).copy(), am.cpu().numpy().copy()
+
+    try:
+        ref_l, ref_t = step()
+        assert kd.kd_device_status(m) == 0
+        kd.kd_debug_inject_wait_timeout(m, cls)
+        step()  # the faulted step (its outputs are not valid)
+        with pytest.raises(kd.KdError) as e:
+            kd.kd_device_status(m)
+        assert e.value.name == "KD_ERR_DEVICE"
+        assert kd.kd_device_status(m) == 0  # read and cleared
+        got_l, got_t = step()  # the same positions again
+        assert np.array_equal(got_l, ref_l), cls
+        assert np.array_equal(got_t, ref_t), cls
+        assert kd.kd_device_status(m) == 0
+    finally:
+        for sid in ids:
+            kd.kd_session_free(m, sid)
