@@ -42,16 +42,23 @@ def bind(kd, m, lens):
     return ids
 
 
-def picks_of(kd, lg, B, params=None):
-    """The standalone pick kernels on stored logits."""
-    out = torch.empty(B, dtype=torch.int32, device="cuda")
-    if params is None:
-        ws = torch.zeros(kd.KD_ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
-        kd.kd_argmax(lg, B, SHAPE.vocab, out, ws)
-    else:
-        ws = torch.zeros(kd.KD_SAMPLE_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
-        kd.kd_sample(lg, B, SHAPE.vocab, params, out, ws)
-    return out.cpu().numpy()
+def picks_of(kd, lg, B, sp=None):
+    """The standalone pick kernels on stored logits, 16 rows per call; sp: the
+    rows' (temperatures, seeds, counters) for sampling, or None."""
+    got = []
+    for r0 in range(0, B, 16):
+        r1 = min(B, r0 + 16)
+        out = torch.empty(r1 - r0, dtype=torch.int32, device="cuda")
+        rows = lg[r0:r1].contiguous()
+        if sp is None:
+            ws = torch.zeros(kd.KD_ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+            kd.kd_argmax(rows, r1 - r0, SHAPE.vocab, out, ws)
+        else:
+            ws = torch.zeros(kd.KD_SAMPLE_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+            params = kd.sample_params(*(list(x[r0:r1]) for x in sp))
+            kd.kd_sample(rows, r1 - r0, SHAPE.vocab, params, out, ws)
+        got.append(out.cpu().numpy())
+    return np.concatenate(got)
 
 
 def run_and_compare(kd, m, B, sampled):
@@ -65,9 +72,9 @@ def run_and_compare(kd, m, B, sampled):
         for step in range(3):
             pos = [n + step for n in lens]
             if sampled:
-                params = kd.sample_params(temps, [100 + b for b in range(B)], [step * 7 + b for b in range(B)])
-                kd.kd_decode_step_sampled(m, ids, tok, pos, params, lg, out)
-                want = picks_of(kd, lg, B, params)
+                sp = (temps, [100 + b for b in range(B)], [step * 7 + b for b in range(B)])
+                kd.kd_decode_step_sampled(m, ids, tok, pos, kd.sample_params(*sp), lg, out)
+                want = picks_of(kd, lg, B, sp)
             else:
                 kd.kd_decode_step(m, ids, tok, pos, lg, out)
                 want = picks_of(kd, lg, B)
@@ -159,10 +166,22 @@ def test_fused_pick_all_nan_rows_give_minus_one(kdlib, weights):
         assert torch.isnan(lg).all()
         assert (out.cpu().numpy() == -1).all()
         assert (picks_of(kd, lg, B) == -1).all()
-        params = kd.sample_params([0.7] * B, list(range(B)), [0] * B)
-        kd.kd_decode_step_sampled(m, ids, tok, lens, params, lg, out)
+        sp = ([0.7] * B, list(range(B)), [0] * B)
+        kd.kd_decode_step_sampled(m, ids, tok, lens, kd.sample_params(*sp), lg, out)
         assert (out.cpu().numpy() == -1).all()
-        assert (picks_of(kd, lg, B, params) == -1).all()
+        assert (picks_of(kd, lg, B, sp) == -1).all()
         assert kd.kd_device_status(m) == 0
+    finally:
+        kd.kd_model_free(m)
+
+
+def test_fused_pick_in_groups_of_16(kdlib, weights):
+    """B = 20 runs as groups of 16 and 4 rows: each group's lm_head makes its
+    rows' picks, equal to the pick kernels on the logits the step stored."""
+    kd = kdlib
+    m = kd.kd_model_load(kd.make_config(SHAPE, 24, CAP), weights)
+    try:
+        run_and_compare(kd, m, 20, sampled=False)
+        run_and_compare(kd, m, 20, sampled=True)
     finally:
         kd.kd_model_free(m)
