@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1)
 // warp, whose lanes read whole records (HD/32 dims each, 16- or 8-byte loads)
 // and sum their range in split order, COMB_UNROLL records in flight; the first
 // COMB_UNROLL records of every range are requested before anything else, so that
-// a short session's merge waits for one round of loads.  Each thread reads the
+// a short session's merge waits for one batch of loads.  Each thread reads the
 // (m, l) of splits t, t + 32 NW, ... into shared memory; M is a block max, the
 // weights e^{m_s - M} are formed once per split and the denominator is a fixed
 // tree (each thread summing its splits in order, then the warps' sums in warp

@@ -28,8 +28,8 @@ struct PickLane {
 // The Gumbel words of this lane's four rows (gq + 8k, k < 4) of row group g in
 // column (nt, j) -- entry e takes word e mod 4 of Philox block e / 4.  The four
 // lanes gq = 4h + t (t < 4) of one cq need blocks 8g + 2k + h, k < 4, and word t
-// of each: lane t computes block k = t, and four shuffle rounds transpose the
-// words (in round s lane t reads block (t + s) mod 4 from the lane that made it,
+// of each: lane t computes block k = t, and four shuffle steps transpose the
+// words (in step s lane t reads block (t + s) mod 4 from the lane that made it,
 // which sends its word (k - s) mod 4).  Every lane takes part.  Out of line:
 // only sampled steps call it, and its code stays out of the streaming loop.
 __device__ __noinline__ void pick_words(const PickParams& p, int g, int gq, int lane, uint64_t (&out)[4]) {
@@ -38,7 +38,7 @@ __device__ __noinline__ void pick_words(const PickParams& p, int g, int gq, int 
     philox4x64_10((uint64_t)(8 * g + 2 * t + h), p.ctr, 0, 0, p.seed, 0, w);
 #pragma unroll
     for (int sft = 0; sft < 4; ++sft) {
-        const int q = (t - sft) & 3;  // the word this lane sends in this round
+        const int q = (t - sft) & 3;  // the word this lane sends in this step
         const uint64_t send = q == 0 ? w[0] : q == 1 ? w[1] : q == 2 ? w[2] : w[3];
         const int k = (t + sft) & 3;  // the block this lane receives
         const int src = ((h * 4 + k) << 2) | (lane & 3);
